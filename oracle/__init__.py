@@ -1,0 +1,19 @@
+"""Independent fp64 oracle of the theta-bundle reconstruction linear.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the benchmark's
+CPU-baseline leg, never by the library.
+"""
+from .reconstruction import (  # noqa: F401
+    band_of_layer,
+    bf16_bits_of_value,
+    bf16_ordinal,
+    effective_weight,
+    effective_weight_bf16,
+    error_stats,
+    linear,
+    linear_qkv,
+    ls_residual,
+    ls_scale,
+    round_to_bf16,
+    within_tolerance,
+)
