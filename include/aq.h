@@ -1,0 +1,160 @@
+/*
+ * aq.h -- C ABI of the theta-bundle reconstruction linear on GB300 (sm_103a).
+ *
+ * A theta bundle replaces one projection's dense [out, in] weight by
+ *   W0 [out, in]  a dense block shared by the layers of a projection family,
+ *   s  [out]      a per-output-row scale,
+ *   U  [out, r], V [in, r]  a rank-r delta,
+ * ("How attnquant works", section "The theta bundle"). The projection is rebuilt by
+ * the reconstruction identity y = s . (W0 x) + U (V^T x) and its load-time form
+ * W_eff = diag(s) . W0 + U . V^T ("How attnquant works", "The reconstruction
+ * identity"; "Execution paths", "Precompute-outside: the production path").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor is bfloat16, row-major, with an explicit leading dimension (in
+ *   elements). Orientation follows "Execution paths", "The GEMM formulation":
+ *   x [M, in], y [M, out], W0 [out, in], V [in, r], U [out, r]; s scales y's columns.
+ * - Every tensor pointer is a DEVICE pointer owned by the caller; the library keeps
+ *   no reference after a call returns and allocates no device memory.
+ * - Alignment: pointers 16-byte aligned, every leading dimension a multiple of 8
+ *   elements (rows start on 16-byte boundaries: the kernels move operands with TMA).
+ * - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL is
+ *   the legacy default stream). They return once the work is enqueued. They may be
+ *   captured into CUDA graphs. Kernels are launched with programmatic dependent
+ *   launch so that a call's weight prefetch overlaps the tail of the previous one;
+ *   activations are touched only after the previous kernel in the stream finished.
+ * - Errors: argument errors are detected on the host before anything is enqueued and
+ *   returned as an aq_status; aq_last_error() then describes them (thread-local).
+ *   No C++ exception crosses this interface. Faults detected on the device (a bounded
+ *   wait that expired) are recorded in a per-device status word read by
+ *   aq_device_status().
+ * - Rounding: products accumulate in fp32; each output element is rounded to bf16
+ *   once (nearest-even). t = V^T x is held in bf16 between the two kernels that
+ *   produce and consume it.
+ */
+#ifndef AQ_H_
+#define AQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AQ_ABI_VERSION 1
+
+/* Largest supported rank r. ("Execution paths", "The custom op": a path refuses ranks
+ * beyond what its layout supports and says so; here the limit is 256.) */
+#define AQ_MAX_RANK 256
+
+typedef enum aq_status {
+  AQ_OK = 0,
+  AQ_ERR_INVALID_ARG = 1,  /* NULL pointer where one is required, negative size, bad value */
+  AQ_ERR_SHAPE = 2,        /* out/in/r inconsistent, leading dimension too small, size limits */
+  AQ_ERR_ALIGNMENT = 3,    /* pointer not 16-byte aligned or leading dimension not a multiple of 8 */
+  AQ_ERR_UNSUPPORTED = 4,  /* r > AQ_MAX_RANK, or the current device is not sm_103 */
+  AQ_ERR_WORKSPACE = 5,    /* workspace missing, misaligned or smaller than required */
+  AQ_ERR_OVERLAP = 6,      /* an output buffer overlaps an input buffer */
+  AQ_ERR_CUDA = 7,         /* a CUDA runtime or driver call failed (message in aq_last_error) */
+  AQ_ERR_TIMEOUT = 8       /* device side: a bounded wait inside a kernel expired */
+} aq_status;
+
+/* One projection's theta bundle. All pointers are device pointers to bf16 data.
+ *   W0    [out, in], row stride ld_w0 >= in
+ *   s     [out], contiguous
+ *   U     [out, r], row stride ld_u >= r     (may be NULL iff r == 0)
+ *   V     [in, r],  row stride ld_v >= r     (may be NULL iff r == 0)
+ * r == 0 means U and V are empty and the weight is the scaled shared block alone
+ * ("How attnquant works", "How the decomposition produces s, U, and V").
+ * Limits: 1 <= out, 1 <= in, both < 2^31 and in <= 65536 * 64; 0 <= r <= AQ_MAX_RANK. */
+typedef struct aq_theta {
+  const void* W0;
+  int64_t ld_w0;
+  const void* s;
+  const void* U;
+  int64_t ld_u;
+  const void* V;
+  int64_t ld_v;
+  int32_t out;
+  int32_t in;
+  int32_t r;
+} aq_theta;
+
+/* Bytes of device workspace aq_linear (n_theta == 1) or aq_linear_qkv (n_theta == 3,
+ * pass the three bundles) needs for M tokens. The workspace holds t = V^T x (bf16)
+ * and, for large M, a transposed copy of V. Its contents need no initialisation and
+ * are scratch between calls. Returns 0 if no workspace is needed (r == 0 or M == 0)
+ * and (size_t)-1 for invalid arguments. */
+size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
+
+/* y[m, o] = RN_bf16( s[o] * sum_i W0[o,i] x[m,i] + sum_k U[o,k] * t[m,k] ),
+ *           t[m, k] = sum_i V[i,k] x[m,i]
+ * ("How attnquant works", "The reconstruction identity"; axes as in "Execution paths",
+ * "The GEMM formulation").
+ *   th        the bundle (host pointer to the struct; the struct's pointers are device)
+ *   x         [M, in] device, row stride ldx >= in
+ *   y         [M, out] device, row stride ldy >= out; must not overlap x, W0, s, U, V
+ *   workspace device, >= aq_linear_workspace_bytes(th, 1, M) bytes, 256-byte aligned
+ *             (may be NULL when that size is 0)
+ *   stream    cudaStream_t
+ * M == 0 is a no-op returning AQ_OK. Small M (decode) streams W0 once with a
+ * swap-AB tensor-core kernel; large M (prefill) runs a tcgen05 GEMM; the fused
+ * epilogue applies s and adds the rank-r term in both. */
+aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
+                    void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* The three attention projections of one layer over the same x in one pass
+ * ("Execution paths", "Precompute-outside: the production path" and "The GEMM
+ * formulation": Q/K/V batched into one dispatch). th[0..2] are the q, k and v
+ * bundles (all with the same `in`; out and r may differ); y[j] is [M, th[j].out] with
+ * row stride ldy[j]. Passing y[1] = y[0] + out_q, y[2] = y[1] + out_k and a common
+ * ldy = out_q + out_k + out_v yields the concatenated [M, q|k|v] layout. Outputs must
+ * not overlap each other or any input. workspace: aq_linear_workspace_bytes(th, 3, M). */
+aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t ldx,
+                        void* const y[3], const int64_t ldy[3],
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* W_eff[o, i] = RN_bf16( s[o] * W0[o,i] + sum_k U[o,k] * V[i,k] )
+ * ("Execution paths", "Precompute-outside: the production path": built once per
+ * layer at load). W_eff is [out, in] device, row stride ld_weff >= in, and must not
+ * overlap W0, s, U or V. Needs no workspace. The sum over k accumulates in fp32 on
+ * the tensor cores; s * W0 is exact in fp32; one final rounding. */
+aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream);
+
+/* Synchronises `stream`, then returns the device status word of the current device
+ * (AQ_OK, or AQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last clear)
+ * and clears it. A kernel whose wait expires stops its work (its outputs are then
+ * undefined), releases its tensor memory and exits; the CUDA context stays usable. */
+aq_status aq_device_status(void* stream);
+
+/* Test hook for the bounded-wait path: launches one block that waits on a barrier no
+ * thread ever arrives on, with a limit of timeout_us microseconds (1..1000000). The
+ * wait expires, the block records AQ_ERR_TIMEOUT in the device status word and
+ * exits; aq_device_status() then reports it. No fault, trap or hang is involved. */
+aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
+
+/* Path selection for aq_linear / aq_linear_qkv. AQ_PATH_AUTO picks by M (decode
+ * kernel for M <= aq_decode_max_m(), prefill kernel above). The other values force a
+ * path for tests; both paths are valid for every M. Process-wide setting. */
+typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2 } aq_path;
+aq_status aq_set_path(aq_path path);
+int32_t aq_decode_max_m(void);
+/* Path the last aq_linear / aq_linear_qkv call on this thread took (1 or 2; 0 if none). */
+int32_t aq_last_path(void);
+
+/* Number of kernel launches the last successful aq_* call on this thread enqueued. */
+int32_t aq_last_launch_count(void);
+
+const char* aq_status_string(aq_status status);
+/* Thread-local description of the last error returned on this thread ("" if none). */
+const char* aq_last_error(void);
+int32_t aq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AQ_H_ */

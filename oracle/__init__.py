@@ -15,5 +15,6 @@ from .reconstruction import (  # noqa: F401
     ls_residual,
     ls_scale,
     round_to_bf16,
+    weight_acceptance,
     within_tolerance,
 )

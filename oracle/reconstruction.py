@@ -171,6 +171,33 @@ def bf16_ordinal(bits) -> np.ndarray:
     return np.where(b & 0x8000, -mag, mag)
 
 
+def weight_acceptance(got_bits, W0, s, U, V, unit_roundoff: float = 2.0 ** -23) -> dict:
+    """Element-wise acceptance of a bf16 W_eff computed with fp32 accumulation.
+
+    Bar: within 1 bf16 ulp of RN_bf16(W_eff). Where that ulp is smaller than what any
+    fp32 evaluation can guarantee -- elements where s·W0 and U·Vᵀ nearly cancel -- the
+    element is held instead to the classical error bound of a floating-point dot
+    product of n = r + 1 terms (Higham, "Accuracy and Stability of Numerical
+    Algorithms", sec. 3.1: |fl(Σ a_i) − Σ a_i| <= γ_n Σ |a_i|, γ_n = n·u / (1 − n·u)),
+    taken with u = 2^-23 so that truncating accumulation is covered too, plus half a
+    bf16 ulp for the final rounding. Returns counts and the largest ulp distance.
+    """
+    W0, s, U, V = map(_f64, (W0, s, U, V))
+    exact = effective_weight(W0, s, U, V)
+    ref_bits = bf16_bits_of_value(round_to_bf16(exact))
+    got_bits = np.asarray(got_bits, dtype=np.uint16)
+    ulp = np.abs(bf16_ordinal(got_bits) - bf16_ordinal(ref_bits))
+    got = (got_bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    n = U.shape[1] + 1
+    gamma = n * unit_roundoff / (1.0 - n * unit_roundoff)
+    terms = np.abs(s[:, None] * W0) + np.abs(U) @ np.abs(V).T
+    bound = gamma * terms + np.abs(got) * 2.0 ** -8 + 2.0 ** -133
+    ok = (ulp <= 1) | (np.abs(got - exact) <= bound)
+    return {"elements": int(ulp.size), "within_1ulp": int(np.count_nonzero(ulp <= 1)),
+            "max_ulp": int(ulp.max()) if ulp.size else 0, "all_ok": bool(np.all(ok)),
+            "outside_bound": int(np.count_nonzero(~ok))}
+
+
 def bf16_bits_of_value(v) -> np.ndarray:
     """Bit patterns of doubles that are exactly representable in bf16 (e.g. the
     output of ``round_to_bf16``)."""

@@ -1,1 +1,28 @@
-"""Theta-bundle reconstruction linear for GB300 (sm_103a)."""
+"""Theta-bundle reconstruction linear for GB300 (sm_103a).
+
+y = s * (W0 x) + U (V^T x) and W_eff = diag(s) W0 + U V^T as hand-written CUDA kernels
+behind a C ABI (include/aq.h); this package holds the in-tree build, the ctypes
+binding, the banded-stack bookkeeping and the seeded input generator.
+"""
+from .binding import (  # noqa: F401
+    AQ_ERR_TIMEOUT,
+    AQ_MAX_RANK,
+    AQ_OK,
+    AQ_PATH_AUTO,
+    AQ_PATH_DECODE,
+    AQ_PATH_PREFILL,
+    AqError,
+    Theta,
+    aq_decode_max_m,
+    aq_device_status,
+    aq_last_launch_count,
+    aq_last_path,
+    aq_linear,
+    aq_linear_qkv,
+    aq_linear_workspace_bytes,
+    aq_precompute,
+    aq_selftest_bounded_wait,
+    aq_set_path,
+    load,
+)
+from .stack import StackMismatchError, ThetaStack, band_of  # noqa: F401

@@ -1,0 +1,272 @@
+"""ctypes binding of the C ABI in ``include/aq.h`` (argument marshalling only).
+
+Every function here has the C entry point's name and does nothing but turn torch
+tensors into device pointers, leading dimensions and the current CUDA stream, call the
+library, and turn a non-zero ``aq_status`` into an exception. All arithmetic happens in
+the CUDA kernels of ``libaq_gb300.so``; if that library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+from . import build_lib
+
+AQ_OK = 0
+AQ_ERR_INVALID_ARG = 1
+AQ_ERR_SHAPE = 2
+AQ_ERR_ALIGNMENT = 3
+AQ_ERR_UNSUPPORTED = 4
+AQ_ERR_WORKSPACE = 5
+AQ_ERR_OVERLAP = 6
+AQ_ERR_CUDA = 7
+AQ_ERR_TIMEOUT = 8
+AQ_MAX_RANK = 256
+
+AQ_PATH_AUTO = 0
+AQ_PATH_DECODE = 1
+AQ_PATH_PREFILL = 2
+
+EXPORTED_SYMBOLS = [
+    "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
+    "aq_device_status", "aq_selftest_bounded_wait", "aq_set_path", "aq_decode_max_m",
+    "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
+    "aq_abi_version",
+]
+
+
+class AqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class c_theta(ctypes.Structure):
+    _fields_ = [
+        ("W0", ctypes.c_void_p), ("ld_w0", ctypes.c_int64),
+        ("s", ctypes.c_void_p),
+        ("U", ctypes.c_void_p), ("ld_u", ctypes.c_int64),
+        ("V", ctypes.c_void_p), ("ld_v", ctypes.c_int64),
+        ("out", ctypes.c_int32), ("in_", ctypes.c_int32), ("r", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return build_lib.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libaq_gb300.so (built in-tree by ``build_lib.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with rank_weight_reconstruction_gb300.build_lib.build() "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    th_p = ctypes.POINTER(c_theta)
+    lib.aq_linear_workspace_bytes.argtypes = [th_p, i32, i64]
+    lib.aq_linear_workspace_bytes.restype = sz
+    lib.aq_linear.argtypes = [th_p, vp, i64, i64, vp, i64, vp, sz, vp]
+    lib.aq_linear.restype = ctypes.c_int
+    lib.aq_linear_qkv.argtypes = [th_p, vp, i64, i64, ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
+    lib.aq_linear_qkv.restype = ctypes.c_int
+    lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
+    lib.aq_precompute.restype = ctypes.c_int
+    lib.aq_device_status.argtypes = [vp]
+    lib.aq_device_status.restype = ctypes.c_int
+    lib.aq_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
+    lib.aq_selftest_bounded_wait.restype = ctypes.c_int
+    lib.aq_set_path.argtypes = [ctypes.c_int]
+    lib.aq_set_path.restype = ctypes.c_int
+    for name in ("aq_decode_max_m", "aq_last_path", "aq_last_launch_count", "aq_abi_version"):
+        getattr(lib, name).argtypes = []
+        getattr(lib, name).restype = i32
+    lib.aq_status_string.argtypes = [ctypes.c_int]
+    lib.aq_status_string.restype = ctypes.c_char_p
+    lib.aq_last_error.argtypes = []
+    lib.aq_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _status_name(st: int) -> str:
+    names = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARG", 2: "AQ_ERR_SHAPE", 3: "AQ_ERR_ALIGNMENT",
+             4: "AQ_ERR_UNSUPPORTED", 5: "AQ_ERR_WORKSPACE", 6: "AQ_ERR_OVERLAP", 7: "AQ_ERR_CUDA",
+             8: "AQ_ERR_TIMEOUT"}
+    return names.get(st, f"status {st}")
+
+
+def _check(st: int) -> None:
+    if st != AQ_OK:
+        msg = load().aq_last_error().decode(errors="replace")
+        raise AqError(st, msg)
+
+
+# ----------------------------------------------------------------------------------
+# tensor marshalling
+# ----------------------------------------------------------------------------------
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _ld(t) -> int:
+    """Leading dimension (elements) of a row-major 2-D bf16 tensor or view."""
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"expected a bfloat16 tensor, got {t.dtype}")
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError("expected a 2-D row-major tensor (unit column stride)")
+    return int(t.stride(0)) if t.size(0) > 1 else int(max(t.stride(0), t.size(1)))
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class Theta:
+    """A theta bundle on the device: W0 [out, in], s [out], U [out, r], V [in, r], each a
+    bf16 tensor (views with padded leading dimensions are fine); U, V None when r == 0."""
+    W0: object
+    s: object
+    U: object = None
+    V: object = None
+
+    @property
+    def out(self) -> int:
+        return int(self.W0.size(0))
+
+    @property
+    def inp(self) -> int:
+        return int(self.W0.size(1))
+
+    @property
+    def r(self) -> int:
+        return 0 if self.U is None else int(self.U.size(1))
+
+    def c(self) -> c_theta:
+        r = self.r
+        return c_theta(
+            W0=_ptr(self.W0), ld_w0=_ld(self.W0), s=_ptr(self.s),
+            U=_ptr(self.U) if r else 0, ld_u=_ld(self.U) if r else 0,
+            V=_ptr(self.V) if r else 0, ld_v=_ld(self.V) if r else 0,
+            out=self.out, in_=self.inp, r=r)
+
+
+def aq_linear_workspace_bytes(thetas, M: int) -> int:
+    ths = [thetas] if isinstance(thetas, Theta) else list(thetas)
+    arr = (c_theta * len(ths))(*[t.c() for t in ths])
+    n = load().aq_linear_workspace_bytes(arr, len(ths), int(M))
+    if n == ctypes.c_size_t(-1).value:
+        raise AqError(AQ_ERR_INVALID_ARG, "aq_linear_workspace_bytes: invalid arguments")
+    return int(n)
+
+
+def _padded_empty(rows: int, cols: int, device):
+    """[rows, cols] bf16 view of a buffer whose leading dimension is a multiple of 8
+    (the ABI wants 16-byte aligned rows)."""
+    import torch
+    ld = (cols + 7) // 8 * 8
+    return torch.empty(rows, ld, dtype=torch.bfloat16, device=device)[:, :cols]
+
+
+def _workspace(nbytes: int, device):
+    import torch
+    if nbytes == 0:
+        return None
+    # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def aq_linear(theta: Theta, x, y=None, workspace=None, stream=None):
+    """y = s * (W0 x) + U (V^T x) for x [M, in] -> y [M, out] (bf16)."""
+    import torch
+    M = int(x.size(0))
+    if y is None:
+        y = _padded_empty(M, theta.out, x.device)
+    nbytes = aq_linear_workspace_bytes(theta, M)
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    th = theta.c()
+    _check(load().aq_linear(ctypes.byref(th), _ptr(x), M, _ld(x), _ptr(y), _ld(y), _ptr(workspace),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(),
+                            _stream(stream)))
+    return y
+
+
+def aq_linear_qkv(thetas, x, ys=None, workspace=None, stream=None):
+    """The q, k, v projections over one x in one pass; returns the three outputs."""
+    import torch
+    thetas = list(thetas)
+    assert len(thetas) == 3
+    M = int(x.size(0))
+    if ys is None:
+        ys = [_padded_empty(M, t.out, x.device) for t in thetas]
+    nbytes = aq_linear_workspace_bytes(thetas, M)
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    arr = (c_theta * 3)(*[t.c() for t in thetas])
+    yp = (ctypes.c_void_p * 3)(*[_ptr(y) for y in ys])
+    ldy = (ctypes.c_int64 * 3)(*[_ld(y) for y in ys])
+    _check(load().aq_linear_qkv(arr, _ptr(x), M, _ld(x), yp, ldy, _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
+    return ys
+
+
+def aq_precompute(theta: Theta, W_eff=None, stream=None):
+    """W_eff = diag(s) W0 + U V^T as a bf16 [out, in] tensor."""
+    import torch
+    if W_eff is None:
+        W_eff = _padded_empty(theta.out, theta.inp, theta.W0.device)
+    th = theta.c()
+    _check(load().aq_precompute(ctypes.byref(th), _ptr(W_eff), _ld(W_eff), _stream(stream)))
+    return W_eff
+
+
+def aq_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    return int(load().aq_device_status(_stream(stream)))
+
+
+def aq_selftest_bounded_wait(timeout_us: int, stream=None) -> None:
+    _check(load().aq_selftest_bounded_wait(int(timeout_us), _stream(stream)))
+
+
+def aq_set_path(path: int) -> None:
+    _check(load().aq_set_path(int(path)))
+
+
+def aq_decode_max_m() -> int:
+    return int(load().aq_decode_max_m())
+
+
+def aq_last_path() -> int:
+    return int(load().aq_last_path())
+
+
+def aq_last_launch_count() -> int:
+    return int(load().aq_last_launch_count())
+
+
+def aq_abi_version() -> int:
+    return int(load().aq_abi_version())
+
+
+def aq_last_error() -> str:
+    return load().aq_last_error().decode(errors="replace")
+
+
+def aq_status_string(st: int) -> str:
+    return load().aq_status_string(int(st)).decode()

@@ -1,0 +1,621 @@
+// aq_host.cu -- the C ABI declared in include/aq.h: argument validation, work planning
+// (tile sizes, grid, pipeline depth), TMA descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "aq.h"
+#include "aq_internal.h"
+
+using namespace aq;
+
+namespace {
+
+thread_local std::string t_err;
+thread_local int32_t t_last_path = 0;
+thread_local int32_t t_launches = 0;
+std::atomic<int> g_path{AQ_PATH_AUTO};
+
+constexpr int kDecodeMaxM = 64;                       // swap-AB decode kernel up to this M
+constexpr uint64_t kTimeoutNs = 1000ull * 1000 * 1000;  // limit of one in-kernel wait: 1 s
+constexpr size_t kSmemSlack = 1024;                   // room to align the dynamic smem base
+
+aq_status fail(aq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+aq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(AQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------------
+// per-device facts, queried once
+// ---------------------------------------------------------------------------------
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  size_t smem_optin = 0;
+  int32_t* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+aq_status device_info(DevInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(AQ_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(AQ_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a (GB300)",
+                  dev, major, minor);
+    if ((e = configure_kernels(dev, static_cast<size_t>(smem))))
+      return cuda_fail(e, "cudaFuncSetAttribute");
+    int32_t* st = device_status_ptr(dev, &e);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.sms = sms;
+    d.smem_optin = static_cast<size_t>(smem);
+    d.status = st;
+    d.ready = true;
+  }
+  *out = &d;
+  return AQ_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(aq_status* st) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  *st = fn ? AQ_OK : fail(AQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return fn;
+}
+
+// bf16 matrix [outer, inner] with row stride ld (elements); box {64, box_outer}; 128-byte
+// swizzle; out-of-bounds elements read as zero.
+aq_status tmap_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
+                  int box_outer, const char* what) {
+  aq_status st;
+  EncodeTiledFn fn = encode_fn(&st);
+  if (!fn) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(AQ_ERR_CUDA, "cuTensorMapEncodeTiled(%s: %lld x %lld, ld %lld, box rows %d) failed: %d", what,
+                (long long)outer, (long long)inner, (long long)ld, box_outer, (int)r);
+  return AQ_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bytes spanned by a row-strided bf16 matrix.
+struct Span {
+  uintptr_t base = 0;
+  int64_t rows = 0, cols = 0, ld = 0;
+  const char* name = "";
+  bool empty() const { return base == 0 || rows <= 0 || cols <= 0; }
+  uintptr_t lo() const { return base; }
+  uintptr_t hi() const { return base + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2); }
+};
+
+Span span(const void* p, int64_t rows, int64_t cols, int64_t ld, const char* name) {
+  Span s;
+  s.base = reinterpret_cast<uintptr_t>(p);
+  s.rows = rows;
+  s.cols = cols;
+  s.ld = ld;
+  s.name = name;
+  return s;
+}
+
+// Exact for equal leading dimensions (e.g. q/k/v outputs as column slices of one
+// buffer); conservative otherwise.
+bool overlaps(const Span& a, const Span& b) {
+  if (a.empty() || b.empty()) return false;
+  if (a.hi() <= b.lo() || b.hi() <= a.lo()) return false;
+  if (a.ld != b.ld || a.ld <= 0) return true;
+  const int64_t diff = static_cast<int64_t>(b.base) - static_cast<int64_t>(a.base);
+  if (diff % 2 != 0) return true;
+  const int64_t l = a.ld;
+  const int64_t d = diff / 2;
+  const int64_t c = ((d % l) + l) % l;  // column of b's first element within a's row grid
+  // b covers columns [c, c + b.cols) modulo l; a covers [0, a.cols)
+  if (b.cols >= l || a.cols >= l) return true;
+  auto inter = [](int64_t x0, int64_t x1, int64_t y0, int64_t y1) { return x0 < y1 && y0 < x1; };
+  if (c + b.cols <= l) return inter(c, c + b.cols, 0, a.cols);
+  return inter(c, l, 0, a.cols) || inter(0, c + b.cols - l, 0, a.cols);
+}
+
+aq_status check_theta(const aq_theta* th, const char* who) {
+  if (!th) return fail(AQ_ERR_INVALID_ARG, "%s: theta is NULL", who);
+  if (!th->W0 || !th->s) return fail(AQ_ERR_INVALID_ARG, "%s: W0 and s must be non-NULL", who);
+  if (th->out < 1 || th->in < 1) return fail(AQ_ERR_SHAPE, "%s: out=%d in=%d must be >= 1", who, th->out, th->in);
+  if (th->in > 65536 * 64) return fail(AQ_ERR_SHAPE, "%s: in=%d exceeds the supported maximum", who, th->in);
+  if (th->r < 0) return fail(AQ_ERR_SHAPE, "%s: r=%d is negative", who, th->r);
+  if (th->r > AQ_MAX_RANK)
+    return fail(AQ_ERR_UNSUPPORTED, "%s: r=%d exceeds AQ_MAX_RANK=%d", who, th->r, AQ_MAX_RANK);
+  if (th->ld_w0 < th->in) return fail(AQ_ERR_SHAPE, "%s: ld_w0=%lld < in=%d", who, (long long)th->ld_w0, th->in);
+  if (!aligned16(th->W0) || !aligned16(th->s) || th->ld_w0 % 8 != 0)
+    return fail(AQ_ERR_ALIGNMENT, "%s: W0/s must be 16-byte aligned and ld_w0 a multiple of 8", who);
+  if (th->r > 0) {
+    if (!th->U || !th->V) return fail(AQ_ERR_INVALID_ARG, "%s: U and V must be non-NULL when r=%d > 0", who, th->r);
+    if (th->ld_u < th->r || th->ld_v < th->r)
+      return fail(AQ_ERR_SHAPE, "%s: ld_u=%lld / ld_v=%lld must be >= r=%d", who, (long long)th->ld_u,
+                  (long long)th->ld_v, th->r);
+    if (!aligned16(th->U) || !aligned16(th->V) || th->ld_u % 8 != 0 || th->ld_v % 8 != 0)
+      return fail(AQ_ERR_ALIGNMENT, "%s: U/V must be 16-byte aligned and ld_u, ld_v multiples of 8", who);
+  }
+  return AQ_OK;
+}
+
+void theta_spans(const aq_theta* th, Span* out4) {
+  out4[0] = span(th->W0, th->out, th->in, th->ld_w0, "W0");
+  out4[1] = span(th->s, 1, th->out, th->out, "s");
+  out4[2] = span(th->r > 0 ? th->U : nullptr, th->out, th->r, th->ld_u, "U");
+  out4[3] = span(th->r > 0 ? th->V : nullptr, th->in, th->r, th->ld_v, "V");
+}
+
+// ---------------------------------------------------------------------------------
+// workspace layout of aq_linear / aq_linear_qkv
+// ---------------------------------------------------------------------------------
+struct WsLayout {
+  int64_t ld_t = 0;            // row stride of t [M, sum r_pad]
+  int64_t t_col[kMaxSeg] = {};  // column offset of family j in t
+  size_t t_bytes = 0;
+  size_t vt_off[kMaxSeg] = {};  // byte offset of V^T of family j
+  int64_t ldvt = 0;
+  size_t total = 0;
+  bool any_r = false;
+  bool use_vt = false;
+};
+
+WsLayout ws_layout(const aq_theta* const* th, int n, int64_t M) {
+  WsLayout w;
+  for (int j = 0; j < n; ++j) {
+    w.t_col[j] = w.ld_t;
+    if (th[j]->r > 0) {
+      w.any_r = true;
+      w.ld_t += round_up(th[j]->r, 8);
+    }
+  }
+  if (!w.any_r || M <= 0) return w;
+  w.t_bytes = static_cast<size_t>(round_up(M * w.ld_t * 2, 256));
+  w.total = w.t_bytes;
+  w.use_vt = M > kDecodeMaxM;
+  if (w.use_vt) {
+    w.ldvt = round_up(th[0]->in, 8);
+    for (int j = 0; j < n; ++j) {
+      w.vt_off[j] = w.total;
+      if (th[j]->r > 0) w.total += static_cast<size_t>(round_up(static_cast<int64_t>(th[j]->r) * w.ldvt * 2, 256));
+    }
+  }
+  return w;
+}
+
+// ---------------------------------------------------------------------------------
+// planners
+// ---------------------------------------------------------------------------------
+uint32_t tmem_cols_for(int n) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(n)) c <<= 1;
+  return c;
+}
+
+// Decode kernels leave room on each SM for the small-M down-projection kernel that runs
+// just before them (about 44 KB of shared memory), so both can be resident together.
+constexpr size_t kDecodeSmemBudget = 176 * 1024;
+
+int stages_for(uint32_t stage_bytes, size_t smem_cap, size_t fixed) {
+  const size_t budget = std::min<size_t>(smem_cap, 227 * 1024) - fixed;
+  int st = static_cast<int>(budget / stage_bytes);
+  return std::max(2, std::min(st, kMaxStages));
+}
+
+// Balanced rows per tile for the decode kernel: about one tile per SM (or a small whole
+// number per SM) with at most 128 rows each.
+int decode_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int sms) {
+  int64_t rows = 0;
+  for (int j = 0; j < n; ++j) rows += th[j]->out;
+  for (int64_t w = 1;; ++w) {
+    const int64_t R = std::max<int64_t>(1, ceil_div(rows * n_tok_tiles, w * sms));
+    if (R <= kMmaM) return static_cast<int>(R);
+  }
+}
+
+// Prefill N tile: minimise (waves x tile width + per-tile overhead).
+int prefill_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int sms) {
+  static const int cand[] = {256, 224, 192, 160, 128, 112, 96, 80, 64, 48, 32, 16};
+  int best = 256;
+  double best_cost = 1e300;
+  for (int bn : cand) {
+    int64_t tiles = 0;
+    for (int j = 0; j < n; ++j) tiles += n_tok_tiles * ceil_div(th[j]->out, bn);
+    const double cost = static_cast<double>(ceil_div(tiles, sms)) * (bn + 32);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+aq_status launch_or_fail(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  ++t_launches;
+  return AQ_OK;
+}
+
+aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M, int64_t ldx,
+                      void* const* ys, const int64_t* ldys, void* ws, size_t ws_bytes, void* stream) {
+  const char* who = n == 1 ? "aq_linear" : "aq_linear_qkv";
+  t_launches = 0;
+  for (int j = 0; j < n; ++j) {
+    aq_status st = check_theta(th[j], who);
+    if (st != AQ_OK) return st;
+    if (th[j]->in != th[0]->in)
+      return fail(AQ_ERR_SHAPE, "%s: family %d has in=%d but family 0 has in=%d", who, j, th[j]->in, th[0]->in);
+  }
+  const int K = th[0]->in;
+  if (M < 0) return fail(AQ_ERR_SHAPE, "%s: M=%lld is negative", who, (long long)M);
+  if (M > (int64_t(1) << 31) - 1) return fail(AQ_ERR_SHAPE, "%s: M=%lld is too large", who, (long long)M);
+  if (M == 0) return AQ_OK;
+  if (!x) return fail(AQ_ERR_INVALID_ARG, "%s: x is NULL", who);
+  if (ldx < K || ldx % 8 != 0 || !aligned16(x))
+    return fail(ldx < K ? AQ_ERR_SHAPE : AQ_ERR_ALIGNMENT, "%s: x must be 16-byte aligned with ldx (%lld) >= in and a multiple of 8",
+                who, (long long)ldx);
+  for (int j = 0; j < n; ++j) {
+    if (!ys[j]) return fail(AQ_ERR_INVALID_ARG, "%s: output %d is NULL", who, j);
+    if (ldys[j] < th[j]->out) return fail(AQ_ERR_SHAPE, "%s: ldy of output %d (%lld) < out=%d", who, j, (long long)ldys[j], th[j]->out);
+    if (ldys[j] % 8 != 0 || !aligned16(ys[j]))
+      return fail(AQ_ERR_ALIGNMENT, "%s: output %d must be 16-byte aligned with ldy a multiple of 8", who, j);
+  }
+  const WsLayout wl = ws_layout(th, n, M);
+  if (wl.total > 0) {
+    if (!ws) return fail(AQ_ERR_WORKSPACE, "%s: workspace of %zu bytes required, got NULL", who, wl.total);
+    if (ws_bytes < wl.total) return fail(AQ_ERR_WORKSPACE, "%s: workspace of %zu bytes required, got %zu", who, wl.total, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(AQ_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", who);
+  }
+  // overlap checks
+  {
+    Span ins[1 + 4 * kMaxSeg];
+    int ni = 0;
+    ins[ni++] = span(x, M, K, ldx, "x");
+    for (int j = 0; j < n; ++j) {
+      theta_spans(th[j], ins + ni);
+      ni += 4;
+    }
+    Span wsp = span(wl.total ? ws : nullptr, 1, static_cast<int64_t>(wl.total / 2), static_cast<int64_t>(wl.total / 2), "workspace");
+    for (int j = 0; j < n; ++j) {
+      Span yj = span(ys[j], M, th[j]->out, ldys[j], "y");
+      for (int i = 0; i < ni; ++i)
+        if (overlaps(yj, ins[i])) return fail(AQ_ERR_OVERLAP, "%s: output %d overlaps input %s", who, j, ins[i].name);
+      if (overlaps(yj, wsp)) return fail(AQ_ERR_OVERLAP, "%s: output %d overlaps the workspace", who, j);
+      for (int k = 0; k < j; ++k)
+        if (overlaps(yj, span(ys[k], M, th[k]->out, ldys[k], "y")))
+          return fail(AQ_ERR_OVERLAP, "%s: outputs %d and %d overlap", who, k, j);
+    }
+    for (int i = 0; i < ni; ++i)
+      if (overlaps(wsp, ins[i])) return fail(AQ_ERR_OVERLAP, "%s: the workspace overlaps input %s", who, ins[i].name);
+  }
+
+  DevInfo* dev = nullptr;
+  aq_status st = device_info(&dev);
+  if (st != AQ_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int path_cfg = g_path.load();
+  const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint16_t* tbuf = reinterpret_cast<uint16_t*>(wsb);
+
+  // ---- t = V^T x for every family with r > 0 ----
+  if (wl.any_r) {
+    if (!wl.use_vt) {
+      DownParams dp = {};
+      dp.x = static_cast<const uint16_t*>(x);
+      dp.ldx = ldx;
+      dp.ldt = wl.ld_t;
+      dp.M = static_cast<int32_t>(M);
+      dp.K = K;
+      dp.mgroups = static_cast<int32_t>(ceil_div(M, 16));
+      int csize = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, ceil_div(K, 256))));
+      dp.kslice = static_cast<int32_t>(round_up(ceil_div(K, csize), 8));
+      dp.csize = static_cast<int32_t>(ceil_div(K, dp.kslice));
+      int by = 0;
+      for (int j = 0; j < n; ++j) {
+        if (th[j]->r == 0) continue;
+        DownSeg& s = dp.seg[dp.nseg++];
+        s.V = static_cast<const uint16_t*>(th[j]->V);
+        s.ldv = th[j]->ld_v;
+        s.r = th[j]->r;
+        s.t = tbuf + wl.t_col[j];
+        s.kchunks = static_cast<int32_t>(ceil_div(th[j]->r, 32));
+        s.block_begin = by;
+        by += s.kchunks;
+      }
+      if ((st = launch_or_fail(launch_down(dp, by, cs, true), "launch t = V^T x (small M)")) != AQ_OK) return st;
+    } else {
+      TransposeParams tp = {};
+      tp.K = K;
+      int max_r = 0;
+      for (int j = 0; j < n; ++j) {
+        if (th[j]->r == 0) continue;
+        TransposeSeg& s = tp.seg[tp.nseg++];
+        s.V = static_cast<const uint16_t*>(th[j]->V);
+        s.ldv = th[j]->ld_v;
+        s.Vt = reinterpret_cast<uint16_t*>(wsb + wl.vt_off[j]);
+        s.ldvt = wl.ldvt;
+        s.r = th[j]->r;
+        max_r = std::max(max_r, th[j]->r);
+      }
+      if ((st = launch_or_fail(launch_transpose(tp, max_r, cs, true), "launch V transpose")) != AQ_OK) return st;
+      // t GEMM: tokens x V^T, normal orientation, plain bf16 epilogue into the workspace
+      GemmParams gp = {};
+      gp.M = static_cast<int32_t>(M);
+      gp.K = K;
+      gp.tok_tile = kMmaM;
+      gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+      int rt = 16;
+      for (int j = 0; j < n; ++j) rt = std::max<int>(rt, static_cast<int>(round_up(th[j]->r, 16)));
+      gp.row_tile = rt;
+      gp.n_mma = rt;
+      if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, kMmaM, "x")) != AQ_OK) return st;
+      int tiles = 0;
+      for (int j = 0; j < n; ++j) {
+        if (th[j]->r == 0) continue;
+        GemmSeg& s = gp.seg[gp.nseg++];
+        if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, rt, "V^T")) != AQ_OK) return st;
+        s.s = nullptr;
+        s.y = tbuf + wl.t_col[j];
+        s.ldy = wl.ld_t;
+        s.rows = th[j]->r;
+        s.r = 0;
+        s.n_row_tiles = 1;
+        s.tile_begin = tiles;
+        tiles += gp.n_tok_tiles;
+      }
+      gp.total_tiles = tiles;
+      gp.prefetch_w = 0;  // V^T comes from the transpose kernel just before
+      gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
+      gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
+      gp.tmem_cols = tmem_cols_for(gp.n_mma);
+      gp.status = dev->status;
+      gp.timeout_ns = kTimeoutNs;
+      const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+      const int grid = std::min(tiles, dev->sms);
+      if ((st = launch_or_fail(launch_gemm(gp, false, grid, smem, cs, true), "launch t GEMM")) != AQ_OK) return st;
+    }
+  }
+
+  // ---- main GEMM with the fused reconstruction epilogue ----
+  GemmParams gp = {};
+  gp.M = static_cast<int32_t>(M);
+  gp.K = K;
+  if (decode) {
+    gp.tok_tile = static_cast<int32_t>(std::min<int64_t>(256, round_up(M, 16)));
+    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, gp.tok_tile));
+    gp.row_tile = decode_row_tile(th, n, gp.n_tok_tiles, dev->sms);
+    gp.n_mma = gp.tok_tile;
+  } else {
+    gp.tok_tile = kMmaM;
+    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+    gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
+    gp.n_mma = gp.row_tile;
+  }
+  if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, gp.tok_tile, "x")) != AQ_OK) return st;
+  int tiles = 0;
+  bool any_lr = false;
+  for (int j = 0; j < n; ++j) {
+    GemmSeg& s = gp.seg[gp.nseg++];
+    if ((st = tmap_2d(&s.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, gp.row_tile, "W0")) != AQ_OK) return st;
+    if (th[j]->r > 0) {
+      any_lr = true;
+      if ((st = tmap_2d(&s.tm_u, th[j]->U, th[j]->r, th[j]->out, th[j]->ld_u, gp.row_tile, "U")) != AQ_OK) return st;
+      if ((st = tmap_2d(&s.tm_t, tbuf + wl.t_col[j], th[j]->r, M, wl.ld_t, gp.tok_tile, "t")) != AQ_OK) return st;
+    }
+    s.s = static_cast<const uint16_t*>(th[j]->s);
+    s.y = static_cast<uint16_t*>(ys[j]);
+    s.ldy = ldys[j];
+    s.rows = th[j]->out;
+    s.r = th[j]->r;
+    s.n_row_tiles = static_cast<int32_t>(ceil_div(th[j]->out, gp.row_tile));
+    s.tile_begin = tiles;
+    tiles += s.n_row_tiles * gp.n_tok_tiles;
+  }
+  gp.total_tiles = tiles;
+  gp.prefetch_w = 1;
+  gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
+  gp.stages = stages_for(gp.stage_bytes, decode ? std::min(dev->smem_optin, kDecodeSmemBudget) : dev->smem_optin,
+                         kHeaderBytes + kSmemSlack);
+  gp.tmem_cols = tmem_cols_for(any_lr ? 2 * gp.n_mma : gp.n_mma);
+  gp.status = dev->status;
+  gp.timeout_ns = kTimeoutNs;
+  const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+  const int grid = std::min(tiles, dev->sms);
+  if ((st = launch_or_fail(launch_gemm(gp, decode, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK)
+    return st;
+  t_last_path = decode ? AQ_PATH_DECODE : AQ_PATH_PREFILL;
+  return AQ_OK;
+}
+
+}  // namespace
+
+// =====================================================================================
+// exported C ABI
+// =====================================================================================
+extern "C" {
+
+size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M) {
+  if (!th || (n_theta != 1 && n_theta != 3) || M < 0) return static_cast<size_t>(-1);
+  const aq_theta* ptrs[kMaxSeg];
+  for (int j = 0; j < n_theta; ++j) {
+    if (th[j].r < 0 || th[j].r > AQ_MAX_RANK || th[j].in < 1) return static_cast<size_t>(-1);
+    ptrs[j] = &th[j];
+  }
+  return ws_layout(ptrs, n_theta, M).total;
+}
+
+aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y, int64_t ldy,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!th) return fail(AQ_ERR_INVALID_ARG, "aq_linear: theta is NULL");
+  const aq_theta* ptrs[1] = {th};
+  void* ys[1] = {y};
+  int64_t lds[1] = {ldy};
+  return linear_impl(ptrs, 1, x, M, ldx, ys, lds, workspace, workspace_bytes, stream);
+}
+
+aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t ldx, void* const y[3],
+                        const int64_t ldy[3], void* workspace, size_t workspace_bytes, void* stream) {
+  if (!th || !y || !ldy) return fail(AQ_ERR_INVALID_ARG, "aq_linear_qkv: NULL array argument");
+  const aq_theta* ptrs[3] = {&th[0], &th[1], &th[2]};
+  return linear_impl(ptrs, 3, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
+}
+
+aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream) {
+  t_launches = 0;
+  aq_status st = check_theta(th, "aq_precompute");
+  if (st != AQ_OK) return st;
+  if (!W_eff) return fail(AQ_ERR_INVALID_ARG, "aq_precompute: W_eff is NULL");
+  if (ld_weff < th->in) return fail(AQ_ERR_SHAPE, "aq_precompute: ld_weff=%lld < in=%d", (long long)ld_weff, th->in);
+  if (ld_weff % 8 != 0 || !aligned16(W_eff))
+    return fail(AQ_ERR_ALIGNMENT, "aq_precompute: W_eff must be 16-byte aligned with ld_weff a multiple of 8");
+  {
+    Span ins[4];
+    theta_spans(th, ins);
+    Span we = span(W_eff, th->out, th->in, ld_weff, "W_eff");
+    for (int i = 0; i < 4; ++i)
+      if (overlaps(we, ins[i])) return fail(AQ_ERR_OVERLAP, "aq_precompute: W_eff overlaps %s", ins[i].name);
+  }
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != AQ_OK) return st;
+  PrecomputeParams pp = {};
+  pp.out = th->out;
+  pp.in = th->in;
+  pp.r = th->r;
+  pp.bn = 128;
+  pp.s = static_cast<const uint16_t*>(th->s);
+  pp.n_row_tiles = static_cast<int32_t>(ceil_div(th->out, kMmaM));
+  pp.n_col_tiles = static_cast<int32_t>(ceil_div(th->in, pp.bn));
+  pp.total_tiles = pp.n_row_tiles * pp.n_col_tiles;
+  if ((st = tmap_2d(&pp.tm_w0, th->W0, th->in, th->out, th->ld_w0, kMmaM, "W0")) != AQ_OK) return st;
+  if ((st = tmap_2d(&pp.tm_we, W_eff, th->in, th->out, ld_weff, kMmaM, "W_eff")) != AQ_OK) return st;
+  if (th->r > 0) {
+    if ((st = tmap_2d(&pp.tm_u, th->U, th->r, th->out, th->ld_u, kMmaM, "U")) != AQ_OK) return st;
+    if ((st = tmap_2d(&pp.tm_v, th->V, th->r, th->in, th->ld_v, pp.bn, "V")) != AQ_OK) return st;
+  }
+  pp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + pp.bn * 128, 1024));
+  pp.stages = 3;
+  pp.tmem_cols = th->r > 0 ? tmem_cols_for(2 * pp.bn) : 32;
+  pp.status = dev->status;
+  pp.timeout_ns = kTimeoutNs;
+  const size_t smem = kSmemSlack + kHeaderBytes + 3u * static_cast<size_t>(pp.bn) * 256u +
+                      static_cast<size_t>(pp.stages) * pp.stage_bytes;
+  if (smem > dev->smem_optin) return fail(AQ_ERR_UNSUPPORTED, "aq_precompute: needs %zu bytes of shared memory", smem);
+  const int grid = std::min(pp.total_tiles, dev->sms);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return launch_or_fail(launch_precompute(pp, grid, smem, cs, true), "launch precompute");
+}
+
+aq_status aq_device_status(void* stream) {
+  DevInfo* dev = nullptr;
+  aq_status st = device_info(&dev);
+  if (st != AQ_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int32_t v = 0;
+  if ((e = cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read device status");
+  if ((e = cudaMemset(dev->status, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "clear device status");
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (v == AQ_OK) return AQ_OK;
+  if (v == AQ_ERR_TIMEOUT) return fail(AQ_ERR_TIMEOUT, "a bounded wait inside a kernel expired");
+  return fail(AQ_ERR_CUDA, "unexpected device status %d", v);
+}
+
+aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000)
+    return fail(AQ_ERR_INVALID_ARG, "aq_selftest_bounded_wait: timeout_us=%u outside [1, 1000000]", timeout_us);
+  DevInfo* dev = nullptr;
+  aq_status st = device_info(&dev);
+  if (st != AQ_OK) return st;
+  t_launches = 0;
+  return launch_or_fail(launch_bounded_wait_selftest(dev->status, uint64_t(timeout_us) * 1000u,
+                                                     static_cast<cudaStream_t>(stream)),
+                        "launch bounded-wait self test");
+}
+
+aq_status aq_set_path(aq_path path) {
+  if (path != AQ_PATH_AUTO && path != AQ_PATH_DECODE && path != AQ_PATH_PREFILL)
+    return fail(AQ_ERR_INVALID_ARG, "aq_set_path: unknown path %d", (int)path);
+  g_path.store(path);
+  return AQ_OK;
+}
+
+int32_t aq_decode_max_m(void) { return kDecodeMaxM; }
+int32_t aq_last_path(void) { return t_last_path; }
+int32_t aq_last_launch_count(void) { return t_launches; }
+int32_t aq_abi_version(void) { return AQ_ABI_VERSION; }
+
+const char* aq_status_string(aq_status s) {
+  switch (s) {
+    case AQ_OK: return "AQ_OK";
+    case AQ_ERR_INVALID_ARG: return "AQ_ERR_INVALID_ARG";
+    case AQ_ERR_SHAPE: return "AQ_ERR_SHAPE";
+    case AQ_ERR_ALIGNMENT: return "AQ_ERR_ALIGNMENT";
+    case AQ_ERR_UNSUPPORTED: return "AQ_ERR_UNSUPPORTED";
+    case AQ_ERR_WORKSPACE: return "AQ_ERR_WORKSPACE";
+    case AQ_ERR_OVERLAP: return "AQ_ERR_OVERLAP";
+    case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
+    case AQ_ERR_TIMEOUT: return "AQ_ERR_TIMEOUT";
+  }
+  return "AQ_ERR_UNKNOWN";
+}
+
+const char* aq_last_error(void) { return t_err.c_str(); }
+
+}  // extern "C"

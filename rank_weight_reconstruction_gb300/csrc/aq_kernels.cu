@@ -1,0 +1,799 @@
+// aq_kernels.cu -- sm_103a kernels of the theta-bundle reconstruction linear
+//   y = s . (W0 x) + U (V^T x)         ("How attnquant works", "The reconstruction identity")
+//   W_eff = diag(s) W0 + U V^T         ("Execution paths", "Precompute-outside")
+//
+// aq_gemm_kernel<swap>   tcgen05 GEMM over the K = in loop with TMA-fed shared-memory ring;
+//                        the rank-r up-projection runs as extra K blocks into a second TMEM
+//                        accumulator and the epilogue forms s * D_main + D_low, rounded once.
+//                        swap = true (decode): output rows are the 128 accumulator lanes and
+//                        tokens the N dimension, each CTA owning a balanced slice of rows.
+//                        swap = false (prefill): 128 tokens per tile, output rows as N.
+// aq_down_kernel         t = V^T x for small M on CUDA cores; a thread-block cluster splits
+//                        `in` and reduces the partial sums through distributed shared memory.
+// aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
+// aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
+//                        epilogue, W_eff written back with TMA stores.
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "aq_internal.h"
+#include "aq_ptx.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace aq {
+
+__device__ int32_t g_device_status;  // AQ_OK or AQ_ERR_TIMEOUT, one word per device
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Wait without honouring the abort flag (used to drain in-flight asynchronous work after
+// an abort); bounded by its own limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+constexpr uint64_t kDrainNs = 20ull * 1000 * 1000;  // 20 ms per drained barrier
+
+// Every lane waits; the outcome is made warp-uniform so that warp-collective tcgen05
+// instructions after it are always executed by the whole warp or by none of it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const AbortCtl& ctl) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
+}
+
+// ------------------------------------------------------------------------------------
+// GEMM with fused reconstruction epilogue
+// ------------------------------------------------------------------------------------
+struct TileCoord {
+  int seg;
+  int row0;
+  int tok0;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
+  int si = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxSeg; ++j)
+    if (j < p.nseg && tile >= p.seg[j].tile_begin) si = j;
+  const int local = tile - p.seg[si].tile_begin;
+  TileCoord c;
+  c.seg = si;
+  c.tok0 = (local % p.n_tok_tiles) * p.tok_tile;
+  c.row0 = (local / p.n_tok_tiles) * p.row_tile;
+  return c;
+}
+
+template <bool kSwap>
+__global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tmem_full = empty + kMaxStages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* mma_done = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint8_t* ring = smem + kHeaderBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4 * 32);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_x);
+    for (int j = 0; j < p.nseg; ++j) {
+      tma_prefetch_desc(&p.seg[j].tm_w);
+      if (p.seg[j].r > 0) {
+        tma_prefetch_desc(&p.seg[j].tm_u);
+        tma_prefetch_desc(&p.seg[j].tm_t);
+      }
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  // The next kernel in the stream may now be scheduled and start its own weight
+  // prefetch; it touches activations only after this grid has completed.
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nkb_main = ceil_div_i(p.K, kBK);
+  const uint32_t tx_bytes = static_cast<uint32_t>(p.row_tile + p.tok_tile) * 128u;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, fill_par = 0;
+      bool ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+        const TileCoord tc = tile_coord(p, tile);
+        const GemmSeg& sg = p.seg[tc.seg];
+        const int nkb = nkb_main + (sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0);
+        int kb = 0;
+        if (it == 0 && !p.prefetch_w) pdl_wait_prior_grid();
+        if (it == 0 && p.prefetch_w) {
+          // Weight tiles of the first stages go out before waiting on the previous grid.
+          const int pre = nkb_main < p.stages ? nkb_main : p.stages;
+          for (; kb < pre; ++kb) {
+            uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
+            mbar_arrive_expect_tx(&full[kb], tx_bytes);
+            if (kSwap) tma_load_2d(st, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
+            else tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
+            filled |= 1u << kb;
+          }
+          pdl_wait_prior_grid();
+          for (int j = 0; j < pre; ++j) {
+            uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
+            if (kSwap) tma_load_2d(st + kStageA, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
+            else tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
+          }
+          stage = pre;
+          if (stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        for (; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], tx_bytes);
+          const CUtensorMap* ma;
+          const CUtensorMap* mb;
+          int ka, ra, rb;
+          if (kb < nkb_main) {
+            ka = kb * kBK;
+            ma = kSwap ? &sg.tm_w : &p.tm_x;
+            mb = kSwap ? &p.tm_x : &sg.tm_w;
+          } else {
+            ka = (kb - nkb_main) * kBK;
+            ma = kSwap ? &sg.tm_u : &sg.tm_t;
+            mb = kSwap ? &sg.tm_t : &sg.tm_u;
+          }
+          ra = kSwap ? tc.row0 : tc.tok0;
+          rb = kSwap ? tc.tok0 : tc.row0;
+          tma_load_2d(st, ma, ka, ra, &full[stage], pol);
+          tma_load_2d(st + kStageA, mb, ka, rb, &full[stage], pol);
+          filled |= 1u << stage;
+          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before the CTA can exit.
+        for (int s = 0; s < p.stages; ++s)
+          if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_par >> s) & 1u, kDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = idesc_bf16_f32(kMmaM, p.n_mma);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    // Start the bounded waits only once the previous grid is done, so that a long
+    // predecessor cannot be mistaken for a stalled pipeline.
+    pdl_wait_prior_grid();
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord(p, tile);
+      const GemmSeg& sg = p.seg[tc.seg];
+      const int nkb = nkb_main + (sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0);
+      if (!warp_wait(tmem_empty, (it & 1) ^ 1, ctl)) break;
+      tc_fence_after();
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!warp_wait(&full[stage], phase, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const bool low = kb >= nkb_main;
+          const int kb_local = low ? kb - nkb_main : kb;
+          const uint32_t d = tmem_base + (low ? static_cast<uint32_t>(p.n_mma) : 0u);
+          const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t b_addr = a_addr + kStageA;
+          int nk = kBK / kUmmaK;
+          if (low) {
+            const int rem = sg.r - kb_local * kBK;
+            nk = rem >= kBK ? nk : ceil_div_i(rem, kUmmaK);
+          }
+          for (int j = 0; j < nk; ++j) {
+            tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc,
+                        (kb_local > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok && lane == 0) tc_commit(tmem_full);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      tc_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: warps 2..5, one TMEM lane quadrant each ----------------
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    pdl_wait_prior_grid();
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord(p, tile);
+      const GemmSeg& sg = p.seg[tc.seg];
+      const bool has_lr = sg.r > 0;
+      if (!warp_wait(tmem_full, it & 1, ctl)) break;
+      tc_fence_after();
+      if (kSwap) {
+        const int row = tc.row0 + lrow;
+        const bool row_ok = lrow < p.row_tile && row < sg.rows;
+        const float sc = (row_ok && sg.s != nullptr) ? bf16_to_f32(sg.s[row]) : 1.0f;
+        for (int c = 0; c < p.n_mma; c += 16) {
+          float a[16], b[16];
+          tmem_ld_16(t_lane + c, a);
+          if (has_lr) tmem_ld_16(t_lane + p.n_mma + c, b);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = tc.tok0 + c + j;
+              if (c + j < p.tok_tile && tok < p.M) {
+                const float v = fmaf(sc, a[j], has_lr ? b[j] : 0.0f);
+                sg.y[static_cast<int64_t>(tok) * sg.ldy + row] = f32_to_bf16_rn(v);
+              }
+            }
+          }
+        }
+      } else {
+        const int tok = tc.tok0 + lrow;
+        const bool tok_ok = tok < p.M;
+        uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
+        for (int c = 0; c < p.n_mma; c += 16) {
+          float a[16], b[16];
+          tmem_ld_16(t_lane + c, a);
+          if (has_lr) tmem_ld_16(t_lane + p.n_mma + c, b);
+          tmem_ld_wait();
+          const int o0 = tc.row0 + c;
+          if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
+          float sc[16];
+          const bool full_chunk = (c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows);
+          if (sg.s == nullptr) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sc[j] = 1.0f;
+          } else if (full_chunk) {
+            const uint4 s0 = __ldg(reinterpret_cast<const uint4*>(sg.s + o0));
+            const uint4 s1 = __ldg(reinterpret_cast<const uint4*>(sg.s + o0 + 8));
+            const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              sc[2 * j] = __uint_as_float(sw[j] << 16);
+              sc[2 * j + 1] = __uint_as_float(sw[j] & 0xFFFF0000u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              sc[j] = (c + j < p.row_tile && o0 + j < sg.rows) ? bf16_to_f32(sg.s[o0 + j]) : 0.0f;
+          }
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = fmaf(sc[j], a[j], has_lr ? b[j] : 0.0f);
+          if (full_chunk) {
+            uint4 w0, w1;
+            w0.x = pack_bf16x2(v[0], v[1]);
+            w0.y = pack_bf16x2(v[2], v[3]);
+            w0.z = pack_bf16x2(v[4], v[5]);
+            w0.w = pack_bf16x2(v[6], v[7]);
+            w1.x = pack_bf16x2(v[8], v[9]);
+            w1.y = pack_bf16x2(v[10], v[11]);
+            w1.z = pack_bf16x2(v[12], v[13]);
+            w1.w = pack_bf16x2(v[14], v[15]);
+            *reinterpret_cast<uint4*>(yrow + o0) = w0;
+            *reinterpret_cast<uint4*>(yrow + o0 + 8) = w1;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < p.row_tile && o0 + j < sg.rows) yrow[o0 + j] = f32_to_bf16_rn(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+}
+
+// ------------------------------------------------------------------------------------
+// t = V^T x for small M (CUDA cores, cluster reduction over `in`)
+// ------------------------------------------------------------------------------------
+constexpr int kDownThreads = 256;
+constexpr int kDownChunk = 384;   // rows of x staged in shared memory at a time
+
+__global__ void __launch_bounds__(kDownThreads) aq_down_kernel(const __grid_constant__ DownParams p) {
+  __shared__ __align__(16) float xs[kDownChunk * 16];
+  __shared__ float red[8][16][33];
+  __shared__ float part[16 * 32];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = static_cast<int>(cluster.block_rank());
+  const int csize = static_cast<int>(cluster.num_blocks());
+
+  int si = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxSeg; ++j)
+    if (j < p.nseg && static_cast<int>(blockIdx.y) >= p.seg[j].block_begin) si = j;
+  const DownSeg& sg = p.seg[si];
+  const int k0 = (static_cast<int>(blockIdx.y) - sg.block_begin) * 32;
+  const int m0 = static_cast<int>(blockIdx.z) * 16;
+  const int tid = threadIdx.x;
+  const int tk = tid & 31;
+  const int tg = tid >> 5;
+  const int k = k0 + tk;
+
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+
+  float acc[16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
+  const int i_begin = crank * p.kslice;
+  const int i_end = min(p.K, i_begin + p.kslice);
+  for (int c0 = i_begin; c0 < i_end; c0 += kDownChunk) {
+    const int len = min(kDownChunk, i_end - c0);
+    __syncthreads();
+    for (int idx = tid; idx < 16 * len; idx += kDownThreads) {
+      const int m = idx / len;
+      const int i = idx - m * len;
+      float v = 0.0f;
+      if (m0 + m < p.M) v = bf16_to_f32(p.x[static_cast<int64_t>(m0 + m) * p.ldx + c0 + i]);
+      xs[i * 16 + m] = v;
+    }
+    __syncthreads();
+    if (k < sg.r) {
+      const uint16_t* vcol = sg.V + k;
+      for (int i = tg; i < len; i += 8) {
+        const float v = bf16_to_f32(vcol[static_cast<int64_t>(c0 + i) * sg.ldv]);
+        const float4* xr = reinterpret_cast<const float4*>(&xs[i * 16]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 xv = xr[q];
+          acc[4 * q + 0] = fmaf(v, xv.x, acc[4 * q + 0]);
+          acc[4 * q + 1] = fmaf(v, xv.y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(v, xv.z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(v, xv.w, acc[4 * q + 3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 16; ++m) red[tg][m][tk] = acc[m];
+  __syncthreads();
+  for (int idx = tid; idx < 512; idx += kDownThreads) {
+    const int m = idx >> 5;
+    const int kk = idx & 31;
+    float s = 0.0f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) s += red[g][m][kk];
+    part[idx] = s;
+  }
+  cluster.sync();
+  // Each CTA of the cluster finishes a slice of the 16 x 32 outputs, summing the
+  // partials of all CTAs in rank order (deterministic).
+  const int per = (512 + csize - 1) / csize;
+  for (int idx = crank * per + tid; idx < min(512, (crank + 1) * per); idx += kDownThreads) {
+    float s = 0.0f;
+    for (int q = 0; q < csize; ++q) s += cluster.map_shared_rank(part, q)[idx];
+    const int m = idx >> 5;
+    const int kk = idx & 31;
+    if (m0 + m < p.M && k0 + kk < sg.r)
+      sg.t[static_cast<int64_t>(m0 + m) * p.ldt + k0 + kk] = f32_to_bf16_rn(s);
+  }
+  cluster.sync();
+}
+
+// ------------------------------------------------------------------------------------
+// V [in, r] -> V^T [r, in]
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) aq_transpose_kernel(const __grid_constant__ TransposeParams p) {
+  __shared__ uint16_t tile[32][34];
+  const TransposeSeg& sg = p.seg[blockIdx.z];
+  const int i0 = blockIdx.x * 32;
+  const int k0 = blockIdx.y * 32;
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  if (k0 >= sg.r) return;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = i0 + ty + 8 * j;
+    const int k = k0 + tx;
+    tile[ty + 8 * j][tx] = (i < p.K && k < sg.r) ? sg.V[static_cast<int64_t>(i) * sg.ldv + k] : 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int k = k0 + ty + 8 * j;
+    const int i = i0 + tx;
+    if (k < sg.r && i < p.K) sg.Vt[static_cast<int64_t>(k) * sg.ldvt + i] = tile[tx][ty + 8 * j];
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// W_eff = s * W0 + U V^T
+// ------------------------------------------------------------------------------------
+constexpr int kPreCBufs = 3;   // W0 / W_eff tiles in flight per CTA
+constexpr int kPreAcc = 2;     // TMEM accumulators
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    aq_precompute_kernel(const __grid_constant__ PrecomputeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* c_full = empty + kMaxStages;
+  uint64_t* c_empty = c_full + kPreCBufs;
+  uint64_t* acc_full = c_empty + kPreCBufs;
+  uint64_t* acc_empty = acc_full + kPreAcc;
+  uint64_t* epi_done = acc_empty + kPreAcc;
+  uint64_t* mma_done = epi_done + kPreCBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const uint32_t cbuf_bytes = static_cast<uint32_t>(p.bn) * 256u;  // bn/64 boxes of 128 x 128 B
+  uint8_t* cbuf = smem + kHeaderBytes;
+  uint8_t* ring = cbuf + kPreCBufs * cbuf_bytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
+  const bool has_mma = p.r > 0;
+  const int nkb = has_mma ? ceil_div_i(p.r, kBK) : 0;
+  const int nbox = p.bn / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kPreCBufs; ++b) {
+      mbar_init(&c_full[b], 1);
+      mbar_init(&c_empty[b], 1);
+      mbar_init(&epi_done[b], 4 * 32);
+    }
+    for (int b = 0; b < kPreAcc; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4 * 32);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_w0);
+    tma_prefetch_desc(&p.tm_we);
+    if (has_mma) {
+      tma_prefetch_desc(&p.tm_u);
+      tma_prefetch_desc(&p.tm_v);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, fill_par = 0, cfilled = 0, cfill_par = 0;
+      bool ok = true;
+      pdl_wait_prior_grid();
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+        const int o0 = (tile / p.n_col_tiles) * kMmaM;
+        const int i0 = (tile % p.n_col_tiles) * p.bn;
+        const int cb = it % kPreCBufs;
+        const uint32_t cph = static_cast<uint32_t>(it / kPreCBufs) & 1u;
+        if (!mbar_wait(&c_empty[cb], cph ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c_full[cb], cbuf_bytes);
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(cbuf + cb * cbuf_bytes + j * kStageA, &p.tm_w0, i0 + 64 * j, o0, &c_full[cb],
+                      pol_stream);
+        cfilled |= 1u << cb;
+        cfill_par = (cfill_par & ~(1u << cb)) | (cph << cb);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kMmaM + p.bn) * 128u);
+          tma_load_2d(st, &p.tm_u, kb * kBK, o0, &full[stage], pol_keep);
+          tma_load_2d(st + kStageA, &p.tm_v, kb * kBK, i0, &full[stage], pol_keep);
+          filled |= 1u << stage;
+          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < p.stages; ++s)
+          if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_par >> s) & 1u, kDrainNs);
+        for (int b = 0; b < kPreCBufs; ++b)
+          if (cfilled & (1u << b)) mbar_wait_drain(&c_full[b], (cfill_par >> b) & 1u, kDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (has_mma) {
+      const uint32_t idesc = idesc_bf16_f32(kMmaM, p.bn);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+        const int ab = it & 1;
+        const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!warp_wait(&acc_empty[ab], aph ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(ab * p.bn);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!warp_wait(&full[stage], phase, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * p.stage_bytes);
+            const uint32_t b_addr = a_addr + kStageA;
+            const int rem = p.r - kb * kBK;
+            const int nk = rem >= kBK ? kBK / kUmmaK : ceil_div_i(rem, kUmmaK);
+            for (int j = 0; j < nk; ++j)
+              tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc,
+                          (kb > 0 || j > 0) ? 1u : 0u);
+            tc_commit(&empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok && lane == 0) tc_commit(&acc_full[ab]);
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_commit(mma_done);
+        mbar_wait_drain(mma_done, 0, kDrainNs);
+      }
+      __syncwarp();
+    }
+  } else {
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;  // row of the tile (TMEM lane) this thread owns
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const bool leader = (warp == 2 && lane == 0);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const int o0 = (tile / p.n_col_tiles) * kMmaM;
+      const int i0 = (tile % p.n_col_tiles) * p.bn;
+      const int cb = it % kPreCBufs;
+      const uint32_t cph = static_cast<uint32_t>(it / kPreCBufs) & 1u;
+      const int ab = it & 1;
+      const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+      if (!warp_wait(&c_full[cb], cph, ctl)) break;
+      if (has_mma) {
+        if (!warp_wait(&acc_full[ab], aph, ctl)) break;
+        tc_fence_after();
+      }
+      const int o = o0 + lrow;
+      const float sc = (o < p.out) ? bf16_to_f32(p.s[o]) : 0.0f;
+      uint8_t* ctile = cbuf + cb * cbuf_bytes;
+      for (int c = 0; c < p.bn; c += 16) {
+        float d[16];
+        if (has_mma) {
+          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c), d);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) d[j] = 0.0f;
+        }
+        // W0 row segment: box (c / 64), two 16-byte chunks at swizzled positions.
+        uint8_t* rowp = ctile + (c / 64) * kStageA + lrow * 128;
+        const int ch0 = (c % 64) / 8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4* cp = reinterpret_cast<uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4));
+          const uint4 w = *cp;
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          uint32_t res[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = fmaf(sc, __uint_as_float(ww[e] << 16), d[h * 8 + 2 * e]);
+            const float hi = fmaf(sc, __uint_as_float(ww[e] & 0xFFFF0000u), d[h * 8 + 2 * e + 1]);
+            res[e] = pack_bf16x2(lo, hi);
+          }
+          *cp = make_uint4(res[0], res[1], res[2], res[3]);
+        }
+      }
+      if (has_mma) {
+        tc_fence_before();
+        mbar_arrive(&acc_empty[ab]);
+      }
+      // All 128 epilogue threads publish their rows; the leader waits (bounded) for
+      // all of them, then one TMA store per 64-column box writes the tile out.
+      fence_proxy_async_smem();
+      mbar_arrive(&epi_done[cb]);
+      if (leader) {
+        if (!mbar_wait(&epi_done[cb], cph, ctl)) break;
+        for (int j = 0; j < nbox; ++j) tma_store_2d(&p.tm_we, ctile + j * kStageA, i0 + 64 * j, o0);
+        tma_store_commit();
+        tma_store_wait_read_all();
+        mbar_arrive(&c_empty[cb]);
+      }
+    }
+    if (leader) tma_store_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+}
+
+// ------------------------------------------------------------------------------------
+// Bounded-wait self test: one block waits on a barrier nobody arrives on.
+// ------------------------------------------------------------------------------------
+__global__ void aq_selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const AbortCtl ctl{&abort_flag, status, timeout_ns};
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, ctl);
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------------------------
+// host-side launch helpers
+// ------------------------------------------------------------------------------------
+static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             bool pdl, void** args, dim3 cluster = dim3(1, 1, 1)) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster.x;
+    attrs[n].val.clusterDim.y = cluster.y;
+    attrs[n].val.clusterDim.z = cluster.z;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_gemm(const GemmParams& p, bool swap, int grid, size_t smem, cudaStream_t st,
+                        bool pdl) {
+  void* args[] = {const_cast<GemmParams*>(&p)};
+  const void* fn = swap ? reinterpret_cast<const void*>(&aq_gemm_kernel<true>)
+                        : reinterpret_cast<const void*>(&aq_gemm_kernel<false>);
+  return launch_ex(fn, dim3(grid), dim3(kGemmThreads), smem, st, pdl, args);
+}
+
+cudaError_t launch_down(const DownParams& p, int grid_y, cudaStream_t st, bool pdl) {
+  void* args[] = {const_cast<DownParams*>(&p)};
+  return launch_ex(reinterpret_cast<const void*>(&aq_down_kernel), dim3(p.csize, grid_y, p.mgroups),
+                   dim3(kDownThreads), 0, st, pdl, args, dim3(p.csize, 1, 1));
+}
+
+cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl) {
+  void* args[] = {const_cast<TransposeParams*>(&p)};
+  dim3 grid((p.K + 31) / 32, (max_r + 31) / 32, p.nseg);
+  return launch_ex(reinterpret_cast<const void*>(&aq_transpose_kernel), grid, dim3(256), 0, st, pdl,
+                   args);
+}
+
+cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
+                              bool pdl) {
+  void* args[] = {const_cast<PrecomputeParams*>(&p)};
+  return launch_ex(reinterpret_cast<const void*>(&aq_precompute_kernel), dim3(grid), dim3(kGemmThreads),
+                   smem, st, pdl, args);
+}
+
+cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st) {
+  void* args[] = {&status, &timeout_ns};
+  return launch_ex(reinterpret_cast<const void*>(&aq_selftest_wait_kernel), dim3(1), dim3(32), 0, st,
+                   false, args);
+}
+
+cudaError_t configure_kernels(int device, size_t max_smem) {
+  (void)device;
+  cudaError_t e;
+  const int s = static_cast<int>(max_smem);
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+    return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+    return e;
+  if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+    return e;
+  return cudaSuccess;
+}
+
+int32_t* device_status_ptr(int device, cudaError_t* err) {
+  (void)device;
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_device_status);
+  return static_cast<int32_t*>(p);
+}
+
+}  // namespace aq

@@ -252,6 +252,36 @@ def small_int_x(seed_keys, M: int, inp: int, lim: int = 3) -> np.ndarray:
     return _matrix(v, M, inp, ld_for(inp))
 
 
+def _sparse_ints(state: int, n: int, lim: int, density: float) -> np.ndarray:
+    """Integers in [-lim, lim] \\ {0} with probability ``density``, else 0."""
+    z = splitmix64(state, np.arange(2 * n, dtype=np.uint64)).reshape(n, 2)
+    keep = (z[:, 0] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53) < density
+    mag = (z[:, 1] % np.uint64(lim)).astype(np.int64) + 1
+    sign = np.where((z[:, 1] >> np.uint64(32)) & np.uint64(1), -1, 1)
+    return np.where(keep, sign * mag, 0).astype(np.float64)
+
+
+def sparse_int_theta(seed_keys, out: int, inp: int, r: int, w_lim: int = 2, uv_lim: int = 1,
+                     w_density: float = 0.5, v_density: float = 0.1, u_density: float = 0.5) -> Theta:
+    """Integer-valued bundle for bit-exact checks: sparse small integers keep every
+    partial sum (W0 x, Vᵀx and the final y) small enough to be exact in fp32 and,
+    for t and y, in bf16 as well; s is drawn from {0.5, 1, 2}."""
+    W0 = _matrix(_sparse_ints(stream_seed(*seed_keys, "W0"), out * inp, w_lim, w_density), out, inp,
+                 ld_for(inp))
+    choice = np.array([0.5, 1.0, 2.0])
+    z = splitmix64(stream_seed(*seed_keys, "s"), np.arange(out, dtype=np.uint64))
+    s = bf16_bits_from_f64(choice[(z % np.uint64(3)).astype(np.int64)])
+    if r == 0:
+        return Theta(W0, s, None, None, out, inp, 0)
+    U = _matrix(_sparse_ints(stream_seed(*seed_keys, "U"), out * r, w_lim, u_density), out, r, ld_for(r))
+    V = _matrix(_sparse_ints(stream_seed(*seed_keys, "V"), inp * r, uv_lim, v_density), inp, r, ld_for(r))
+    return Theta(W0, s, U, V, out, inp, r)
+
+
+def sparse_int_x(seed_keys, M: int, inp: int, density: float = 0.3) -> np.ndarray:
+    return _matrix(_sparse_ints(stream_seed(*seed_keys, "x"), M * inp, 1, density), M, inp, ld_for(inp))
+
+
 # ----------------------------------------------------------------------------------
 # Workload shapes (sizes only; no trained weights are involved anywhere)
 # ----------------------------------------------------------------------------------

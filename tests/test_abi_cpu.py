@@ -1,0 +1,137 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side argument
+validation works without a GPU (no compute calls are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rank_weight_reconstruction_gb300 as aq
+from rank_weight_reconstruction_gb300 import binding, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "aq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(aq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("aq_linear", "aq_linear_qkv", "aq_precompute", "aq_linear_workspace_bytes"):
+        assert name in syms
+    assert sorted(binding.EXPORTED_SYMBOLS) == syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    assert binding.aq_abi_version() == 1
+    assert binding.aq_status_string(0) == "AQ_OK"
+    assert binding.aq_status_string(8) == "AQ_ERR_TIMEOUT"
+    assert binding.aq_status_string(99) == "AQ_ERR_UNKNOWN"
+    assert aq.aq_decode_max_m() == 64
+
+
+def _theta(out=64, inp=32, r=4, W0=0x1000, s=0x2000, U=0x3000, V=0x4000, ld_w0=None, ld_u=8, ld_v=8):
+    return binding.c_theta(W0=W0, ld_w0=ld_w0 or inp, s=s, U=U if r else 0, ld_u=ld_u if r else 0,
+                           V=V if r else 0, ld_v=ld_v if r else 0, out=out, in_=inp, r=r)
+
+
+def _linear(lib, th, x=0x100000, M=4, ldx=32, y=0x200000, ldy=64, ws=0x300000, ws_bytes=1 << 20):
+    return lib.aq_linear(ctypes.byref(th), x, M, ldx, y, ldy, ws, ws_bytes, None)
+
+
+def test_workspace_bytes(lib):
+    th = _theta(out=64, inp=32, r=4)
+    # t: M x round_up(r, 8) bf16, rounded to 256 bytes; no V^T copy at small M
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 4) == 256
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 0) == 0
+    # large M adds V^T [r, round_up(in, 8)]
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 100) == 1792 + 256
+    th0 = _theta(r=0)
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th0), 1, 1000) == 0
+    arr = (binding.c_theta * 3)(_theta(r=4), _theta(r=0), _theta(r=12))
+    assert lib.aq_linear_workspace_bytes(arr, 3, 8) == 512  # 8 x (8 + 16) x 2 -> 384 -> 512
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 2, 8) == ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(r=257), binding.AQ_ERR_UNSUPPORTED),
+    (dict(r=-1), binding.AQ_ERR_SHAPE),
+    (dict(out=0), binding.AQ_ERR_SHAPE),
+    (dict(ld_w0=16), binding.AQ_ERR_SHAPE),
+    (dict(ld_w0=36), binding.AQ_ERR_ALIGNMENT),
+    (dict(W0=0x1008), binding.AQ_ERR_ALIGNMENT),
+    (dict(U=0), binding.AQ_ERR_INVALID_ARG),
+    (dict(ld_u=2), binding.AQ_ERR_SHAPE),
+    (dict(ld_v=12), binding.AQ_ERR_ALIGNMENT),
+    (dict(s=0), binding.AQ_ERR_INVALID_ARG),
+])
+def test_theta_validation(lib, kw, status):
+    assert _linear(lib, _theta(**kw)) == status
+    assert binding.aq_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), binding.AQ_ERR_SHAPE),
+    (dict(x=0), binding.AQ_ERR_INVALID_ARG),
+    (dict(ldx=16), binding.AQ_ERR_SHAPE),
+    (dict(ldx=36), binding.AQ_ERR_ALIGNMENT),
+    (dict(y=0), binding.AQ_ERR_INVALID_ARG),
+    (dict(ldy=40), binding.AQ_ERR_SHAPE),
+    (dict(y=0x200004), binding.AQ_ERR_ALIGNMENT),
+    (dict(ws=0), binding.AQ_ERR_WORKSPACE),
+    (dict(ws_bytes=16), binding.AQ_ERR_WORKSPACE),
+    (dict(ws=0x300010), binding.AQ_ERR_WORKSPACE),
+    (dict(y=0x100000 + 64), binding.AQ_ERR_OVERLAP),      # y inside x
+    (dict(y=0x1000), binding.AQ_ERR_OVERLAP),             # y on W0
+    (dict(ws=0x200000 + 256), binding.AQ_ERR_OVERLAP),    # workspace inside y
+])
+def test_call_validation(lib, kw, status):
+    assert _linear(lib, _theta(), **kw) == status, binding.aq_last_error()
+
+
+def test_m_zero_is_noop(lib):
+    assert _linear(lib, _theta(), M=0, x=0, y=0, ws=0, ws_bytes=0) == binding.AQ_OK
+
+
+def test_qkv_validation(lib):
+    th = (binding.c_theta * 3)(_theta(out=16, r=4, W0=0x10000), _theta(out=8, r=4, W0=0x20000),
+                               _theta(out=8, r=4, W0=0x30000))
+    ys = (ctypes.c_void_p * 3)(0x200000, 0x200000 + 32, 0x200000 + 48)
+    ld = (ctypes.c_int64 * 3)(32, 32, 32)
+    # column slices of one [M, 32] buffer at 0/16/24 overlap: 16-wide q slice covers columns 0..15
+    ys_bad = (ctypes.c_void_p * 3)(0x200000, 0x200000 + 16, 0x200000 + 48)
+    assert lib.aq_linear_qkv(th, 0x100000, 4, 32, ys_bad, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_OVERLAP
+    th_in = (binding.c_theta * 3)(_theta(inp=32), _theta(inp=40, ld_w0=40), _theta(inp=32))
+    assert lib.aq_linear_qkv(th_in, 0x100000, 4, 40, ys, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_SHAPE
+
+
+def test_precompute_validation(lib):
+    th = _theta()
+    assert lib.aq_precompute(ctypes.byref(th), 0, 32, None) == binding.AQ_ERR_INVALID_ARG
+    assert lib.aq_precompute(ctypes.byref(th), 0x500000, 16, None) == binding.AQ_ERR_SHAPE
+    assert lib.aq_precompute(ctypes.byref(th), 0x1000 + 64, 32, None) == binding.AQ_ERR_OVERLAP
+
+
+def test_path_setting(lib):
+    assert lib.aq_set_path(7) == binding.AQ_ERR_INVALID_ARG
+    assert lib.aq_set_path(binding.AQ_PATH_AUTO) == binding.AQ_OK
+
+
+def test_selftest_argument_check(lib):
+    assert lib.aq_selftest_bounded_wait(0, None) == binding.AQ_ERR_INVALID_ARG
+    assert lib.aq_selftest_bounded_wait(2_000_000, None) == binding.AQ_ERR_INVALID_ARG

@@ -1,0 +1,356 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle.
+
+Bars (fixed before any kernel was written):
+* reconstruction linear: max |y - y_ref| <= 1e-2 * max |y_ref| and relative L2 <= 2e-3
+  over the whole output (or over the sampled rows at full 31B-class sizes);
+* integer-valued inputs: every intermediate is exact in fp32 and bf16, so the result
+  must equal the oracle bit for bit on every path;
+* W_eff: every element within 1 bf16 ulp of RN_bf16(oracle); passthrough and r = 0 with
+  power-of-two scales exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rank_weight_reconstruction_gb300 as aq
+from rank_weight_reconstruction_gb300 import synth
+
+from helpers import bits, dev, dev_theta, host_f64, x_f64
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [aq.AQ_PATH_DECODE, aq.AQ_PATH_PREFILL]
+PATH_IDS = {aq.AQ_PATH_AUTO: "auto", aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_PREFILL: "prefill"}
+
+
+@pytest.fixture(autouse=True)
+def _restore_path():
+    yield
+    aq.aq_set_path(aq.AQ_PATH_AUTO)
+
+
+def assert_close(y, y_ref, what=""):
+    st = oracle.error_stats(y, y_ref)
+    assert oracle.within_tolerance(y, y_ref), f"{what}: {st}"
+    return st
+
+
+def run_linear(th, xb, path=aq.AQ_PATH_AUTO, M=None):
+    aq.aq_set_path(path)
+    x = dev(xb)[:, : th.inp]
+    y = aq.aq_linear(dev_theta(th), x)
+    torch.cuda.synchronize()
+    return y
+
+
+def test_bounded_wait_reports_timeout():
+    assert aq.aq_device_status() == aq.AQ_OK
+    aq.aq_selftest_bounded_wait(2000)
+    assert aq.aq_device_status() == aq.AQ_ERR_TIMEOUT
+    assert aq.aq_device_status() == aq.AQ_OK     # reading clears it
+    # the context is still usable
+    th = synth.make_theta(("bw",), 64, 64, 4)
+    xb = synth.make_x(("bw",), 2, 64)
+    y = run_linear(th, xb)
+    assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, 64)))
+    assert aq.aq_device_status() == aq.AQ_OK
+
+
+# ----------------------------------------------------------------------------------
+# integer-valued cases: bit-exact on every path
+# ----------------------------------------------------------------------------------
+INT_SHAPES = [  # out, in, r, M
+    (8, 16, 1, 1), (16, 64, 0, 3), (40, 64, 3, 5), (130, 200, 17, 33), (257, 72, 65, 17),
+    (300, 136, 64, 130), (96, 1152, 16, 16), (1000, 96, 8, 1), (64, 264, 128, 200),
+    (200, 64, 256, 65), (17, 8, 2, 300),
+]
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
+@pytest.mark.parametrize("shape", INT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_integer_bit_exact(shape, path):
+    out, inp, r, M = shape
+    th = synth.sparse_int_theta(("int", *shape), out, inp, r)
+    xb = synth.sparse_int_x(("int", *shape), M, inp)
+    W0, s, U, V = th.f64()
+    xf = x_f64(xb, inp)
+    y_ref = oracle.linear(W0, s, U, V, xf)
+    t_ref = xf @ V
+    # preconditions of exactness: t (held in bf16 between kernels) and y representable
+    assert np.array_equal(oracle.round_to_bf16(t_ref), t_ref)
+    assert np.array_equal(oracle.round_to_bf16(y_ref), y_ref)
+    y = run_linear(th, xb, path)
+    assert aq.aq_last_path() == path
+    np.testing.assert_array_equal(host_f64(y), y_ref)
+
+
+# ----------------------------------------------------------------------------------
+# tiny configuration: 256 x 256, r = 8, M = 1 (+ r = 0 and passthrough)
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("path", [aq.AQ_PATH_AUTO] + PATHS, ids=lambda p: PATH_IDS[p])
+@pytest.mark.parametrize("variant", ["r8", "r0", "passthrough"])
+def test_tiny_config(variant, path):
+    if variant == "r8":
+        th = synth.make_theta(("cfg1",), 256, 256, 8)
+    elif variant == "r0":
+        th = synth.make_theta(("cfg1", "r0"), 256, 256, 0)
+    else:
+        th = synth.passthrough_theta(("cfg1", "pt"), 256, 256, 8)
+    xb = synth.make_x(("cfg1",), 1, 256)
+    y = run_linear(th, xb, path)
+    W0, s, U, V = th.f64()
+    xf = x_f64(xb, 256)
+    y_ref = oracle.linear(W0, s, U, V, xf)
+    assert_close(host_f64(y), y_ref, f"{variant}/{PATH_IDS[path]}")
+    if variant == "passthrough":
+        # closed form: y = W0 x
+        assert_close(host_f64(y), xf @ W0.T)
+    if variant == "r0":
+        assert_close(host_f64(y), s[None, :] * (xf @ W0.T))
+
+
+# ----------------------------------------------------------------------------------
+# ragged shapes and both paths, random values
+# ----------------------------------------------------------------------------------
+RAGGED = [(100, 72, 5, 1), (333, 200, 33, 7), (129, 1000, 64, 129), (1000, 264, 4, 63),
+          (2000, 128, 130, 65), (48, 4096, 16, 300), (520, 512, 256, 1000)]
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+def test_ragged_random(shape, path):
+    out, inp, r, M = shape
+    th = synth.make_theta(("rag", *shape), out, inp, r)
+    xb = synth.make_x(("rag", *shape), M, inp)
+    y = run_linear(th, xb, path)
+    assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, inp)), str(shape))
+
+
+def test_padded_leading_dims_and_canaries():
+    """x, y with padded leading dimensions inside larger buffers: everything outside
+    the output window keeps its sentinel."""
+    out, inp, r, M = 200, 136, 12, 9
+    th = synth.make_theta(("pad",), out, inp, r)
+    xb = synth.make_x(("pad",), M, inp)
+    xbuf = torch.zeros(M, 160, dtype=torch.bfloat16, device="cuda")
+    xbuf[:, :inp] = dev(xb)[:, :inp]
+    for path in PATHS:
+        aq.aq_set_path(path)
+        ybuf = torch.full((M + 2, 224), -7.0, dtype=torch.bfloat16, device="cuda")
+        y = ybuf[1:M + 1, 8:8 + out]
+        aq.aq_linear(dev_theta(th), xbuf[:, :inp], y=y)
+        torch.cuda.synchronize()
+        assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, inp)))
+        yb = host_f64(ybuf)
+        mask = np.ones_like(yb, dtype=bool)
+        mask[1:M + 1, 8:8 + out] = False
+        assert np.all(yb[mask] == -7.0)
+
+
+def test_m_zero_noop():
+    th = synth.make_theta(("m0",), 64, 64, 4)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    y = aq.aq_linear(dev_theta(th), x)
+    assert y.shape == (0, 64)
+
+
+def test_batch_rows_match_single_token_calls():
+    out, inp, r = 640, 384, 16
+    th = synth.make_theta(("rows",), out, inp, r)
+    xb = synth.make_x(("rows",), 12, inp)
+    y_all = host_f64(run_linear(th, xb))
+    for m in (0, 5, 11):
+        y1 = host_f64(run_linear(th, xb[m:m + 1]))
+        assert_close(y1[0], y_all[m])
+
+
+# ----------------------------------------------------------------------------------
+# Gemma-3-1B-shaped decode layer (r = 16, M in {1, 4, 16}), Q/K/V batched
+# ----------------------------------------------------------------------------------
+def _gemma_layer(layer, r, M, row_scale=None):
+    fam = synth.GEMMA3_1B_FAMILIES
+    thetas = {}
+    for name, (out, inp) in fam.items():
+        W0 = synth.make_w0(("gemma", name), out, inp)          # G = 1: shared by all layers
+        thetas[name] = synth.make_theta(("gemma", name, layer), out, inp, r, W0=W0)
+    xs = {inp: synth.make_x(("gemma-x", layer, inp, M), M, inp, row_scale) for inp in (1152, 1024, 6912)}
+    return thetas, xs
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("layer", [0, 25])
+def test_gemma_decode_layer(layer, M):
+    thetas, xs = _gemma_layer(layer, 16, M)
+    qkv = [thetas[n] for n in ("q_proj", "k_proj", "v_proj")]
+    ys = aq.aq_linear_qkv([dev_theta(t) for t in qkv], dev(xs[1152])[:, :1152])
+    torch.cuda.synchronize()
+    for t, y in zip(qkv, ys):
+        assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xs[1152], 1152)), "qkv")
+    for name in ("o_proj", "gate_proj", "up_proj", "down_proj"):
+        t = thetas[name]
+        y = run_linear(t, xs[t.inp])
+        assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xs[t.inp], t.inp)), name)
+
+
+@pytest.mark.parametrize("M", [1, 16, 100, 512])
+def test_qkv_stacked_layout(M):
+    """y_q, y_k, y_v as column slices of one [M, 1536] buffer (the concatenated layout)."""
+    thetas, xs = _gemma_layer(3, 16, M)
+    qkv = [thetas[n] for n in ("q_proj", "k_proj", "v_proj")]
+    Y = torch.zeros(M, 1536, dtype=torch.bfloat16, device="cuda")
+    views = [Y[:, :1024], Y[:, 1024:1280], Y[:, 1280:]]
+    aq.aq_linear_qkv([dev_theta(t) for t in qkv], dev(xs[1152])[:, :1152], ys=views)
+    torch.cuda.synchronize()
+    Yh = host_f64(Y)
+    xf = x_f64(xs[1152], 1152)
+    ref = np.concatenate([oracle.linear(*t.f64(), xf) for t in qkv], axis=1)
+    assert_close(Yh, ref)
+
+
+def test_qkv_mixed_ranks():
+    out_in = [(512, 256), (128, 256), (136, 256)]
+    ths = [synth.make_theta(("mix", j), o, i, r) for j, ((o, i), r) in enumerate(zip(out_in, (0, 8, 40)))]
+    for M in (3, 70):
+        xb = synth.make_x(("mix", M), M, 256)
+        ys = aq.aq_linear_qkv([dev_theta(t) for t in ths], dev(xb)[:, :256])
+        torch.cuda.synchronize()
+        for t, y in zip(ths, ys):
+            assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xb, 256)))
+
+
+# ----------------------------------------------------------------------------------
+# Gemma-3-1B shapes at prefill (r = 64, rows of x scaled by U(0.5, 2))
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [512, 2048, 8192])
+def test_gemma_prefill(M):
+    thetas, xs = _gemma_layer(7, 64, M, row_scale=(0.5, 2.0))
+    names = list(thetas) if M < 8192 else ["gate_proj", "down_proj", "o_proj"]
+    for name in names:
+        t = thetas[name]
+        y = run_linear(t, xs[t.inp])
+        assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xs[t.inp], t.inp)), f"{name} M={M}")
+    qkv = [thetas[n] for n in ("q_proj", "k_proj", "v_proj")]
+    ys = aq.aq_linear_qkv([dev_theta(t) for t in qkv], dev(xs[1152])[:, :1152])
+    torch.cuda.synchronize()
+    for t, y in zip(qkv, ys):
+        assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xs[1152], 1152)), f"qkv M={M}")
+
+
+# ----------------------------------------------------------------------------------
+# rank / shape sweep on gate-like and down-like projections
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 8, 64, 512, 4096])
+@pytest.mark.parametrize("r", [0, 4, 16, 64, 256])
+@pytest.mark.parametrize("shape", [(6912, 1152), (1152, 6912)], ids=["gate", "down"])
+def test_rank_sweep(shape, r, M):
+    out, inp = shape
+    th = synth.make_theta(("sweep", out, inp, r), out, inp, r)
+    xb = synth.make_x(("sweep", out, inp, M), M, inp)
+    y = host_f64(run_linear(th, xb))
+    W0, s, U, V = th.f64()
+    xf = x_f64(xb, inp)
+    rows = np.arange(M) if M <= 512 else np.unique(np.linspace(0, M - 1, 64).astype(int))
+    assert_close(y[rows], oracle.linear(W0, s, U, V, xf[rows]))
+
+
+# ----------------------------------------------------------------------------------
+# 31B-class projection: out 21504, in 5376, r 128, M in {1, 32, 8192}
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 32, 8192])
+def test_31b_projection(M):
+    out, inp = synth.CLASS31B_SHAPES["wide"]
+    th = synth.make_theta(("31b", "wide", 0), out, inp, 128)
+    xb = synth.make_x(("31b-x", M), M, inp)
+    y = host_f64(run_linear(th, xb))
+    W0, s, U, V = th.f64()
+    xf = x_f64(xb, inp)
+    rows = np.arange(M) if M <= 32 else np.unique(np.linspace(0, M - 1, 48).astype(int))
+    assert_close(y[rows], oracle.linear(W0, s, U, V, xf[rows]))
+
+
+# ----------------------------------------------------------------------------------
+# precompute W_eff
+# ----------------------------------------------------------------------------------
+def _ulp_diff(got_bits, ref_value):
+    ref_bits = oracle.bf16_bits_of_value(ref_value)
+    return np.abs(oracle.bf16_ordinal(got_bits) - oracle.bf16_ordinal(ref_bits))
+
+
+def assert_weight_ok(W, th):
+    acc = oracle.weight_acceptance(bits(W), *th.f64())
+    assert acc["all_ok"], acc
+    # the 1-ulp bar holds everywhere except on near-cancelling elements
+    assert acc["within_1ulp"] >= acc["elements"] - max(4, acc["elements"] // 100000), acc
+    return acc
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 8), (300, 200, 17), (129, 1000, 64), (1000, 136, 0),
+                                   (520, 384, 256), (64, 72, 4), (1152, 6912, 16), (6912, 1152, 130)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_precompute_within_one_ulp(shape):
+    out, inp, r = shape
+    th = synth.make_theta(("pre", *shape), out, inp, r)
+    W = aq.aq_precompute(dev_theta(th))
+    torch.cuda.synchronize()
+    assert_weight_ok(W, th)
+
+
+def test_precompute_passthrough_and_pow2_scale_exact():
+    th = synth.passthrough_theta(("pre-pt",), 300, 264, 16)
+    W = aq.aq_precompute(dev_theta(th))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(W), th.W0[:, :264])
+    th0 = synth.make_theta(("pre-r0",), 200, 136, 0)
+    th0.s = synth.bf16_bits_from_f64(np.ldexp(1.0, np.arange(200) % 5 - 2))
+    W = aq.aq_precompute(dev_theta(th0))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(W), oracle.bf16_bits_of_value(oracle.effective_weight_bf16(*th0.f64())))
+
+
+def test_precompute_integer_exact():
+    th = synth.sparse_int_theta(("pre-int",), 260, 200, 40)
+    W = aq.aq_precompute(dev_theta(th))
+    torch.cuda.synchronize()
+    ref = oracle.effective_weight(*th.f64())
+    assert np.all(np.abs(ref) <= 128)
+    np.testing.assert_array_equal(host_f64(W), ref)
+
+
+def test_precompute_into_padded_buffer_with_canaries():
+    th = synth.make_theta(("pre-pad",), 130, 72, 8)
+    buf = torch.full((132, 96), 3.0, dtype=torch.bfloat16, device="cuda")
+    W = buf[1:131, 8:80]
+    aq.aq_precompute(dev_theta(th), W_eff=W)
+    torch.cuda.synchronize()
+    assert_weight_ok(W, th)
+    b = host_f64(buf)
+    mask = np.ones_like(b, dtype=bool)
+    mask[1:131, 8:80] = False
+    assert np.all(b[mask] == 3.0)
+
+
+def test_weight_then_dense_matches_identity():
+    """y computed as W_eff x (torch matmul consuming the GPU-built W_eff) agrees with the
+    oracle's factorised y: the load-time and in-graph forms are the same projection."""
+    th = synth.make_theta(("weffx",), 1152, 1024, 16)
+    W = aq.aq_precompute(dev_theta(th))
+    xb = synth.make_x(("weffx",), 8, 1024)
+    y = (dev(xb)[:, :1024].float() @ W.float().t())
+    assert_close(y.double().cpu().numpy(), oracle.linear(*th.f64(), x_f64(xb, 1024)))
+
+
+@pytest.mark.parametrize("shape", ["square", "wide"])
+def test_31b_band_precompute(shape):
+    """60-layer stack with G = 4 bands: the first and last layer (bands 0 and 3) checked
+    in full, element by element."""
+    out, inp = synth.CLASS31B_SHAPES[shape]
+    W0b = {b: synth.make_w0(("31b-band", shape, b), out, inp) for b in (0, 3)}
+    for layer in (0, 59):
+        band = oracle.band_of_layer(layer, 60, 4)
+        th = synth.make_theta(("31b-layer", shape, layer), out, inp, 128, W0=W0b[band])
+        W = aq.aq_precompute(dev_theta(th))
+        torch.cuda.synchronize()
+        assert_weight_ok(W, th)
+        del W
+    assert aq.aq_device_status() == aq.AQ_OK
