@@ -336,6 +336,14 @@ def run_ours(args, dist: Dist):
     for _ in range(args.warmup):
         g.replay()
     torch.cuda.synchronize()
+    if args.profile:
+        # kernel-profiler mode: the eager warm-up (one launch pair per call), W warm-up
+        # replays and K replays of the step, nothing else
+        for _ in range(args.steps):
+            g.replay()
+        torch.cuda.synchronize()
+        return {"profile": True, "launches_per_step": launches, "warmup": args.warmup, "steps": args.steps,
+                "status": aq.aq_device_status()}
     dist.barrier()
     torch.cuda.synchronize()
     ev_s, ev_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -654,6 +662,8 @@ def main():
     ap.add_argument("--skip-precompute", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="run only the captured decode step (for kernel-profiler launch lists)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
