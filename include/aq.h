@@ -117,6 +117,25 @@ aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t 
                         void* const y[3], const int64_t ldy[3],
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* aq_linear for callers that may not allocate device memory. The paper has no
+ * counterpart: this entry point exists for callers such as plugins inside a runtime that
+ * owns all device memory, or serving loops that forbid allocation after start-up.
+ * Same arguments and results as aq_linear, minus the workspace: the scratch it needs
+ * (aq_linear_workspace_bytes(th, 1, M) bytes) comes from one array of
+ * AQ_NOALLOC_WORKSPACE_BYTES compiled into the library, which every GPU that uses the
+ * library keeps allocated until the process exits. The caller still passes x and y.
+ *   - A call whose scratch need exceeds AQ_NOALLOC_WORKSPACE_BYTES is rejected with
+ *     AQ_ERR_WORKSPACE (message in aq_last_error) before anything is enqueued.
+ *   - The first call on a device looks up the array's device address on that device;
+ *     make that first call before capturing a stream into a CUDA graph.
+ *   - All calls on a device share the one array and it keeps the previous call's
+ *     contents (nothing in it needs to start at zero). Calls that can overlap on the GPU
+ *     -- on different streams without ordering between them -- race on it; order them.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
+#define AQ_NOALLOC_WORKSPACE_BYTES (4u * 1024u * 1024u)
+aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
+                            void* y, int64_t ldy, void* stream);
+
 /* W_eff[o, i] = RN_bf16( s[o] * W0[o,i] + sum_k U[o,k] * V[i,k] )
  * ("Execution paths", "Precompute-outside: the production path": built once per
  * layer at load). W_eff is [out, in] device, row stride ld_weff >= in, and must not

@@ -32,8 +32,9 @@ EXPORTED_SYMBOLS = [
     "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
     "aq_device_status", "aq_selftest_bounded_wait", "aq_set_path", "aq_decode_max_m",
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
-    "aq_abi_version",
+    "aq_abi_version", "aq_linear_noalloc",
 ]
+AQ_NOALLOC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 
 class AqError(RuntimeError):
@@ -78,6 +79,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_linear.restype = ctypes.c_int
     lib.aq_linear_qkv.argtypes = [th_p, vp, i64, i64, ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
     lib.aq_linear_qkv.restype = ctypes.c_int
+    lib.aq_linear_noalloc.argtypes = [th_p, vp, i64, i64, vp, i64, vp]
+    lib.aq_linear_noalloc.restype = ctypes.c_int
     lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
     lib.aq_precompute.restype = ctypes.c_int
     lib.aq_device_status.argtypes = [vp]
@@ -202,6 +205,18 @@ def aq_linear(theta: Theta, x, y=None, workspace=None, stream=None):
     _check(load().aq_linear(ctypes.byref(th), _ptr(x), M, _ld(x), _ptr(y), _ld(y), _ptr(workspace),
                             0 if workspace is None else workspace.numel() * workspace.element_size(),
                             _stream(stream)))
+    return y
+
+
+def aq_linear_noalloc(theta: Theta, x, y=None, stream=None):
+    """aq_linear without a workspace argument: the library's built-in scratch array is
+    used, so the library itself allocates nothing (y is allocated here only if not
+    given)."""
+    M = int(x.size(0))
+    if y is None:
+        y = _padded_empty(M, theta.out, x.device)
+    th = theta.c()
+    _check(load().aq_linear_noalloc(ctypes.byref(th), _ptr(x), M, _ld(x), _ptr(y), _ld(y), _stream(stream)))
     return y
 
 

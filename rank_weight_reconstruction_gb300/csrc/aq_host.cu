@@ -485,6 +485,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
 
 }  // namespace
 
+int aq::set_last_error(int status, const char* message) {
+  t_err = message ? message : "";
+  return status;
+}
+
 // =====================================================================================
 // exported C ABI
 // =====================================================================================

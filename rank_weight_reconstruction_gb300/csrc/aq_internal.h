@@ -123,6 +123,8 @@ cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, 
                               bool pdl);
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t configure_kernels(int device, size_t max_smem);
+// Records the message aq_last_error() returns on this thread and passes the status through.
+int set_last_error(int status, const char* message);
 int32_t* device_status_ptr(int device, cudaError_t* err);
 
 }  // namespace aq

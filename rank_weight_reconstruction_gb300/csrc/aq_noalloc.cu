@@ -1,0 +1,79 @@
+// aq_noalloc.cu -- aq_linear_noalloc: the reconstruction linear for callers that are not
+// allowed to allocate device memory.
+//
+// aq_linear needs a small scratch area (t = V^T x, and for more than 64 tokens a
+// transposed copy of V) that its caller normally allocates. Some callers cannot do that:
+// a plugin inside an inference runtime that owns all device memory and hands plugins
+// only their input and output buffers, a serving loop that forbids allocation after
+// start-up (cudaMalloc can synchronise the device and fragments a fixed memory budget),
+// or code running where no allocator is reachable at all. For them the scratch lives in
+// one fixed array compiled into this library.
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "aq.h"
+#include "aq_internal.h"
+
+// The scratch area. Every GPU on which this library is used holds these bytes until the
+// process exits. All calls on a device share it; it keeps whatever the last call wrote.
+static __device__ __align__(256) unsigned char aq_noalloc_scratch[AQ_NOALLOC_WORKSPACE_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};  // device address of aq_noalloc_scratch, per device index
+
+// In host code the array's name is only a host-side stand-in; the kernels need its
+// device address, which is looked up once per device with that device current.
+aq_status scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "aq_linear_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
+    return static_cast<aq_status>(aq::set_last_error(AQ_ERR_CUDA, msg));
+  }
+  if (dev < 0 || dev >= 64)
+    return static_cast<aq_status>(aq::set_last_error(AQ_ERR_UNSUPPORTED, "aq_linear_noalloc: device index out of range"));
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, aq_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      char msg[256];
+      snprintf(msg, sizeof msg, "aq_linear_noalloc: cudaGetSymbolAddress of the scratch array failed: %s",
+               cudaGetErrorString(e));
+      return static_cast<aq_status>(aq::set_last_error(AQ_ERR_CUDA, msg));
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return AQ_OK;
+}
+
+}  // namespace
+
+extern "C" aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y,
+                                       int64_t ldy, void* stream) {
+  if (!th) return static_cast<aq_status>(aq::set_last_error(AQ_ERR_INVALID_ARG, "aq_linear_noalloc: theta is NULL"));
+  const size_t need = aq_linear_workspace_bytes(th, 1, M);
+  if (need == static_cast<size_t>(-1))  // invalid sizes: let aq_linear's validation name them
+    return aq_linear(th, x, M, ldx, y, ldy, nullptr, 0, stream);
+  if (need > static_cast<size_t>(AQ_NOALLOC_WORKSPACE_BYTES)) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "aq_linear_noalloc: M=%lld, r=%d, in=%d needs %zu bytes of scratch, more than the %u bytes "
+             "built into the library; use aq_linear with a caller-provided workspace",
+             (long long)M, th->r, th->in, need, (unsigned)AQ_NOALLOC_WORKSPACE_BYTES);
+    return static_cast<aq_status>(aq::set_last_error(AQ_ERR_WORKSPACE, msg));
+  }
+  if (need == 0) return aq_linear(th, x, M, ldx, y, ldy, nullptr, 0, stream);
+  void* scratch = nullptr;
+  aq_status st = scratch_address(&scratch);
+  if (st != AQ_OK) return st;
+  // Nothing in the scratch has to start at zero: every byte the kernels read is first
+  // written by the same call.
+  return aq_linear(th, x, M, ldx, y, ldy, scratch, AQ_NOALLOC_WORKSPACE_BYTES, stream);
+}
