@@ -274,7 +274,7 @@ class DecodeStack:
             ws = max(ws, aq.aq_linear_workspace_bytes([th0["q_proj"], th0["k_proj"], th0["v_proj"]], M))
             for f in ("o_proj", "gate_proj", "up_proj", "down_proj"):
                 ws = max(ws, aq.aq_linear_workspace_bytes(th0[f], M))
-        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)   # sync part must start at 0
 
     def calls(self, only=None):
         """List of (family key, callable) in step order."""
@@ -480,7 +480,7 @@ def extras(result, args, dist, stack, device, pk):
                            U=dev_bits(th.U, device)[:, :r], V=dev_bits(th.V, device)[:, :r])
         layers.append(ths)
     ys = {f: torch.empty(M, o, dtype=torch.bfloat16, device=device) for f, (o, _) in FAMS.items()}
-    ws = torch.empty(max(aq.aq_linear_workspace_bytes([layers[0]["q_proj"], layers[0]["k_proj"],
+    ws = torch.zeros(max(aq.aq_linear_workspace_bytes([layers[0]["q_proj"], layers[0]["k_proj"],
                                                         layers[0]["v_proj"]], M),
                          aq.aq_linear_workspace_bytes(layers[0]["down_proj"], M)), dtype=torch.uint8, device=device)
 
@@ -527,7 +527,8 @@ def extras(result, args, dist, stack, device, pk):
               V=dev_bits(th.V, device)[:, :128])
     x = dev_bits(synth.make_x(("bench-31b",), 8192, inp), device)[:, :inp]
     y = torch.empty(8192, out, dtype=torch.bfloat16, device=device)
-    ws = torch.empty(aq.aq_linear_workspace_bytes(T, 8192), dtype=torch.uint8, device=device)
+    ws = torch.zeros(max(aq.aq_linear_workspace_bytes(T, m) for m in (1, 32, 8192)), dtype=torch.uint8,
+                     device=device)
     aq.aq_linear(T, x, y=y, workspace=ws)
     torch.cuda.synchronize()
     g31 = torch.cuda.CUDAGraph()

@@ -82,11 +82,20 @@ typedef struct aq_theta {
   int32_t r;
 } aq_theta;
 
+/* Workspace of aq_linear / aq_linear_qkv. Its first AQ_WORKSPACE_SYNC_BYTES hold the
+ * counters and the fp32 accumulator of t = V^T x that the CTAs of the decode kernel share:
+ * that part must be zero before the workspace is first used (e.g. cudaMemset once after
+ * allocating it), and every call that completes leaves it zero again, so one workspace
+ * can serve any sequence of calls, shapes and paths on a stream. The rest is scratch
+ * that needs no initialisation (per-CTA partial sums at decode; t in bf16 and a
+ * transposed copy of V at prefill). After a call whose bounded wait expired
+ * (aq_device_status() == AQ_ERR_TIMEOUT) the sync part must be zeroed again. */
+#define AQ_WORKSPACE_SYNC_BYTES (128u * 1024u)
+
 /* Bytes of device workspace aq_linear (n_theta == 1) or aq_linear_qkv (n_theta == 3,
- * pass the three bundles) needs for M tokens. The workspace holds t = V^T x (bf16)
- * and, for large M, a transposed copy of V. Its contents need no initialisation and
- * are scratch between calls. Returns 0 if no workspace is needed (r == 0 or M == 0)
- * and (size_t)-1 for invalid arguments. */
+ * pass the three bundles) needs for M tokens, on either path. Returns 0 if none is
+ * needed (M == 0, or M above the decode limit with r == 0) and (size_t)-1 for invalid
+ * arguments. */
 size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
 
 /* y[m, o] = RN_bf16( s[o] * sum_i W0[o,i] x[m,i] + sum_k U[o,k] * t[m,k] ),
@@ -96,12 +105,13 @@ size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M)
  *   th        the bundle (host pointer to the struct; the struct's pointers are device)
  *   x         [M, in] device, row stride ldx >= in
  *   y         [M, out] device, row stride ldy >= out; must not overlap x, W0, s, U, V
- *   workspace device, >= aq_linear_workspace_bytes(th, 1, M) bytes, 256-byte aligned
- *             (may be NULL when that size is 0)
+ *   workspace device, >= aq_linear_workspace_bytes(th, 1, M) bytes, 256-byte aligned,
+ *             first AQ_WORKSPACE_SYNC_BYTES zero (see above); NULL when that size is 0
  *   stream    cudaStream_t
- * M == 0 is a no-op returning AQ_OK. Small M (decode) streams W0 once with a
- * swap-AB tensor-core kernel; large M (prefill) runs a tcgen05 GEMM; the fused
- * epilogue applies s and adds the rank-r term in both. */
+ * M == 0 is a no-op returning AQ_OK. Decode (M <= aq_decode_max_m() = 32) is one
+ * launch that streams W0 once, split evenly over the SMs; prefill (larger M) runs a
+ * tcgen05 GEMM after a small t = x V GEMM. Both fuse s and the rank-r term into the
+ * epilogue. Concurrent calls sharing one workspace must be ordered on the GPU. */
 aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
                     void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
                     void* stream);
@@ -129,10 +139,13 @@ aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t 
  *   - The first call on a device looks up the array's device address on that device;
  *     make that first call before capturing a stream into a CUDA graph.
  *   - All calls on a device share the one array and it keeps the previous call's
- *     contents (nothing in it needs to start at zero). Calls that can overlap on the GPU
- *     -- on different streams without ordering between them -- race on it; order them.
+ *     contents. Its sync part (see AQ_WORKSPACE_SYNC_BYTES) starts at zero when the
+ *     library is loaded and every completed call leaves it zero; after an expired wait
+ *     (AQ_ERR_TIMEOUT) results of later calls are undefined. Calls that can overlap on
+ *     the GPU -- on different streams without ordering between them -- race on the
+ *     array; order them.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
-#define AQ_NOALLOC_WORKSPACE_BYTES (4u * 1024u * 1024u)
+#define AQ_NOALLOC_WORKSPACE_BYTES (8u * 1024u * 1024u)
 aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
                             void* y, int64_t ldy, void* stream);
 
@@ -157,7 +170,8 @@ aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
 
 /* Path selection for aq_linear / aq_linear_qkv. AQ_PATH_AUTO picks by M (decode
  * kernel for M <= aq_decode_max_m(), prefill kernel above). The other values force a
- * path for tests; both paths are valid for every M. Process-wide setting. */
+ * path for tests: prefill works for every M, decode for M <= aq_decode_max_m() (larger M
+ * returns AQ_ERR_UNSUPPORTED). Process-wide setting. */
 typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2 } aq_path;
 aq_status aq_set_path(aq_path path);
 int32_t aq_decode_max_m(void);

@@ -34,7 +34,8 @@ EXPORTED_SYMBOLS = [
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
     "aq_abi_version", "aq_linear_noalloc",
 ]
-AQ_NOALLOC_WORKSPACE_BYTES = 4 * 1024 * 1024
+AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
+AQ_WORKSPACE_SYNC_BYTES = 128 * 1024
 
 
 class AqError(RuntimeError):
@@ -184,12 +185,17 @@ def _padded_empty(rows: int, cols: int, device):
     return torch.empty(rows, ld, dtype=torch.bfloat16, device=device)[:, :cols]
 
 
-def _workspace(nbytes: int, device):
+def new_workspace(nbytes: int, device):
+    """A workspace for aq_linear / aq_linear_qkv: zero-filled (its sync part must start
+    at zero; the library keeps it zero), 256-byte aligned (torch's caching allocator
+    returns 512-byte aligned blocks). Reuse it across calls on one stream."""
     import torch
     if nbytes == 0:
         return None
-    # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
-    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+_workspace = new_workspace
 
 
 def aq_linear(theta: Theta, x, y=None, workspace=None, stream=None):

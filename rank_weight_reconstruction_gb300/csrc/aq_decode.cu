@@ -1,0 +1,516 @@
+// aq_decode.cu -- the decode kernel (M <= 32 tokens) of the reconstruction linear
+//   y = s . (W0 x) + U (V^T x)            ("How attnquant works", "The reconstruction identity")
+//
+// At decode the work is an HBM stream of W0 with a tiny contraction per element, so the
+// design is about keeping every SM's memory pipe full and the critical path short:
+//   * every W0-streaming CTA owns a balanced, contiguous range of output rows of one
+//     family over the whole K, so no partial sum of y ever leaves the CTA;
+//   * warp 0 feeds a TMA ring (W0 boxes of the CTA's rows x 64, x boxes tok_tile x 64,
+//     128-byte swizzle); warps 1..8 split the rows into 16-row slabs and, when there are
+//     fewer than 8 slabs, split K between the warps of a slab; they run the M <= 32
+//     contraction with mma.sync (m16n8k16, bf16 in, fp32 accumulate) from ldmatrix
+//     fragments and add the warps' partial sums in shared memory in a fixed order.
+//     A tcgen05.mma with M = 128, K = 16 costs about 148 cycles at any N on this part, so
+//     one issuing thread moving a 128 x 16 W0 slice per instruction cannot keep up with
+//     HBM, while eight warps of mma.sync use a small fraction of their rate here;
+//   * a few extra CTAs compute t = V^T x, each over a slice of `in`, add their partial
+//     sums in shared memory and then once per element into an fp32 accumulator in the
+//     workspace's sync region; the streaming CTAs wait for them only in their epilogue,
+//     y = RN_bf16(s * z + U t); the last CTA to finish clears the sync region.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "aq_internal.h"
+#include "aq_ptx.cuh"
+
+namespace aq {
+namespace {
+
+__device__ __forceinline__ uint8_t* align_1k(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Every lane waits; the outcome is made warp-uniform because ldmatrix and mma.sync that
+// follow are warp-collective.
+__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, const AbortCtl& ctl) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
+}
+
+// Barrier of the 256 consumer threads on an mbarrier, so that a wait that never ends is
+// bounded like every other wait in the kernel.
+__device__ __forceinline__ bool cons_sync(uint64_t* bar, uint32_t& phase, const AbortCtl& ctl) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase, ctl);
+  phase ^= 1u;
+  return ok;
+}
+
+__device__ __forceinline__ int seg_of_cta(const DecodeParams& p, int g) {
+  int si = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxSeg; ++j)
+    if (j < p.nseg && g >= p.seg[j].cta_begin) si = j;
+  return si;
+}
+
+}  // namespace
+
+template <int NT>
+__global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1k(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* cbar = empty + kMaxStages;
+  int* abort_flag = reinterpret_cast<int*>(cbar + 1);
+  int* bcast = abort_flag + 1;
+  uint8_t* epi = smem + kHeaderBytes;
+  uint8_t* ring = epi + p.epi_bytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+  const bool t_cta = cta < p.t_ctas;
+  const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
+  constexpr int kTok = NT * 8;
+
+  // this CTA's family and rows (streaming CTAs only)
+  const int g = cta - p.t_ctas;
+  const int si = t_cta ? 0 : seg_of_cta(p, g);
+  const DecodeSeg& sg = p.seg[si];
+  const int l = g - sg.cta_begin;
+  const int R = sg.chunk_rows;
+  const int nstage = (p.nkb + p.kbox - 1) / p.kbox;
+  // Every streaming CTA reads the same x blocks; starting each CTA at a different k stage
+  // spreads those reads over the L2 slices instead of all SMs hitting one block at once.
+  const int rot = t_cta ? 0 : (g * 7) % nstage;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecConsumers / 32);
+    }
+    mbar_init(cbar, kDecConsumers);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (!t_cta && warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_x);
+    tma_prefetch_desc(&sg.tm_w);
+  }
+  // The next kernel in the stream may now be scheduled and start its own weight
+  // prefetch; it touches activations and workspace only after this grid completes.
+  pdl_launch_dependents();
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- TMA producer (streaming CTAs) ----------------
+    if (!t_cta && lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      // the CTA's (chunk, stage) sequence
+      int total = 0;
+      for (int ch = 0; ch < sg.chunks; ++ch)
+        if ((l * sg.chunks + ch) * R < sg.rows) total += nstage;
+      const int pre = total < p.stages ? total : p.stages;
+      uint32_t filled = 0, fill_par = 0;
+      auto issue = [&](int q, int slot, bool weights, bool acts) {
+        const int ch = q / nstage;
+        const int st = (q - ch * nstage + rot) % nstage;   // rotated k order (see rot)
+        const int row0 = (l * sg.chunks + ch) * R;
+        const int kb0 = st * p.kbox;
+        const int nb = min(p.kbox, p.nkb - kb0);
+        uint8_t* base = ring + static_cast<size_t>(slot) * p.stage_bytes;
+        if (weights) {
+          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nb) * (R + p.M) * 128u);
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(base + b * p.wbox_bytes, &sg.tm_w, (kb0 + b) * kBK, row0, &full[slot], pol);
+        }
+        if (acts)
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(base + p.kbox * p.wbox_bytes + b * p.tok_tile * 128, &p.tm_x, (kb0 + b) * kBK, 0,
+                        &full[slot], pol);
+      };
+      // W0 of the first stages goes out before waiting on the previous grid.
+      for (int q = 0; q < pre; ++q) {
+        issue(q, q, true, false);
+        filled |= 1u << q;
+      }
+      pdl_wait_prior_grid();
+      for (int q = 0; q < pre; ++q) issue(q, q, false, true);
+      int slot = pre == p.stages ? 0 : pre;
+      uint32_t phase = pre == p.stages ? 1u : 0u;
+      bool ok = true;
+      for (int q = pre; q < total; ++q) {
+        if (!mbar_wait(&empty[slot], phase ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        issue(q, slot, true, true);
+        filled |= 1u << slot;
+        fill_par = (fill_par & ~(1u << slot)) | (phase << slot);
+        if (++slot == p.stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < p.stages; ++s)
+          if (filled & (1u << s)) {
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&full[s], (fill_par >> s) & 1u))
+              if (global_timer_ns() - t0 > 20000000ull) break;
+          }
+      }
+    }
+  } else {
+    const int cw = warp - 1;              // consumer warp 0..7
+    const int ct = threadIdx.x - 32;      // 0..255
+    const int gq = lane >> 2, qq = lane & 3;
+    uint32_t cph = 0;
+    bool ok = true;
+    pdl_wait_prior_grid();
+
+    if (t_cta) {
+      // ---- t = V^T x over this CTA's slice of `in` ----
+      const int ks = (p.K + p.t_ctas - 1) / p.t_ctas;
+      const int i0 = cta * ks;
+      const int i1 = min(p.K, i0 + ks);
+      const int rp = (p.r_total + 3) & ~3;             // padded t width (4-wide blocks)
+      const int ntot = p.M * p.r_total;
+      float* tacc = reinterpret_cast<float*>(epi);       // [M][r_total]   (<= 96 KB spans into the ring)
+      const int tacc_bytes = (ntot * 4 + 1023) & ~1023;
+      uint8_t* stage_area = epi + tacc_bytes;
+      const int cap = static_cast<int>(p.epi_bytes) + p.stages * static_cast<int>(p.stage_bytes) - tacc_bytes;
+      const int chunk = max(1, min(cap / (kDecMaxTok * 4 + rp * 2), 1 << 20));
+      float* xs = reinterpret_cast<float*>(stage_area);                          // [chunk][32]
+      uint16_t* vs = reinterpret_cast<uint16_t*>(stage_area + chunk * kDecMaxTok * 4);  // [chunk][rp]
+      for (int idx = ct; idx < ntot; idx += kDecConsumers) tacc[idx] = 0.0f;
+      // thread -> (4 tokens x 4 columns) block and a residue class of rows
+      const int mb = (p.M + 3) / 4, kbk = rp / 4;
+      const int blocks = mb * kbk;
+      const int igroups = max(1, kDecConsumers / blocks);
+      const int blk = ct % blocks, ig = ct / blocks;
+      const bool worker = blocks <= kDecConsumers ? (ig < igroups) : true;
+      float acc[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+      for (int a = i0; ok && a < i1; a += chunk) {
+        const int n = min(chunk, i1 - a);
+        if (!(ok = cons_sync(cbar, cph, ctl))) break;
+        // staging loads, eight in flight per thread
+        for (int base = ct; base < n * kDecMaxTok; base += 8 * kDecConsumers) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kDecConsumers;
+            const int m = idx / n, i = idx - m * n;
+            v[u] = (idx < n * kDecMaxTok && m < p.M) ? bf16_to_f32(p.x[static_cast<int64_t>(m) * p.ldx + a + i]) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kDecConsumers;
+            if (idx < n * kDecMaxTok) {
+              const int m = idx / n, i = idx - m * n;
+              xs[i * kDecMaxTok + m] = v[u];
+            }
+          }
+        }
+        for (int idx = ct; idx < n * (rp - p.r_total); idx += kDecConsumers) {
+          const int i = idx / (rp - p.r_total), k = idx - i * (rp - p.r_total);
+          vs[i * rp + p.r_total + k] = 0;
+        }
+        for (int j = 0; j < p.nseg; ++j) {
+          const DecodeSeg& sj = p.seg[j];
+          const int tot = n * sj.r;
+          for (int base = ct; base < tot; base += 8 * kDecConsumers) {
+            uint16_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + u * kDecConsumers;
+              const int i = idx / sj.r, k = idx - i * sj.r;
+              v[u] = idx < tot ? sj.V[static_cast<int64_t>(a + i) * sj.ldv + k] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + u * kDecConsumers;
+              if (idx < tot) {
+                const int i = idx / sj.r, k = idx - i * sj.r;
+                vs[i * rp + sj.t_col + k] = v[u];
+              }
+            }
+          }
+        }
+        if (!(ok = cons_sync(cbar, cph, ctl))) break;
+        // blocks beyond the thread count (very wide t) loop over several blocks
+        for (int b2 = blk; b2 < blocks; b2 += (blocks <= kDecConsumers ? blocks : kDecConsumers)) {
+          if (!worker) break;
+          const int m0 = (b2 / kbk) * 4, k0 = (b2 % kbk) * 4;
+          float lacc[4][4];
+#pragma unroll
+          for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+            for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = 0.0f;
+          for (int i = (blocks <= kDecConsumers ? ig : 0); i < n; i += (blocks <= kDecConsumers ? igroups : 1)) {
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[i * kDecMaxTok + m0]);
+            const uint2 vv = *reinterpret_cast<const uint2*>(&vs[i * rp + k0]);
+            const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xFFFF0000u);
+            const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xFFFF0000u);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            const float va[4] = {v0, v1, v2, v3};
+#pragma unroll
+            for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+              for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = fmaf(xa[x0], va[y0], lacc[x0][y0]);
+          }
+          if (blocks <= kDecConsumers) {
+#pragma unroll
+            for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+              for (int y0 = 0; y0 < 4; ++y0) acc[x0][y0] += lacc[x0][y0];
+          } else {
+#pragma unroll
+            for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+              for (int y0 = 0; y0 < 4; ++y0) {
+                const int m = m0 + x0, k = k0 + y0;
+                if (m < p.M && k < p.r_total) atomicAdd(&tacc[m * p.r_total + k], lacc[x0][y0]);
+              }
+          }
+        }
+      }
+      if (ok && blocks <= kDecConsumers && worker) {
+        const int m0 = (blk / kbk) * 4, k0 = (blk % kbk) * 4;
+#pragma unroll
+        for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+          for (int y0 = 0; y0 < 4; ++y0) {
+            const int m = m0 + x0, k = k0 + y0;
+            if (m < p.M && k < p.r_total) atomicAdd(&tacc[m * p.r_total + k], acc[x0][y0]);
+          }
+      }
+      if (ok) ok = cons_sync(cbar, cph, ctl);
+      if (ok) {
+        for (int idx = ct; idx < ntot; idx += kDecConsumers) atomicAdd(&p.t_acc[idx], tacc[idx]);
+        __threadfence();
+        ok = cons_sync(cbar, cph, ctl);
+        if (ok && ct == 0) atomicAdd(&p.counters[0], 1);
+      }
+    } else {
+      // ---- stream this CTA's rows of W0 ----
+      const int nslab = (R + 15) / 16;
+      const int kg = 8 / nslab;                 // warps sharing one slab (split over K)
+      const bool active = cw < nslab * kg;
+      const int slab = cw / kg, kgi = cw - slab * kg;
+      float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
+      float* ts = red + 8 * 16 * kTok;                       // [M][r]
+      int slot = 0;
+      uint32_t phase = 0;
+      for (int ch = 0; ok && ch < sg.chunks; ++ch) {
+        const int row0 = (l * sg.chunks + ch) * R;
+        if (row0 >= sg.rows) break;
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        for (int sq = 0; sq < nstage; ++sq) {
+          if (!warp_wait_all(&full[slot], phase, ctl)) {
+            ok = false;
+            break;
+          }
+          const int st = (sq + rot) % nstage;
+          const int nb = min(p.kbox, p.nkb - st * p.kbox);
+          if (active) {
+            const uint32_t sbase = smem_u32(ring + static_cast<size_t>(slot) * p.stage_bytes);
+            for (int step = kgi; step < nb * 4; step += kg) {
+              const int b = step >> 2, j = step & 3;
+              const uint32_t abase = sbase + b * p.wbox_bytes;
+              const uint32_t bbase = sbase + p.kbox * p.wbox_bytes + b * p.tok_tile * 128;
+              const int arow = 16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8;
+              const int achunk = 2 * j + (lane >> 4);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(abase + arow * 128 + ((achunk ^ (arow & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+              for (int np = 0; np < NT / 2; ++np) {
+                const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
+                const int bchunk = 2 * j + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(bbase + brow * 128 + ((bchunk ^ (brow & 7)) << 4), b0, b1, b2, b3);
+                mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          if (++slot == p.stages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        // ---- epilogue of this chunk ----
+        if (!(ok = cons_sync(cbar, cph, ctl))) break;   // red / ts free
+        if (active) {
+          float* my = red + (slab * kg + kgi) * 16 * kTok;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int rr = gq + 8 * h, tok = 8 * nt + 2 * qq;
+              my[rr * kTok + tok] = acc[nt][2 * h];
+              my[rr * kTok + tok + 1] = acc[nt][2 * h + 1];
+            }
+        }
+        if (sg.r > 0) {
+          if (ct == 0) {
+            bool ready = true;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(&p.counters[0]) < p.t_ctas) {
+              __nanosleep(256);   // many CTAs poll one word: keep the line free for the arrivals
+              if (*reinterpret_cast<volatile int*>(abort_flag) || global_timer_ns() - t0 > p.timeout_ns) {
+                *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                atomicExch(p.status, kStatusTimeout);
+                ready = false;
+                break;
+              }
+            }
+            *bcast = ready ? 1 : 0;
+          }
+          if (!(ok = cons_sync(cbar, cph, ctl)) || !*bcast) {
+            ok = false;
+            break;
+          }
+          for (int idx = ct; idx < p.M * sg.r; idx += kDecConsumers) {
+            const int m = idx / sg.r, k = idx - m * sg.r;
+            ts[idx] = __ldcg(&p.t_acc[m * p.r_total + sg.t_col + k]);
+          }
+        }
+        if (!(ok = cons_sync(cbar, cph, ctl))) break;
+        const int row = ct & 127;
+        const int half = ct >> 7;
+        const int o = row0 + row;
+        if (row < R && o < sg.rows) {
+          const int rs = row >> 4, rr = row & 15;
+          float z[kTok / 2];
+#pragma unroll
+          for (int mi = 0; mi < kTok / 2; ++mi) z[mi] = 0.0f;
+          for (int k2 = 0; k2 < kg; ++k2) {
+            const float* pr = red + (rs * kg + k2) * 16 * kTok + rr * kTok;
+#pragma unroll
+            for (int mi = 0; mi < kTok / 2; ++mi) z[mi] += pr[half + 2 * mi];
+          }
+          float low[kTok / 2];
+#pragma unroll
+          for (int mi = 0; mi < kTok / 2; ++mi) low[mi] = 0.0f;
+          if (sg.r > 0) {
+            const uint16_t* urow = sg.U + static_cast<int64_t>(o) * sg.ldu;
+            int k = 0;
+            for (; k + 8 <= sg.r; k += 8) {
+              const uint4 uv = __ldg(reinterpret_cast<const uint4*>(urow + k));
+              const uint32_t w[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float u = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+#pragma unroll
+                for (int mi = 0; mi < kTok / 2; ++mi) {
+                  const int m = half + 2 * mi;
+                  if (m < p.M) low[mi] = fmaf(u, ts[m * sg.r + k + e], low[mi]);
+                }
+              }
+            }
+            for (; k < sg.r; ++k) {
+              const float u = bf16_to_f32(urow[k]);
+#pragma unroll
+              for (int mi = 0; mi < kTok / 2; ++mi) {
+                const int m = half + 2 * mi;
+                if (m < p.M) low[mi] = fmaf(u, ts[m * sg.r + k], low[mi]);
+              }
+            }
+          }
+          const float sc = bf16_to_f32(sg.s[o]);
+#pragma unroll
+          for (int mi = 0; mi < kTok / 2; ++mi) {
+            const int m = half + 2 * mi;
+            if (m < p.M) sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, z[mi], low[mi]));
+          }
+        }
+      }
+    }
+
+    // The last CTA to finish clears the sync region for the next call (nothing to clear
+    // when no family has a rank-r term).
+    if (ok && p.r_total > 0) ok = cons_sync(cbar, cph, ctl);
+    if (ok && p.r_total > 0) {
+      if (ct == 0) {
+        __threadfence();
+        const int old = atomicAdd(&p.counters[1], 1);
+        *bcast = (old == grid - 1) ? 1 : 0;
+      }
+      ok = cons_sync(cbar, cph, ctl);
+      if (ok && *bcast) {
+        __threadfence();
+        for (int idx = ct; idx < p.M * p.r_total; idx += kDecConsumers) p.t_acc[idx] = 0.0f;
+        __threadfence();
+        ok = cons_sync(cbar, cph, ctl);
+        if (ok && ct == 0) {
+          p.counters[0] = 0;
+          p.counters[1] = 0;
+          __threadfence();
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
+  void* args[] = {const_cast<DecodeParams*>(&p)};
+  const void* fn = p.tok_tile > 16 ? reinterpret_cast<const void*>(&aq_decode_kernel<4>)
+                                   : reinterpret_cast<const void*>(&aq_decode_kernel<2>);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t configure_decode(size_t max_smem) {
+  cudaError_t e;
+  const int s = static_cast<int>(max_smem);
+  if ((e = cudaFuncSetAttribute(aq_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  return cudaFuncSetAttribute(aq_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, s);
+}
+
+}  // namespace aq

@@ -22,7 +22,7 @@ thread_local int32_t t_last_path = 0;
 thread_local int32_t t_launches = 0;
 std::atomic<int> g_path{AQ_PATH_AUTO};
 
-constexpr int kDecodeMaxM = 64;                       // swap-AB decode kernel up to this M
+constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
 constexpr uint64_t kTimeoutNs = 1000ull * 1000 * 1000;  // limit of one in-kernel wait: 1 s
 constexpr size_t kSmemSlack = 1024;                   // room to align the dynamic smem base
 
@@ -203,38 +203,46 @@ void theta_spans(const aq_theta* th, Span* out4) {
 
 // ---------------------------------------------------------------------------------
 // workspace layout of aq_linear / aq_linear_qkv
+//   [0, kSyncBytes)   sync region: zero before first use, left zero by every decode call
+//                     (tile arrival counters, fp32 t accumulator)
+//   [kSyncBytes, ..)  scratch, no initialisation needed (prefill: t [M, ld_t] bf16, then
+//                     V^T [r_j, ldvt] per family); decode uses only the sync region
 // ---------------------------------------------------------------------------------
 struct WsLayout {
-  int64_t ld_t = 0;            // row stride of t [M, sum r_pad]
-  int64_t t_col[kMaxSeg] = {};  // column offset of family j in t
-  size_t t_bytes = 0;
-  size_t vt_off[kMaxSeg] = {};  // byte offset of V^T of family j
+  int64_t ld_t = 0;              // prefill: row stride of t [M, sum round_up(r_j, 8)]
+  int64_t t_col[kMaxSeg] = {};   // prefill: column of family j in t
+  int32_t dec_t_col[kMaxSeg] = {};  // decode: column of family j in the fp32 t accumulator
+  int32_t r_total = 0;
+  size_t vt_off[kMaxSeg] = {};   // prefill: byte offset of V^T of family j
   int64_t ldvt = 0;
+  size_t decode_scratch = 0;
+  size_t prefill_scratch = 0;
   size_t total = 0;
   bool any_r = false;
-  bool use_vt = false;
 };
 
 WsLayout ws_layout(const aq_theta* const* th, int n, int64_t M) {
   WsLayout w;
   for (int j = 0; j < n; ++j) {
     w.t_col[j] = w.ld_t;
+    w.dec_t_col[j] = w.r_total;
     if (th[j]->r > 0) {
       w.any_r = true;
       w.ld_t += round_up(th[j]->r, 8);
+      w.r_total += th[j]->r;
     }
   }
-  if (!w.any_r || M <= 0) return w;
-  w.t_bytes = static_cast<size_t>(round_up(M * w.ld_t * 2, 256));
-  w.total = w.t_bytes;
-  w.use_vt = M > kDecodeMaxM;
-  if (w.use_vt) {
+  if (M <= 0) return w;
+  if (w.any_r) {
+    size_t off = static_cast<size_t>(round_up(M * w.ld_t * 2, 256));
     w.ldvt = round_up(th[0]->in, 8);
     for (int j = 0; j < n; ++j) {
-      w.vt_off[j] = w.total;
-      if (th[j]->r > 0) w.total += static_cast<size_t>(round_up(static_cast<int64_t>(th[j]->r) * w.ldvt * 2, 256));
+      w.vt_off[j] = kSyncBytes + off;
+      if (th[j]->r > 0) off += static_cast<size_t>(round_up(static_cast<int64_t>(th[j]->r) * w.ldvt * 2, 256));
     }
+    w.prefill_scratch = off;
   }
+  if (M <= kDecodeMaxM || w.any_r) w.total = kSyncBytes + std::max(w.decode_scratch, w.prefill_scratch);
   return w;
 }
 
@@ -247,25 +255,10 @@ uint32_t tmem_cols_for(int n) {
   return c;
 }
 
-// Decode kernels leave room on each SM for the small-M down-projection kernel that runs
-// just before them (about 44 KB of shared memory), so both can be resident together.
-constexpr size_t kDecodeSmemBudget = 176 * 1024;
-
 int stages_for(uint32_t stage_bytes, size_t smem_cap, size_t fixed) {
   const size_t budget = std::min<size_t>(smem_cap, 227 * 1024) - fixed;
   int st = static_cast<int>(budget / stage_bytes);
   return std::max(2, std::min(st, kMaxStages));
-}
-
-// Balanced rows per tile for the decode kernel: about one tile per SM (or a small whole
-// number per SM) with at most 128 rows each.
-int decode_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int sms) {
-  int64_t rows = 0;
-  for (int j = 0; j < n; ++j) rows += th[j]->out;
-  for (int64_t w = 1;; ++w) {
-    const int64_t R = std::max<int64_t>(1, ceil_div(rows * n_tok_tiles, w * sms));
-    if (R <= kMmaM) return static_cast<int>(R);
-  }
 }
 
 // Prefill N tile: minimise (waves x tile width + per-tile overhead).
@@ -344,109 +337,167 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       if (overlaps(wsp, ins[i])) return fail(AQ_ERR_OVERLAP, "%s: the workspace overlaps input %s", who, ins[i].name);
   }
 
+  const int path_cfg = g_path.load();
+  const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM);
+  if (decode && M > kDecodeMaxM)
+    return fail(AQ_ERR_UNSUPPORTED, "%s: the decode kernel handles at most %d tokens (M=%lld)", who, kDecodeMaxM,
+                (long long)M);
+  if (decode && static_cast<int64_t>(M) * wl.r_total > kMaxTAcc)
+    return fail(AQ_ERR_UNSUPPORTED, "%s: M x total rank = %lld exceeds the decode limit %d", who,
+                (long long)(M * wl.r_total), kMaxTAcc);
   DevInfo* dev = nullptr;
   aq_status st = device_info(&dev);
   if (st != AQ_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const int path_cfg = g_path.load();
-  const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  uint16_t* tbuf = reinterpret_cast<uint16_t*>(wsb);
 
-  // ---- t = V^T x for every family with r > 0 ----
-  if (wl.any_r) {
-    if (!wl.use_vt) {
-      DownParams dp = {};
-      dp.x = static_cast<const uint16_t*>(x);
-      dp.ldx = ldx;
-      dp.ldt = wl.ld_t;
-      dp.M = static_cast<int32_t>(M);
-      dp.K = K;
-      dp.mgroups = static_cast<int32_t>(ceil_div(M, 16));
-      int csize = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, ceil_div(K, 256))));
-      dp.kslice = static_cast<int32_t>(round_up(ceil_div(K, csize), 8));
-      dp.csize = static_cast<int32_t>(ceil_div(K, dp.kslice));
-      int by = 0;
-      for (int j = 0; j < n; ++j) {
-        if (th[j]->r == 0) continue;
-        DownSeg& s = dp.seg[dp.nseg++];
-        s.V = static_cast<const uint16_t*>(th[j]->V);
-        s.ldv = th[j]->ld_v;
-        s.r = th[j]->r;
-        s.t = tbuf + wl.t_col[j];
-        s.kchunks = static_cast<int32_t>(ceil_div(th[j]->r, 32));
-        s.block_begin = by;
-        by += s.kchunks;
-      }
-      if ((st = launch_or_fail(launch_down(dp, by, cs, true), "launch t = V^T x (small M)")) != AQ_OK) return st;
-    } else {
-      TransposeParams tp = {};
-      tp.K = K;
-      int max_r = 0;
-      for (int j = 0; j < n; ++j) {
-        if (th[j]->r == 0) continue;
-        TransposeSeg& s = tp.seg[tp.nseg++];
-        s.V = static_cast<const uint16_t*>(th[j]->V);
-        s.ldv = th[j]->ld_v;
-        s.Vt = reinterpret_cast<uint16_t*>(wsb + wl.vt_off[j]);
-        s.ldvt = wl.ldvt;
-        s.r = th[j]->r;
-        max_r = std::max(max_r, th[j]->r);
-      }
-      if ((st = launch_or_fail(launch_transpose(tp, max_r, cs, true), "launch V transpose")) != AQ_OK) return st;
-      // t GEMM: tokens x V^T, normal orientation, plain bf16 epilogue into the workspace
-      GemmParams gp = {};
-      gp.M = static_cast<int32_t>(M);
-      gp.K = K;
-      gp.tok_tile = kMmaM;
-      gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
-      int rt = 16;
-      for (int j = 0; j < n; ++j) rt = std::max<int>(rt, static_cast<int>(round_up(th[j]->r, 16)));
-      gp.row_tile = rt;
-      gp.n_mma = rt;
-      if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, kMmaM, "x")) != AQ_OK) return st;
-      int tiles = 0;
-      for (int j = 0; j < n; ++j) {
-        if (th[j]->r == 0) continue;
-        GemmSeg& s = gp.seg[gp.nseg++];
-        if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, rt, "V^T")) != AQ_OK) return st;
-        s.s = nullptr;
-        s.y = tbuf + wl.t_col[j];
-        s.ldy = wl.ld_t;
-        s.rows = th[j]->r;
-        s.r = 0;
-        s.n_row_tiles = 1;
-        s.tile_begin = tiles;
-        tiles += gp.n_tok_tiles;
-      }
-      gp.total_tiles = tiles;
-      gp.prefetch_w = 0;  // V^T comes from the transpose kernel just before
-      gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-      gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
-      gp.tmem_cols = tmem_cols_for(gp.n_mma);
-      gp.status = dev->status;
-      gp.timeout_ns = kTimeoutNs;
-      const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
-      const int grid = std::min(tiles, dev->sms);
-      if ((st = launch_or_fail(launch_gemm(gp, false, grid, smem, cs, true), "launch t GEMM")) != AQ_OK) return st;
+  if (decode) {
+    // ---- one launch: W0 streamed by row-owning CTAs, t = V^T x by a few extra CTAs ----
+    DecodeParams dp = {};
+    dp.x = static_cast<const uint16_t*>(x);
+    dp.ldx = ldx;
+    dp.M = static_cast<int32_t>(M);
+    dp.K = K;
+    dp.nkb = static_cast<int32_t>(ceil_div(K, kBK));
+    dp.tok_tile = M <= 16 ? 16 : 32;
+    dp.r_total = wl.r_total;
+    dp.t_ctas = wl.r_total > 0 ? static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(kDecTCtas, K / 64))) : 0;
+    int64_t rows_total = 0;
+    for (int j = 0; j < n; ++j) rows_total += th[j]->out;
+    // streaming CTAs: one per remaining SM, at least 8 rows each, shared among the families
+    // in proportion to their rows (every family gets at least one)
+    const int G = static_cast<int>(std::max<int64_t>(n, std::min<int64_t>(dev->sms - dp.t_ctas, ceil_div(rows_total, 8))));
+    int cnt[kMaxSeg] = {};
+    int used = 0;
+    for (int j = 0; j < n; ++j) {
+      cnt[j] = std::max(1, static_cast<int>(static_cast<int64_t>(G) * th[j]->out / rows_total));
+      used += cnt[j];
     }
+    while (used < G) {  // hand the remainder to the family with the most rows per CTA
+      int best = 0;
+      for (int j = 1; j < n; ++j)
+        if (static_cast<int64_t>(th[j]->out) * cnt[best] > static_cast<int64_t>(th[best]->out) * cnt[j]) best = j;
+      ++cnt[best];
+      ++used;
+    }
+    int max_rows = 8;
+    int cta_begin = 0;
+    for (int j = 0; j < n; ++j) {
+      DecodeSeg& sg = dp.seg[dp.nseg++];
+      const int64_t per = ceil_div(th[j]->out, cnt[j]);
+      sg.chunks = static_cast<int32_t>(ceil_div(per, kMmaM));
+      sg.chunk_rows = static_cast<int32_t>(ceil_div(th[j]->out, static_cast<int64_t>(cnt[j]) * sg.chunks));
+      cnt[j] = static_cast<int>(ceil_div(th[j]->out, static_cast<int64_t>(sg.chunk_rows) * sg.chunks));  // CTAs with rows
+      if ((st = tmap_2d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, sg.chunk_rows, "W0")) != AQ_OK) return st;
+      sg.s = static_cast<const uint16_t*>(th[j]->s);
+      sg.U = static_cast<const uint16_t*>(th[j]->U);
+      sg.ldu = th[j]->ld_u;
+      sg.V = static_cast<const uint16_t*>(th[j]->V);
+      sg.ldv = th[j]->ld_v;
+      sg.y = static_cast<uint16_t*>(ys[j]);
+      sg.ldy = ldys[j];
+      sg.rows = th[j]->out;
+      sg.r = th[j]->r;
+      sg.t_col = wl.dec_t_col[j];
+      sg.cta_begin = cta_begin;
+      cta_begin += cnt[j];
+      max_rows = std::max(max_rows, static_cast<int>(sg.chunk_rows));
+    }
+    if ((st = tmap_2d(&dp.tm_x, x, K, M, ldx, static_cast<int>(M), "x")) != AQ_OK) return st;
+    dp.wbox_bytes = static_cast<uint32_t>(round_up(max_rows, 8) * 128);
+    dp.kbox = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(8, 16384 / dp.wbox_bytes)));
+    dp.kbox = std::min(dp.kbox, dp.nkb);
+    dp.stage_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * (dp.wbox_bytes + dp.tok_tile * 128), 1024));
+    int max_r = 0;
+    for (int j = 0; j < n; ++j) max_r = std::max(max_r, th[j]->r);
+    dp.epi_bytes = static_cast<uint32_t>(round_up(8 * 16 * dp.tok_tile * 4 + M * max_r * 4, 1024));
+    // A t CTA stages the fp32 t block plus rows of x and V in the same space.
+    const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
+    const int64_t t_need = tacc_bytes + 64 * (kDecMaxTok * 4 + 2 * (wl.r_total + 3));
+    // Two CTAs per SM when they fit in about half of the shared memory, so the next call's
+    // CTAs can start streaming W0 while this call's finish; otherwise one large ring.
+    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes;
+    const size_t half = std::min<size_t>(dev->smem_optin, 227 * 1024) / 2 - 1024;
+    int stages2 = static_cast<int>((half - std::min(half, fixed)) / dp.stage_bytes);
+    if (stages2 >= 3 && static_cast<int64_t>(dp.epi_bytes) + stages2 * static_cast<int64_t>(dp.stage_bytes) >= t_need) {
+      dp.stages = std::min(stages2, kMaxStages);
+    } else {
+      dp.stages = stages_for(dp.stage_bytes, dev->smem_optin, fixed);
+      if (static_cast<int64_t>(dp.epi_bytes) + static_cast<int64_t>(dp.stages) * dp.stage_bytes < t_need)
+        return fail(AQ_ERR_UNSUPPORTED, "%s: M x total rank too large for the decode kernel's shared memory", who);
+    }
+    dp.counters = reinterpret_cast<int32_t*>(wsb);
+    dp.t_acc = reinterpret_cast<float*>(wsb + kSyncTAccOffset);
+    dp.status = dev->status;
+    dp.timeout_ns = kTimeoutNs;
+    const int grid = dp.t_ctas + cta_begin;
+    const size_t smem = kSmemSlack + kHeaderBytes + dp.epi_bytes + static_cast<size_t>(dp.stages) * dp.stage_bytes;
+    if ((st = launch_or_fail(launch_decode(dp, grid, smem, cs, true), "launch decode kernel")) != AQ_OK) return st;
+    t_last_path = AQ_PATH_DECODE;
+    return AQ_OK;
   }
 
-  // ---- main GEMM with the fused reconstruction epilogue ----
+  uint16_t* tbuf = reinterpret_cast<uint16_t*>(wsb + kSyncBytes);
+  // ---- t = x V for every family with r > 0: V^T into the workspace, then a tcgen05 GEMM ----
+  if (wl.any_r) {
+    TransposeParams tp = {};
+    tp.K = K;
+    int max_r = 0;
+    for (int j = 0; j < n; ++j) {
+      if (th[j]->r == 0) continue;
+      TransposeSeg& s = tp.seg[tp.nseg++];
+      s.V = static_cast<const uint16_t*>(th[j]->V);
+      s.ldv = th[j]->ld_v;
+      s.Vt = reinterpret_cast<uint16_t*>(wsb + wl.vt_off[j]);
+      s.ldvt = wl.ldvt;
+      s.r = th[j]->r;
+      max_r = std::max(max_r, th[j]->r);
+    }
+    if ((st = launch_or_fail(launch_transpose(tp, max_r, cs, true), "launch V transpose")) != AQ_OK) return st;
+    GemmParams gp = {};
+    gp.M = static_cast<int32_t>(M);
+    gp.K = K;
+    gp.tok_tile = kMmaM;
+    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+    int rt = 16;
+    for (int j = 0; j < n; ++j) rt = std::max<int>(rt, static_cast<int>(round_up(th[j]->r, 16)));
+    gp.row_tile = rt;
+    gp.n_mma = rt;
+    if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, kMmaM, "x")) != AQ_OK) return st;
+    int tiles = 0;
+    for (int j = 0; j < n; ++j) {
+      if (th[j]->r == 0) continue;
+      GemmSeg& s = gp.seg[gp.nseg++];
+      if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, rt, "V^T")) != AQ_OK) return st;
+      s.s = nullptr;
+      s.y = tbuf + wl.t_col[j];
+      s.ldy = wl.ld_t;
+      s.rows = th[j]->r;
+      s.r = 0;
+      s.n_row_tiles = 1;
+      s.tile_begin = tiles;
+      tiles += gp.n_tok_tiles;
+    }
+    gp.total_tiles = tiles;
+    gp.prefetch_w = 0;  // V^T comes from the transpose kernel just before
+    gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
+    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
+    gp.tmem_cols = tmem_cols_for(gp.n_mma);
+    gp.status = dev->status;
+    gp.timeout_ns = kTimeoutNs;
+    const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+    const int grid = std::min(tiles, dev->sms);
+    if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch t GEMM")) != AQ_OK) return st;
+  }
+
+  // ---- prefill GEMM with the fused reconstruction epilogue ----
   GemmParams gp = {};
   gp.M = static_cast<int32_t>(M);
   gp.K = K;
-  if (decode) {
-    gp.tok_tile = static_cast<int32_t>(std::min<int64_t>(256, round_up(M, 16)));
-    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, gp.tok_tile));
-    gp.row_tile = decode_row_tile(th, n, gp.n_tok_tiles, dev->sms);
-    gp.n_mma = gp.tok_tile;
-  } else {
-    gp.tok_tile = kMmaM;
-    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
-    gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
-    gp.n_mma = gp.row_tile;
-  }
+  gp.tok_tile = kMmaM;
+  gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+  gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
+  gp.n_mma = gp.row_tile;
   if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, gp.tok_tile, "x")) != AQ_OK) return st;
   int tiles = 0;
   bool any_lr = false;
@@ -470,16 +521,14 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.total_tiles = tiles;
   gp.prefetch_w = 1;
   gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-  gp.stages = stages_for(gp.stage_bytes, decode ? std::min(dev->smem_optin, kDecodeSmemBudget) : dev->smem_optin,
-                         kHeaderBytes + kSmemSlack);
+  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
   gp.tmem_cols = tmem_cols_for(any_lr ? 2 * gp.n_mma : gp.n_mma);
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;
   const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
   const int grid = std::min(tiles, dev->sms);
-  if ((st = launch_or_fail(launch_gemm(gp, decode, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK)
-    return st;
-  t_last_path = decode ? AQ_PATH_DECODE : AQ_PATH_PREFILL;
+  if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK) return st;
+  t_last_path = AQ_PATH_PREFILL;
   return AQ_OK;
 }
 

@@ -31,9 +31,8 @@ struct GemmSeg {
   int32_t tile_begin;  // first global tile index of this segment
 };
 
-// Tile mapping: the accumulator is D[lane, col] = sum_k A[lane, k] * B[col, k].
-//   swap (decode):  A = row operand (W0 rows, `row_tile` valid lanes), B = tokens (x)
-//   normal (prefill): A = tokens (x, 128 lanes), B = row operand (`row_tile` columns)
+// Tile mapping: the accumulator is D[token, col] = sum_k x[token, k] * W[col, k], with 128
+// tokens per tile as the accumulator lanes and `row_tile` rows of the row operand as N.
 struct GemmParams {
   CUtensorMap tm_x;  // tokens operand x [M, K]
   GemmSeg seg[kMaxSeg];
@@ -44,7 +43,7 @@ struct GemmParams {
   int32_t tok_tile;     // tokens per tile (box rows of tm_x / tm_t)
   int32_t n_tok_tiles;
   int32_t total_tiles;
-  int32_t n_mma;        // MMA N: swap -> round_up(tok_tile, 16); normal -> round_up(row_tile, 16)
+  int32_t n_mma;        // MMA N: round_up(row_tile, 16)
   int32_t stages;
   int32_t prefetch_w;   // 1: the row operand is a weight and may be loaded before the
                         //    previous grid completes; 0: it is produced by that grid
@@ -54,28 +53,57 @@ struct GemmParams {
   uint64_t timeout_ns;
 };
 
-// t = V^T x for small M on CUDA cores, one thread-block cluster per (family, 32
-// columns of t, 16 tokens); the cluster splits `in` and reduces through DSMEM.
-struct DownSeg {
+// Decode (M <= kDecMaxTok tokens): each W0-streaming CTA owns a contiguous range of
+// output rows of one family over the full K; a few extra CTAs compute t = V^T x.
+constexpr int kDecThreads = 288;        // warp 0 TMA producer, warps 1..8 mma.sync consumers
+constexpr int kDecConsumers = 256;
+constexpr int kDecMaxTok = 32;          // tokens the decode kernel handles
+constexpr int kDecMaxEpiBytes = 48 * 1024;  // largest epilogue staging (sums + t)
+constexpr int kDecTCtas = 8;            // CTAs that compute t = V^T x
+// Workspace: [0, kSyncBytes) must be zero before first use and is left zero by every decode
+// call (counters and the fp32 t accumulator); scratch that needs no initialisation follows.
+constexpr size_t kSyncBytes = 128 * 1024;
+constexpr size_t kSyncTAccOffset = 32 * 1024;   // t accumulator inside the sync region
+constexpr int kMaxTAcc = static_cast<int>((kSyncBytes - kSyncTAccOffset) / 4);
+
+struct DecodeSeg {
+  CUtensorMap tm_w;    // W0 [rows, K], box {64, rows_per_chunk}
+  const uint16_t* s;
+  const uint16_t* U;
+  int64_t ldu;
   const uint16_t* V;
   int64_t ldv;
+  uint16_t* y;
+  int64_t ldy;
+  int32_t rows;
   int32_t r;
-  uint16_t* t;   // t [M, r] bf16 at column offset, row stride ldt
-  int32_t kchunks;
-  int32_t block_begin;  // first blockIdx.y of this family
+  int32_t t_col;       // first column of this family in t [M, r_total]
+  int32_t cta_begin;   // first W0-streaming CTA of this family (counted after the t CTAs)
+  int32_t chunk_rows;  // rows per chunk (TMA box rows), <= 128 (M <= 16) or 64
+  int32_t chunks;      // chunks per CTA
 };
 
-struct DownParams {
+struct DecodeParams {
+  CUtensorMap tm_x;    // x [M, K], box {64, M}: only real token rows are loaded
+  DecodeSeg seg[kMaxSeg];
   const uint16_t* x;
   int64_t ldx;
-  int64_t ldt;
+  int32_t nseg;
   int32_t M;
   int32_t K;
-  int32_t mgroups;
-  int32_t nseg;
-  int32_t csize;   // cluster size (CTAs splitting K)
-  int32_t kslice;  // K rows per CTA (multiple of 8)
-  DownSeg seg[kMaxSeg];
+  int32_t nkb;         // 64-wide k blocks
+  int32_t kbox;        // k blocks per pipeline stage
+  int32_t tok_tile;    // 16 or 32
+  int32_t r_total;
+  int32_t t_ctas;      // CTAs [0, t_ctas) compute t; the rest stream W0
+  int32_t stages;
+  uint32_t stage_bytes;
+  uint32_t wbox_bytes; // bytes of one W0 box in a stage: round_up(max chunk_rows, 8) * 128
+  uint32_t epi_bytes;  // epilogue staging: warp sums [8][16][tok_tile] + t [M][max r], 1 KB aligned
+  int32_t* counters;   // sync region: [0] t arrivals, [1] finished CTAs
+  float* t_acc;        // sync region: [M][r_total]
+  int32_t* status;
+  uint64_t timeout_ns;
 };
 
 // V [in, r] -> Vt [r, in] (bf16) for the prefill t GEMM.
@@ -115,9 +143,9 @@ struct PrecomputeParams {
 };
 
 // Launch helpers implemented in aq_kernels.cu; each returns the CUDA error of the launch.
-cudaError_t launch_gemm(const GemmParams& p, bool swap, int grid, size_t smem, cudaStream_t st,
-                        bool pdl);
-cudaError_t launch_down(const DownParams& p, int grid_y, cudaStream_t st, bool pdl);
+cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
+cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
                               bool pdl);

@@ -2,25 +2,19 @@
 //   y = s . (W0 x) + U (V^T x)         ("How attnquant works", "The reconstruction identity")
 //   W_eff = diag(s) W0 + U V^T         ("Execution paths", "Precompute-outside")
 //
-// aq_gemm_kernel<swap>   tcgen05 GEMM over the K = in loop with TMA-fed shared-memory ring;
-//                        the rank-r up-projection runs as extra K blocks into a second TMEM
-//                        accumulator and the epilogue forms s * D_main + D_low, rounded once.
-//                        swap = true (decode): output rows are the 128 accumulator lanes and
-//                        tokens the N dimension, each CTA owning a balanced slice of rows.
-//                        swap = false (prefill): 128 tokens per tile, output rows as N.
-// aq_down_kernel         t = V^T x for small M on CUDA cores; a thread-block cluster splits
-//                        `in` and reduces the partial sums through distributed shared memory.
+// aq_gemm_kernel         prefill (M > 32): tcgen05 GEMM over the K = in loop with a TMA-fed
+//                        shared-memory ring, 128 tokens per tile as accumulator lanes and
+//                        output rows as N; the rank-r up-projection runs as extra K blocks
+//                        into a second TMEM accumulator and the epilogue forms
+//                        s * D_main + D_low, rounded once. Also the t = x V GEMM.
 // aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
 // aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
 //                        epilogue, W_eff written back with TMA stores.
-#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace aq {
 
@@ -73,7 +67,6 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
   return c;
 }
 
-template <bool kSwap>
 __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -146,15 +139,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           for (; kb < pre; ++kb) {
             uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
             mbar_arrive_expect_tx(&full[kb], tx_bytes);
-            if (kSwap) tma_load_2d(st, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
-            else tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
+            tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
             filled |= 1u << kb;
           }
           pdl_wait_prior_grid();
           for (int j = 0; j < pre; ++j) {
             uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-            if (kSwap) tma_load_2d(st + kStageA, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
-            else tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
+            tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
           }
           stage = pre;
           if (stage == p.stages) {
@@ -169,22 +160,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           }
           uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
           mbar_arrive_expect_tx(&full[stage], tx_bytes);
-          const CUtensorMap* ma;
-          const CUtensorMap* mb;
-          int ka, ra, rb;
-          if (kb < nkb_main) {
-            ka = kb * kBK;
-            ma = kSwap ? &sg.tm_w : &p.tm_x;
-            mb = kSwap ? &p.tm_x : &sg.tm_w;
-          } else {
-            ka = (kb - nkb_main) * kBK;
-            ma = kSwap ? &sg.tm_u : &sg.tm_t;
-            mb = kSwap ? &sg.tm_t : &sg.tm_u;
-          }
-          ra = kSwap ? tc.row0 : tc.tok0;
-          rb = kSwap ? tc.tok0 : tc.row0;
-          tma_load_2d(st, ma, ka, ra, &full[stage], pol);
-          tma_load_2d(st + kStageA, mb, ka, rb, &full[stage], pol);
+          // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
+          const bool main_blk = kb < nkb_main;
+          const int ka = main_blk ? kb * kBK : (kb - nkb_main) * kBK;
+          tma_load_2d(st, main_blk ? &p.tm_x : &sg.tm_t, ka, tc.tok0, &full[stage], pol);
+          tma_load_2d(st + kStageA, main_blk ? &sg.tm_w : &sg.tm_u, ka, tc.row0, &full[stage], pol);
           filled |= 1u << stage;
           fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
           if (++stage == p.stages) {
@@ -265,27 +245,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       const bool has_lr = sg.r > 0;
       if (!warp_wait(tmem_full, it & 1, ctl)) break;
       tc_fence_after();
-      if (kSwap) {
-        const int row = tc.row0 + lrow;
-        const bool row_ok = lrow < p.row_tile && row < sg.rows;
-        const float sc = (row_ok && sg.s != nullptr) ? bf16_to_f32(sg.s[row]) : 1.0f;
-        for (int c = 0; c < p.n_mma; c += 16) {
-          float a[16], b[16];
-          tmem_ld_16(t_lane + c, a);
-          if (has_lr) tmem_ld_16(t_lane + p.n_mma + c, b);
-          tmem_ld_wait();
-          if (row_ok) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int tok = tc.tok0 + c + j;
-              if (c + j < p.tok_tile && tok < p.M) {
-                const float v = fmaf(sc, a[j], has_lr ? b[j] : 0.0f);
-                sg.y[static_cast<int64_t>(tok) * sg.ldy + row] = f32_to_bf16_rn(v);
-              }
-            }
-          }
-        }
-      } else {
+      {
         const int tok = tc.tok0 + lrow;
         const bool tok_ok = tok < p.M;
         uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
@@ -346,93 +306,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
-}
-
-// ------------------------------------------------------------------------------------
-// t = V^T x for small M (CUDA cores, cluster reduction over `in`)
-// ------------------------------------------------------------------------------------
-constexpr int kDownThreads = 256;
-constexpr int kDownChunk = 384;   // rows of x staged in shared memory at a time
-
-__global__ void __launch_bounds__(kDownThreads) aq_down_kernel(const __grid_constant__ DownParams p) {
-  __shared__ __align__(16) float xs[kDownChunk * 16];
-  __shared__ float red[8][16][33];
-  __shared__ float part[16 * 32];
-  cg::cluster_group cluster = cg::this_cluster();
-  const int crank = static_cast<int>(cluster.block_rank());
-  const int csize = static_cast<int>(cluster.num_blocks());
-
-  int si = 0;
-#pragma unroll
-  for (int j = 1; j < kMaxSeg; ++j)
-    if (j < p.nseg && static_cast<int>(blockIdx.y) >= p.seg[j].block_begin) si = j;
-  const DownSeg& sg = p.seg[si];
-  const int k0 = (static_cast<int>(blockIdx.y) - sg.block_begin) * 32;
-  const int m0 = static_cast<int>(blockIdx.z) * 16;
-  const int tid = threadIdx.x;
-  const int tk = tid & 31;
-  const int tg = tid >> 5;
-  const int k = k0 + tk;
-
-  pdl_launch_dependents();
-  pdl_wait_prior_grid();
-
-  float acc[16];
-#pragma unroll
-  for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
-  const int i_begin = crank * p.kslice;
-  const int i_end = min(p.K, i_begin + p.kslice);
-  for (int c0 = i_begin; c0 < i_end; c0 += kDownChunk) {
-    const int len = min(kDownChunk, i_end - c0);
-    __syncthreads();
-    for (int idx = tid; idx < 16 * len; idx += kDownThreads) {
-      const int m = idx / len;
-      const int i = idx - m * len;
-      float v = 0.0f;
-      if (m0 + m < p.M) v = bf16_to_f32(p.x[static_cast<int64_t>(m0 + m) * p.ldx + c0 + i]);
-      xs[i * 16 + m] = v;
-    }
-    __syncthreads();
-    if (k < sg.r) {
-      const uint16_t* vcol = sg.V + k;
-      for (int i = tg; i < len; i += 8) {
-        const float v = bf16_to_f32(vcol[static_cast<int64_t>(c0 + i) * sg.ldv]);
-        const float4* xr = reinterpret_cast<const float4*>(&xs[i * 16]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 xv = xr[q];
-          acc[4 * q + 0] = fmaf(v, xv.x, acc[4 * q + 0]);
-          acc[4 * q + 1] = fmaf(v, xv.y, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(v, xv.z, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(v, xv.w, acc[4 * q + 3]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < 16; ++m) red[tg][m][tk] = acc[m];
-  __syncthreads();
-  for (int idx = tid; idx < 512; idx += kDownThreads) {
-    const int m = idx >> 5;
-    const int kk = idx & 31;
-    float s = 0.0f;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) s += red[g][m][kk];
-    part[idx] = s;
-  }
-  cluster.sync();
-  // Each CTA of the cluster finishes a slice of the 16 x 32 outputs, summing the
-  // partials of all CTAs in rank order (deterministic).
-  const int per = (512 + csize - 1) / csize;
-  for (int idx = crank * per + tid; idx < min(512, (crank + 1) * per); idx += kDownThreads) {
-    float s = 0.0f;
-    for (int q = 0; q < csize; ++q) s += cluster.map_shared_rank(part, q)[idx];
-    const int m = idx >> 5;
-    const int kk = idx & 31;
-    if (m0 + m < p.M && k0 + kk < sg.r)
-      sg.t[static_cast<int64_t>(m0 + m) * p.ldt + k0 + kk] = f32_to_bf16_rn(s);
-  }
-  cluster.sync();
 }
 
 // ------------------------------------------------------------------------------------
@@ -742,18 +615,10 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_gemm(const GemmParams& p, bool swap, int grid, size_t smem, cudaStream_t st,
-                        bool pdl) {
+cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<GemmParams*>(&p)};
-  const void* fn = swap ? reinterpret_cast<const void*>(&aq_gemm_kernel<true>)
-                        : reinterpret_cast<const void*>(&aq_gemm_kernel<false>);
-  return launch_ex(fn, dim3(grid), dim3(kGemmThreads), smem, st, pdl, args);
-}
-
-cudaError_t launch_down(const DownParams& p, int grid_y, cudaStream_t st, bool pdl) {
-  void* args[] = {const_cast<DownParams*>(&p)};
-  return launch_ex(reinterpret_cast<const void*>(&aq_down_kernel), dim3(p.csize, grid_y, p.mgroups),
-                   dim3(kDownThreads), 0, st, pdl, args, dim3(p.csize, 1, 1));
+  return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel), dim3(grid), dim3(kGemmThreads), smem, st, pdl,
+                   args);
 }
 
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl) {
@@ -780,10 +645,8 @@ cudaError_t configure_kernels(int device, size_t max_smem) {
   (void)device;
   cudaError_t e;
   const int s = static_cast<int>(max_smem);
-  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
-    return e;
-  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
-    return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = configure_decode(max_smem))) return e;
   if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
     return e;
   return cudaSuccess;

@@ -18,6 +18,8 @@
 
 // The scratch area. Every GPU on which this library is used holds these bytes until the
 // process exits. All calls on a device share it; it keeps whatever the last call wrote.
+// Being a static device array it starts at zero, which is what the workspace's sync part
+// (its first AQ_WORKSPACE_SYNC_BYTES) needs; every completed call leaves that part zero.
 static __device__ __align__(256) unsigned char aq_noalloc_scratch[AQ_NOALLOC_WORKSPACE_BYTES];
 
 namespace {
@@ -73,7 +75,5 @@ extern "C" aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_
   void* scratch = nullptr;
   aq_status st = scratch_address(&scratch);
   if (st != AQ_OK) return st;
-  // Nothing in the scratch has to start at zero: every byte the kernels read is first
-  // written by the same call.
   return aq_linear(th, x, M, ldx, y, ldy, scratch, AQ_NOALLOC_WORKSPACE_BYTES, stream);
 }

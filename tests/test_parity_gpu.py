@@ -44,6 +44,17 @@ def run_linear(th, xb, path=aq.AQ_PATH_AUTO, M=None):
     return y
 
 
+def decode_refused(th, xb, path):
+    """The decode kernel takes at most aq_decode_max_m() tokens; forcing it beyond that
+    is refused before anything is launched."""
+    if path != aq.AQ_PATH_DECODE or xb.shape[0] <= aq.aq_decode_max_m():
+        return False
+    with pytest.raises(aq.AqError) as e:
+        run_linear(th, xb, path)
+    assert e.value.status == aq.binding.AQ_ERR_UNSUPPORTED
+    return True
+
+
 def test_bounded_wait_reports_timeout():
     assert aq.aq_device_status() == aq.AQ_OK
     aq.aq_selftest_bounded_wait(2000)
@@ -80,6 +91,8 @@ def test_integer_bit_exact(shape, path):
     # preconditions of exactness: t (held in bf16 between kernels) and y representable
     assert np.array_equal(oracle.round_to_bf16(t_ref), t_ref)
     assert np.array_equal(oracle.round_to_bf16(y_ref), y_ref)
+    if decode_refused(th, xb, path):
+        return
     y = run_linear(th, xb, path)
     assert aq.aq_last_path() == path
     np.testing.assert_array_equal(host_f64(y), y_ref)
@@ -123,6 +136,8 @@ def test_ragged_random(shape, path):
     out, inp, r, M = shape
     th = synth.make_theta(("rag", *shape), out, inp, r)
     xb = synth.make_x(("rag", *shape), M, inp)
+    if decode_refused(th, xb, path):
+        return
     y = run_linear(th, xb, path)
     assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, inp)), str(shape))
 
@@ -146,6 +161,23 @@ def test_padded_leading_dims_and_canaries():
         mask = np.ones_like(yb, dtype=bool)
         mask[1:M + 1, 8:8 + out] = False
         assert np.all(yb[mask] == -7.0)
+
+
+def test_workspace_shared_across_paths_stays_clean():
+    """One zero-filled workspace serves decode and prefill calls of different shapes in
+    any order; every call leaves the sync region zero."""
+    shapes = [((700, 264, 24), 7), ((300, 520, 40), 100), ((1000, 264, 8), 32), ((700, 264, 24), 1)]
+    need = max(aq.aq_linear_workspace_bytes(dev_theta(synth.make_theta(("ws", *sh), *sh)), M)
+               for sh, M in shapes)
+    ws = aq.binding.new_workspace(need, "cuda")
+    for sh, M in shapes * 2:
+        th = synth.make_theta(("ws", *sh), *sh)
+        xb = synth.make_x(("ws", M), M, sh[1])
+        y = aq.aq_linear(dev_theta(th), dev(xb)[:, : sh[1]], workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, sh[1])), str((sh, M)))
+        assert int(ws[: aq.binding.AQ_WORKSPACE_SYNC_BYTES].count_nonzero()) == 0
+    assert aq.aq_device_status() == aq.AQ_OK
 
 
 def test_m_zero_noop():

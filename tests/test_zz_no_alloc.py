@@ -55,9 +55,9 @@ def test_noalloc_matches_aq_linear_on_two_calls_in_a_row(lib):
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(lib):
-    """M = 8192 tokens at r = 256 needs more than the built-in scratch: refused with a
+    """M = 16384 tokens at r = 256 needs more than the built-in scratch: refused with a
     message before anything reaches the GPU (runs without a GPU)."""
-    out, inp, r, M = 1024, 5376, 256, 8192
+    out, inp, r, M = 1024, 5376, 256, 16384
     th = binding.c_theta(W0=0x100000, ld_w0=inp, s=0x200000, U=0x300000, ld_u=r, V=0x400000, ld_v=r,
                          out=out, in_=inp, r=r)
     need = lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, M)
