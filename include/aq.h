@@ -23,7 +23,12 @@
  *   the legacy default stream). They return once the work is enqueued. They may be
  *   captured into CUDA graphs. Kernels are launched with programmatic dependent
  *   launch so that a call's weight prefetch overlaps the tail of the previous one;
- *   activations are touched only after the previous kernel in the stream finished.
+ *   activations and the workspace are touched only after the previous kernel in the
+ *   stream finished. Weights (W0, s, U, V) may be read before then, so they must not
+ *   be written by a kernel that is still running and has released its dependents
+ *   early (griddepcontrol.launch_dependents). This library's own kernels release
+ *   early only when their outputs are activations; aq_precompute does not, so its
+ *   W_eff may serve as the very next call's W0 on the same stream.
  * - Errors: argument errors are detected on the host before anything is enqueued and
  *   returned as an aq_status; aq_last_error() then describes them (thread-local).
  *   No C++ exception crosses this interface. Faults detected on the device (a bounded

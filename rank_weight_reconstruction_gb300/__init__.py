@@ -24,5 +24,6 @@ from .binding import (  # noqa: F401
     aq_selftest_bounded_wait,
     aq_set_path,
     load,
+    new_workspace,
 )
 from .stack import StackMismatchError, ThetaStack, band_of  # noqa: F401

@@ -77,6 +77,18 @@ __device__ __forceinline__ int seg_of_cta(const DecodeParams& p, int g) {
 
 }  // namespace
 
+// Shared-memory address of 16-byte chunk `c` of k block `b`, row `r` of a stage's W0 (or
+// per-stage x) region, for the two box layouts (3-D: rows (r, b) interleaved; 2-D: one
+// box per k block), both with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t stage_addr(uint32_t base, int w3d, int kbox, uint32_t box_bytes, int r, int b,
+                                               int c) {
+  if (w3d) {
+    const int srow = r * kbox + b;
+    return base + srow * 128 + ((c ^ (srow & 7)) << 4);
+  }
+  return base + b * box_bytes + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -87,7 +99,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   int* abort_flag = reinterpret_cast<int*>(cbar + 1);
   int* bcast = abort_flag + 1;
   uint8_t* epi = smem + kHeaderBytes;
-  uint8_t* ring = epi + p.epi_bytes;
+  uint8_t* xres = epi + p.epi_bytes;
+  uint8_t* ring = xres + p.xres_bytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -107,6 +120,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   // Every streaming CTA reads the same x blocks; starting each CTA at a different k stage
   // spreads those reads over the L2 slices instead of all SMs hitting one block at once.
   const int rot = t_cta ? 0 : (g * 7) % nstage;
+  const uint32_t xbox_bytes = static_cast<uint32_t>(p.tok_tile) * 128u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -117,9 +131,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (!t_cta && warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tm_x);
-    tma_prefetch_desc(&sg.tm_w);
+  if (warp == 0 && lane == 0) {
+    if (t_cta) {
+      tma_prefetch_desc(&p.tm_xt);
+      for (int j = 0; j < p.nseg; ++j)
+        if (p.seg[j].r > 0) tma_prefetch_desc(&p.seg[j].tm_v);
+    } else {
+      tma_prefetch_desc(&sg.tm_w);
+      if (!p.x_res) tma_prefetch_desc(&p.tm_x);
+    }
   }
   // The next kernel in the stream may now be scheduled and start its own weight
   // prefetch; it touches activations and workspace only after this grid completes.
@@ -129,8 +149,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   if (warp == 0) {
     // ---------------- TMA producer (streaming CTAs) ----------------
     if (!t_cta && lane == 0) {
-      const uint64_t pol = policy_evict_normal();
-      // the CTA's (chunk, stage) sequence
       int total = 0;
       for (int ch = 0; ch < sg.chunks; ++ch)
         if ((l * sg.chunks + ch) * R < sg.rows) total += nstage;
@@ -138,20 +156,32 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       uint32_t filled = 0, fill_par = 0;
       auto issue = [&](int q, int slot, bool weights, bool acts) {
         const int ch = q / nstage;
-        const int st = (q - ch * nstage + rot) % nstage;   // rotated k order (see rot)
+        const int st = (q - ch * nstage + rot) % nstage;
         const int row0 = (l * sg.chunks + ch) * R;
         const int kb0 = st * p.kbox;
         const int nb = min(p.kbox, p.nkb - kb0);
         uint8_t* base = ring + static_cast<size_t>(slot) * p.stage_bytes;
+        uint8_t* xbase = base + p.wregion;
         if (weights) {
-          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nb) * (R + p.M) * 128u);
-          for (int b = 0; b < nb; ++b)
-            tma_load_2d(base + b * p.wbox_bytes, &sg.tm_w, (kb0 + b) * kBK, row0, &full[slot], pol);
+          // a 3-D box always covers kbox blocks (those past K read as zeros and still count)
+          const uint32_t nbox = p.w3d ? static_cast<uint32_t>(p.kbox) : static_cast<uint32_t>(nb);
+          const uint32_t xb = p.x_res ? 0u : static_cast<uint32_t>(p.M) * 128u;
+          mbar_arrive_expect_tx(&full[slot], nbox * (static_cast<uint32_t>(R) * 128u + xb));
+          if (p.w3d) {
+            tma_load_3d(base, &sg.tm_w, 0, kb0, row0, &full[slot]);
+          } else {
+            for (int b = 0; b < nb; ++b)
+              tma_load_2d_plain(base + b * p.wbox_bytes, &sg.tm_w, (kb0 + b) * kBK, row0, &full[slot]);
+          }
         }
-        if (acts)
-          for (int b = 0; b < nb; ++b)
-            tma_load_2d(base + p.kbox * p.wbox_bytes + b * p.tok_tile * 128, &p.tm_x, (kb0 + b) * kBK, 0,
-                        &full[slot], pol);
+        if (acts && !p.x_res) {
+          if (p.w3d) {
+            tma_load_3d(xbase, &p.tm_x, 0, kb0, 0, &full[slot]);
+          } else {
+            for (int b = 0; b < nb; ++b)
+              tma_load_2d_plain(xbase + b * xbox_bytes, &p.tm_x, (kb0 + b) * kBK, 0, &full[slot]);
+          }
+        }
       };
       // W0 of the first stages goes out before waiting on the previous grid.
       for (int q = 0; q < pre; ++q) {
@@ -191,103 +221,91 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     const int gq = lane >> 2, qq = lane & 3;
     uint32_t cph = 0;
     bool ok = true;
-    pdl_wait_prior_grid();
 
     if (t_cta) {
-      // ---- t = V^T x over this CTA's slice of `in` ----
-      const int ks = (p.K + p.t_ctas - 1) / p.t_ctas;
+      // ---- t = V^T x over this CTA's slice of `in`, staged by TMA ----
+      // slices start on a multiple of 8 elements: a TMA box's innermost coordinate must
+      // be 16-byte aligned
+      const int ks = ((p.K + p.t_ctas - 1) / p.t_ctas + 7) & ~7;
       const int i0 = cta * ks;
       const int i1 = min(p.K, i0 + ks);
-      const int rp = (p.r_total + 3) & ~3;             // padded t width (4-wide blocks)
       const int ntot = p.M * p.r_total;
-      float* tacc = reinterpret_cast<float*>(epi);       // [M][r_total]   (<= 96 KB spans into the ring)
+      float* tacc = reinterpret_cast<float*>(epi);                 // [M][r_total], fp32
       const int tacc_bytes = (ntot * 4 + 1023) & ~1023;
-      uint8_t* stage_area = epi + tacc_bytes;
-      const int cap = static_cast<int>(p.epi_bytes) + p.stages * static_cast<int>(p.stage_bytes) - tacc_bytes;
-      const int chunk = max(1, min(cap / (kDecMaxTok * 4 + rp * 2), 1 << 20));
-      float* xs = reinterpret_cast<float*>(stage_area);                          // [chunk][32]
-      uint16_t* vs = reinterpret_cast<uint16_t*>(stage_area + chunk * kDecMaxTok * 4);  // [chunk][rp]
+      uint8_t* stage_area = epi + tacc_bytes;                        // V rows, then x rows
+      uint8_t* xsb = stage_area + p.t_rows * p.r8_total * 2;         // [M][t_rows] bf16
       for (int idx = ct; idx < ntot; idx += kDecConsumers) tacc[idx] = 0.0f;
-      // thread -> (4 tokens x 4 columns) block and a residue class of rows
-      const int mb = (p.M + 3) / 4, kbk = rp / 4;
-      const int blocks = mb * kbk;
-      const int igroups = max(1, kDecConsumers / blocks);
-      const int blk = ct % blocks, ig = ct / blocks;
-      const bool worker = blocks <= kDecConsumers ? (ig < igroups) : true;
+      // thread -> (family, 4 tokens x 4 columns) block, and a residue class of rows
+      const int mb = (p.M + 3) / 4;
+      int blocks = 0;
+      for (int j = 0; j < p.nseg; ++j) blocks += mb * (p.seg[j].r8 / 4);
+      const bool few = blocks <= kDecConsumers;
+      const int igroups = few ? kDecConsumers / blocks : 1;
+      const int ig = few ? ct / blocks : 0;
+      const bool worker = few ? ig < igroups : true;
+      const uint32_t vbytes = static_cast<uint32_t>(p.t_rows) * p.r8_total * 2u;
+      const uint32_t xbytes = static_cast<uint32_t>(p.t_rows) * p.M * 2u;
       float acc[4][4];
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
-      for (int a = i0; ok && a < i1; a += chunk) {
-        const int n = min(chunk, i1 - a);
-        if (!(ok = cons_sync(cbar, cph, ctl))) break;
-        // staging loads, eight in flight per thread
-        for (int base = ct; base < n * kDecMaxTok; base += 8 * kDecConsumers) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kDecConsumers;
-            const int m = idx / n, i = idx - m * n;
-            v[u] = (idx < n * kDecMaxTok && m < p.M) ? bf16_to_f32(p.x[static_cast<int64_t>(m) * p.ldx + a + i]) : 0.0f;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kDecConsumers;
-            if (idx < n * kDecMaxTok) {
-              const int m = idx / n, i = idx - m * n;
-              xs[i * kDecMaxTok + m] = v[u];
-            }
-          }
+      int my_j = 0, my_m0 = 0, my_k0 = 0, my_vcol = 0;
+      auto locate = [&](int blk) {
+        int j = 0, rest = blk, vcol = 0;
+        while (j < p.nseg - 1 && rest >= mb * (p.seg[j].r8 / 4)) {
+          rest -= mb * (p.seg[j].r8 / 4);
+          vcol += p.seg[j].r8;
+          ++j;
         }
-        for (int idx = ct; idx < n * (rp - p.r_total); idx += kDecConsumers) {
-          const int i = idx / (rp - p.r_total), k = idx - i * (rp - p.r_total);
-          vs[i * rp + p.r_total + k] = 0;
-        }
-        for (int j = 0; j < p.nseg; ++j) {
-          const DecodeSeg& sj = p.seg[j];
-          const int tot = n * sj.r;
-          for (int base = ct; base < tot; base += 8 * kDecConsumers) {
-            uint16_t v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int idx = base + u * kDecConsumers;
-              const int i = idx / sj.r, k = idx - i * sj.r;
-              v[u] = idx < tot ? sj.V[static_cast<int64_t>(a + i) * sj.ldv + k] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int idx = base + u * kDecConsumers;
-              if (idx < tot) {
-                const int i = idx / sj.r, k = idx - i * sj.r;
-                vs[i * rp + sj.t_col + k] = v[u];
-              }
-            }
+        my_j = j;
+        my_m0 = (rest / (p.seg[j].r8 / 4)) * 4;
+        my_k0 = (rest % (p.seg[j].r8 / 4)) * 4;
+        my_vcol = vcol;
+      };
+      uint32_t tph = 0;
+      for (int a = i0, first = 1; ok && a < i1; a += p.t_rows, first = 0) {
+        const int n = min(p.t_rows, i1 - a);
+        if (!first && !(ok = cons_sync(cbar, cph, ctl))) break;   // staging free again
+        if (ct == 0) {
+          mbar_arrive_expect_tx(&full[0], vbytes + xbytes);
+          int col = 0;
+          for (int j = 0; j < p.nseg; ++j) {
+            if (p.seg[j].r > 0)
+              tma_load_2d_plain(stage_area + static_cast<size_t>(p.t_rows) * col * 2, &p.seg[j].tm_v, 0, a,
+                                &full[0]);
+            col += p.seg[j].r8;
           }
+          if (first) pdl_wait_prior_grid();
+          tma_load_2d_plain(xsb, &p.tm_xt, a, 0, &full[0]);
         }
-        if (!(ok = cons_sync(cbar, cph, ctl))) break;
-        // blocks beyond the thread count (very wide t) loop over several blocks
-        for (int b2 = blk; b2 < blocks; b2 += (blocks <= kDecConsumers ? blocks : kDecConsumers)) {
-          if (!worker) break;
-          const int m0 = (b2 / kbk) * 4, k0 = (b2 % kbk) * 4;
+        if (first) pdl_wait_prior_grid();
+        if (!(ok = mbar_wait(&full[0], tph, ctl))) break;
+        tph ^= 1u;
+        for (int blk = (few ? ct % blocks : ct); worker && blk < blocks; blk += (few ? blocks : kDecConsumers)) {
+          locate(blk);
+          const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage_area) +
+                               static_cast<size_t>(p.t_rows) * my_vcol;     // [t_rows][r8_j]
+          const int r8 = p.seg[my_j].r8;
+          const uint16_t* xs = reinterpret_cast<const uint16_t*>(xsb);      // [M][t_rows]
           float lacc[4][4];
 #pragma unroll
           for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
             for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = 0.0f;
-          for (int i = (blocks <= kDecConsumers ? ig : 0); i < n; i += (blocks <= kDecConsumers ? igroups : 1)) {
-            const float4 xv = *reinterpret_cast<const float4*>(&xs[i * kDecMaxTok + m0]);
-            const uint2 vv = *reinterpret_cast<const uint2*>(&vs[i * rp + k0]);
-            const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xFFFF0000u);
-            const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xFFFF0000u);
-            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
-            const float va[4] = {v0, v1, v2, v3};
+          for (int i = ig; i < n; i += igroups) {
+            const uint2 vv = *reinterpret_cast<const uint2*>(vs + i * r8 + my_k0);
+            const float va[4] = {__uint_as_float(vv.x << 16), __uint_as_float(vv.x & 0xFFFF0000u),
+                                 __uint_as_float(vv.y << 16), __uint_as_float(vv.y & 0xFFFF0000u)};
 #pragma unroll
-            for (int x0 = 0; x0 < 4; ++x0)
+            for (int x0 = 0; x0 < 4; ++x0) {
+              const int m = my_m0 + x0;
+              const float xv = m < p.M ? bf16_to_f32(xs[m * p.t_rows + i]) : 0.0f;
 #pragma unroll
-              for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = fmaf(xa[x0], va[y0], lacc[x0][y0]);
+              for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = fmaf(xv, va[y0], lacc[x0][y0]);
+            }
           }
-          if (blocks <= kDecConsumers) {
+          if (few) {
 #pragma unroll
             for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
@@ -297,20 +315,22 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
               for (int y0 = 0; y0 < 4; ++y0) {
-                const int m = m0 + x0, k = k0 + y0;
-                if (m < p.M && k < p.r_total) atomicAdd(&tacc[m * p.r_total + k], lacc[x0][y0]);
+                const int m = my_m0 + x0, k = my_k0 + y0;
+                if (m < p.M && k < p.seg[my_j].r)
+                  atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
               }
           }
         }
       }
-      if (ok && blocks <= kDecConsumers && worker) {
-        const int m0 = (blk / kbk) * 4, k0 = (blk % kbk) * 4;
+      if (i0 >= i1) pdl_wait_prior_grid();
+      if (ok && few && worker) {
+        locate(ct % blocks);
 #pragma unroll
         for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
           for (int y0 = 0; y0 < 4; ++y0) {
-            const int m = m0 + x0, k = k0 + y0;
-            if (m < p.M && k < p.r_total) atomicAdd(&tacc[m * p.r_total + k], acc[x0][y0]);
+            const int m = my_m0 + x0, k = my_k0 + y0;
+            if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], acc[x0][y0]);
           }
       }
       if (ok) ok = cons_sync(cbar, cph, ctl);
@@ -321,6 +341,41 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         if (ok && ct == 0) atomicAdd(&p.counters[0], 1);
       }
     } else {
+      pdl_wait_prior_grid();
+      // ---- x resident in shared memory (dense rows, zero beyond K) ----
+      if (p.x_res) {
+        uint16_t* xs = reinterpret_cast<uint16_t*>(xres);
+        const int kp = p.nkb * kBK;
+        if ((p.K & 7) == 0) {
+          const int per_row = kp / 8;
+          const int tot = p.M * per_row;
+          for (int base = ct; base < tot; base += 8 * kDecConsumers) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + u * kDecConsumers;
+              const int m = idx / per_row, c8 = idx - m * per_row;
+              v[u] = (idx < tot && c8 * 8 < p.K)
+                         ? __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.ldx) + c8)
+                         : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + u * kDecConsumers;
+              if (idx < tot) {
+                const int m = idx / per_row, c8 = idx - m * per_row;
+                *reinterpret_cast<uint4*>(xs + m * p.xs_ld + c8 * 8) = v[u];
+              }
+            }
+          }
+        } else {
+          for (int idx = ct; idx < p.M * kp; idx += kDecConsumers) {
+            const int m = idx / kp, k = idx - m * kp;
+            xs[m * p.xs_ld + k] = k < p.K ? p.x[static_cast<int64_t>(m) * p.ldx + k] : 0;
+          }
+        }
+        ok = cons_sync(cbar, cph, ctl);
+      }
       // ---- stream this CTA's rows of W0 ----
       const int nslab = (R + 15) / 16;
       const int kg = 8 / nslab;                 // warps sharing one slab (split over K)
@@ -328,6 +383,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       const int slab = cw / kg, kgi = cw - slab * kg;
       float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
       float* ts = red + 8 * 16 * kTok;                       // [M][r]
+      const uint32_t xres_base = smem_u32(xres);
       int slot = 0;
       uint32_t phase = 0;
       for (int ch = 0; ok && ch < sg.chunks; ++ch) {
@@ -346,23 +402,38 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
           const int st = (sq + rot) % nstage;
           const int nb = min(p.kbox, p.nkb - st * p.kbox);
           if (active) {
-            const uint32_t sbase = smem_u32(ring + static_cast<size_t>(slot) * p.stage_bytes);
+            const uint32_t wbase = smem_u32(ring + static_cast<size_t>(slot) * p.stage_bytes);
+            const uint32_t xbase = wbase + p.wregion;
             for (int step = kgi; step < nb * 4; step += kg) {
               const int b = step >> 2, j = step & 3;
-              const uint32_t abase = sbase + b * p.wbox_bytes;
-              const uint32_t bbase = sbase + p.kbox * p.wbox_bytes + b * p.tok_tile * 128;
-              const int arow = 16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8;
-              const int achunk = 2 * j + (lane >> 4);
+              // rows past the chunk read row R-1 again (their sums are dropped), so a
+              // stage holds exactly the chunk's rows
+              const int arow = min(16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8, R - 1);
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(abase + arow * 128 + ((achunk ^ (arow & 7)) << 4), a0, a1, a2, a3);
+              ldsm_x4(stage_addr(wbase, p.w3d, p.kbox, p.wbox_bytes, arow, b, 2 * j + (lane >> 4)), a0, a1, a2, a3);
+              if (p.x_res) {
+                const int k0 = (st * p.kbox + b) * kBK + j * 16 + 2 * qq;
 #pragma unroll
-              for (int np = 0; np < NT / 2; ++np) {
-                const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
-                const int bchunk = 2 * j + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(bbase + brow * 128 + ((bchunk ^ (brow & 7)) << 4), b0, b1, b2, b3);
-                mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                for (int nt = 0; nt < NT; ++nt) {
+                  const int m = 8 * nt + gq;
+                  uint32_t b0 = 0, b1 = 0;
+                  if (m < p.M) {
+                    const uint32_t ad = xres_base + (m * p.xs_ld + k0) * 2;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(ad));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(ad + 16));
+                  }
+                  mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+                }
+              } else {
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                  const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
+                  uint32_t b0, b1, b2, b3;
+                  ldsm_x4(stage_addr(xbase, p.w3d, p.kbox, xbox_bytes, brow, b, 2 * j + ((lane >> 3) & 1)), b0, b1,
+                          b2, b3);
+                  mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                  mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                }
               }
             }
           }
@@ -392,7 +463,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             bool ready = true;
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire_gpu(&p.counters[0]) < p.t_ctas) {
-              __nanosleep(256);   // many CTAs poll one word: keep the line free for the arrivals
+              __nanosleep(128);   // many CTAs poll one word: keep the line free for the arrivals
               if (*reinterpret_cast<volatile int*>(abort_flag) || global_timer_ns() - t0 > p.timeout_ns) {
                 *reinterpret_cast<volatile int*>(abort_flag) = 1;
                 atomicExch(p.status, kStatusTimeout);

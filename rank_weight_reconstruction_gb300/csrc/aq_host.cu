@@ -129,6 +129,47 @@ aq_status tmap_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer
   return AQ_OK;
 }
 
+// bf16 matrix [outer, inner] with row stride ld, box {box_inner, box_outer}, no swizzle
+// (rows land densely in shared memory); out-of-bounds elements read as zero.
+aq_status tmap_2d_plain(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+                        int box_outer, const char* what) {
+  aq_status st;
+  EncodeTiledFn fn = encode_fn(&st);
+  if (!fn) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(AQ_ERR_CUDA, "cuTensorMapEncodeTiled(%s: %lld x %lld, ld %lld, box %d x %d) failed: %d", what,
+                (long long)outer, (long long)inner, (long long)ld, box_outer, box_inner, (int)r);
+  return AQ_OK;
+}
+
+// bf16 matrix [outer, inner] (inner a multiple of 64) seen as [outer, inner / 64, 64], box
+// {64, box_mid, box_outer}, 128-byte swizzle: one request fetches box_mid consecutive
+// 64-wide blocks of box_outer rows.
+aq_status tmap_3d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_mid,
+                  int box_outer, const char* what) {
+  aq_status st;
+  EncodeTiledFn fn = encode_fn(&st);
+  if (!fn) return st;
+  cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(inner / 64), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {128u, static_cast<cuuint64_t>(ld) * 2u};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_mid), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(AQ_ERR_CUDA, "cuTensorMapEncodeTiled(%s 3-D: %lld x %lld, ld %lld, box %d x %d) failed: %d", what,
+                (long long)outer, (long long)inner, (long long)ld, box_outer, box_mid, (int)r);
+  return AQ_OK;
+}
+
 // ---------------------------------------------------------------------------------
 // validation helpers
 // ---------------------------------------------------------------------------------
@@ -361,7 +402,14 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.nkb = static_cast<int32_t>(ceil_div(K, kBK));
     dp.tok_tile = M <= 16 ? 16 : 32;
     dp.r_total = wl.r_total;
-    dp.t_ctas = wl.r_total > 0 ? static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(kDecTCtas, K / 64))) : 0;
+    dp.w3d = (K % kBK) == 0 ? 1 : 0;
+    // t CTAs: about 32 KB of V each, at most kDecMaxTCtas, at least 8 rows of `in` each
+    int64_t v_bytes = 0;
+    for (int j = 0; j < n; ++j) v_bytes += static_cast<int64_t>(th[j]->r) * K * 2;
+    dp.t_ctas = wl.r_total > 0
+                    ? static_cast<int32_t>(std::max<int64_t>(
+                          1, std::min<int64_t>({kDecMaxTCtas, ceil_div(v_bytes, 32 * 1024), ceil_div(K, 8)})))
+                    : 0;
     int64_t rows_total = 0;
     for (int j = 0; j < n; ++j) rows_total += th[j]->out;
     // streaming CTAs: one per remaining SM, at least 8 rows each, shared among the families
@@ -380,15 +428,15 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       ++cnt[best];
       ++used;
     }
-    int max_rows = 8;
+    int max_rows = 8, max_r = 0;
     int cta_begin = 0;
+    int64_t max_share = 0;
     for (int j = 0; j < n; ++j) {
       DecodeSeg& sg = dp.seg[dp.nseg++];
       const int64_t per = ceil_div(th[j]->out, cnt[j]);
       sg.chunks = static_cast<int32_t>(ceil_div(per, kMmaM));
       sg.chunk_rows = static_cast<int32_t>(ceil_div(th[j]->out, static_cast<int64_t>(cnt[j]) * sg.chunks));
       cnt[j] = static_cast<int>(ceil_div(th[j]->out, static_cast<int64_t>(sg.chunk_rows) * sg.chunks));  // CTAs with rows
-      if ((st = tmap_2d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, sg.chunk_rows, "W0")) != AQ_OK) return st;
       sg.s = static_cast<const uint16_t*>(th[j]->s);
       sg.U = static_cast<const uint16_t*>(th[j]->U);
       sg.ldu = th[j]->ld_u;
@@ -398,40 +446,72 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       sg.ldy = ldys[j];
       sg.rows = th[j]->out;
       sg.r = th[j]->r;
+      sg.r8 = static_cast<int32_t>(round_up(th[j]->r, 8));
       sg.t_col = wl.dec_t_col[j];
       sg.cta_begin = cta_begin;
       cta_begin += cnt[j];
       max_rows = std::max(max_rows, static_cast<int>(sg.chunk_rows));
+      max_r = std::max(max_r, th[j]->r);
+      dp.r8_total += sg.r8;
+      max_share = std::max<int64_t>(max_share, static_cast<int64_t>(sg.chunk_rows) * sg.chunks * K * 2);
     }
-    if ((st = tmap_2d(&dp.tm_x, x, K, M, ldx, static_cast<int>(M), "x")) != AQ_OK) return st;
+    const int64_t kp = static_cast<int64_t>(dp.nkb) * kBK;
+    dp.xs_ld = static_cast<int32_t>(kp + 8);
+    dp.x_res = M * (kp + 8) * 2 <= 64 * 1024 ? 1 : 0;
+    dp.xres_bytes = dp.x_res ? static_cast<uint32_t>(round_up(M * (kp + 8) * 2, 1024)) : 0u;
+    // 2-D boxes must start on 1 KB (128-byte swizzle atoms of 8 rows): round rows to 8
     dp.wbox_bytes = static_cast<uint32_t>(round_up(max_rows, 8) * 128);
-    dp.kbox = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(8, 16384 / dp.wbox_bytes)));
-    dp.kbox = std::min(dp.kbox, dp.nkb);
-    dp.stage_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * (dp.wbox_bytes + dp.tok_tile * 128), 1024));
-    int max_r = 0;
-    for (int j = 0; j < n; ++j) max_r = std::max(max_r, th[j]->r);
+    dp.kbox = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>({8, (32 * 1024) / dp.wbox_bytes, dp.nkb})));
+    dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
+    dp.stage_bytes = static_cast<uint32_t>(
+        round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
     dp.epi_bytes = static_cast<uint32_t>(round_up(8 * 16 * dp.tok_tile * 4 + M * max_r * 4, 1024));
-    // A t CTA stages the fp32 t block plus rows of x and V in the same space.
-    const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
-    const int64_t t_need = tacc_bytes + 64 * (kDecMaxTok * 4 + 2 * (wl.r_total + 3));
-    // Two CTAs per SM when they fit in about half of the shared memory, so the next call's
-    // CTAs can start streaming W0 while this call's finish; otherwise one large ring.
-    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes;
-    const size_t half = std::min<size_t>(dev->smem_optin, 227 * 1024) / 2 - 1024;
-    int stages2 = static_cast<int>((half - std::min(half, fixed)) / dp.stage_bytes);
-    if (stages2 >= 3 && static_cast<int64_t>(dp.epi_bytes) + stages2 * static_cast<int64_t>(dp.stage_bytes) >= t_need) {
+    // Two CTAs per SM when a CTA's W0 share is small (the next call's CTAs then stream W0
+    // while this call's finish); one CTA with a deep ring when the share is large.
+    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes;
+    const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
+    const size_t half = cap / 2 - 1024;
+    const int stages2 = fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
+    if (max_share <= 128 * 1024 && stages2 >= 2)
       dp.stages = std::min(stages2, kMaxStages);
-    } else {
+    else
       dp.stages = stages_for(dp.stage_bytes, dev->smem_optin, fixed);
-      if (static_cast<int64_t>(dp.epi_bytes) + static_cast<int64_t>(dp.stages) * dp.stage_bytes < t_need)
+    // t CTAs stage rows of V (all families) and of x in the same shared memory
+    const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
+    const int64_t tspace = static_cast<int64_t>(dp.epi_bytes) + dp.xres_bytes +
+                           static_cast<int64_t>(dp.stages) * dp.stage_bytes - tacc_bytes;
+    if (dp.t_ctas > 0) {
+      const int64_t ks = round_up(ceil_div(K, dp.t_ctas), 8);   // the kernel's slice length
+      const int64_t fit = tspace / (dp.r8_total * 2 + M * 2);
+      dp.t_rows = static_cast<int32_t>(std::min<int64_t>({256, round_up(ks, 8), fit / 8 * 8}));
+      if (dp.t_rows < 8)
         return fail(AQ_ERR_UNSUPPORTED, "%s: M x total rank too large for the decode kernel's shared memory", who);
+      if ((st = tmap_2d_plain(&dp.tm_xt, x, K, M, ldx, dp.t_rows, static_cast<int>(M), "x (t)")) != AQ_OK) return st;
+    }
+    for (int j = 0; j < n; ++j) {
+      DecodeSeg& sg = dp.seg[j];
+      if (dp.w3d) {
+        if ((st = tmap_3d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, dp.kbox, sg.chunk_rows, "W0")) != AQ_OK)
+          return st;
+      } else if ((st = tmap_2d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, sg.chunk_rows, "W0")) != AQ_OK) {
+        return st;
+      }
+      if (th[j]->r > 0 && (st = tmap_2d_plain(&sg.tm_v, th[j]->V, th[j]->r, K, th[j]->ld_v, sg.r8, dp.t_rows, "V")) != AQ_OK)
+        return st;
+    }
+    if (!dp.x_res) {
+      if (dp.w3d) {
+        if ((st = tmap_3d(&dp.tm_x, x, K, M, ldx, dp.kbox, static_cast<int>(M), "x")) != AQ_OK) return st;
+      } else if ((st = tmap_2d(&dp.tm_x, x, K, M, ldx, static_cast<int>(M), "x")) != AQ_OK) {
+        return st;
+      }
     }
     dp.counters = reinterpret_cast<int32_t*>(wsb);
     dp.t_acc = reinterpret_cast<float*>(wsb + kSyncTAccOffset);
     dp.status = dev->status;
     dp.timeout_ns = kTimeoutNs;
     const int grid = dp.t_ctas + cta_begin;
-    const size_t smem = kSmemSlack + kHeaderBytes + dp.epi_bytes + static_cast<size_t>(dp.stages) * dp.stage_bytes;
+    const size_t smem = fixed + static_cast<size_t>(dp.stages) * dp.stage_bytes;
     if ((st = launch_or_fail(launch_decode(dp, grid, smem, cs, true), "launch decode kernel")) != AQ_OK) return st;
     t_last_path = AQ_PATH_DECODE;
     return AQ_OK;

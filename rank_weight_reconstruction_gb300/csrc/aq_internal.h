@@ -59,7 +59,7 @@ constexpr int kDecThreads = 288;        // warp 0 TMA producer, warps 1..8 mma.s
 constexpr int kDecConsumers = 256;
 constexpr int kDecMaxTok = 32;          // tokens the decode kernel handles
 constexpr int kDecMaxEpiBytes = 48 * 1024;  // largest epilogue staging (sums + t)
-constexpr int kDecTCtas = 8;            // CTAs that compute t = V^T x
+constexpr int kDecMaxTCtas = 16;        // most CTAs that compute t = V^T x
 // Workspace: [0, kSyncBytes) must be zero before first use and is left zero by every decode
 // call (counters and the fp32 t accumulator); scratch that needs no initialisation follows.
 constexpr size_t kSyncBytes = 128 * 1024;
@@ -67,7 +67,9 @@ constexpr size_t kSyncTAccOffset = 32 * 1024;   // t accumulator inside the sync
 constexpr int kMaxTAcc = static_cast<int>((kSyncBytes - kSyncTAccOffset) / 4);
 
 struct DecodeSeg {
-  CUtensorMap tm_w;    // W0 [rows, K], box {64, rows_per_chunk}
+  CUtensorMap tm_w;    // W0: 3-D view {64, K/64, rows} with box {64, kbox, chunk_rows} when w3d,
+                       // else 2-D [rows, K] with box {64, chunk_rows}; 128-byte swizzle
+  CUtensorMap tm_v;    // V [in, r]: 2-D, no swizzle, box {r8, t_rows} (t CTAs)
   const uint16_t* s;
   const uint16_t* U;
   int64_t ldu;
@@ -77,14 +79,16 @@ struct DecodeSeg {
   int64_t ldy;
   int32_t rows;
   int32_t r;
+  int32_t r8;          // round_up(r, 8): width of this family's V rows in a t CTA's staging
   int32_t t_col;       // first column of this family in t [M, r_total]
   int32_t cta_begin;   // first W0-streaming CTA of this family (counted after the t CTAs)
-  int32_t chunk_rows;  // rows per chunk (TMA box rows), <= 128 (M <= 16) or 64
+  int32_t chunk_rows;  // rows per chunk (TMA box rows), <= 128
   int32_t chunks;      // chunks per CTA
 };
 
 struct DecodeParams {
-  CUtensorMap tm_x;    // x [M, K], box {64, M}: only real token rows are loaded
+  CUtensorMap tm_x;    // x per stage (when !x_res): like tm_w with M rows
+  CUtensorMap tm_xt;   // x for t CTAs: 2-D, no swizzle, box {t_rows, M}
   DecodeSeg seg[kMaxSeg];
   const uint16_t* x;
   int64_t ldx;
@@ -93,13 +97,20 @@ struct DecodeParams {
   int32_t K;
   int32_t nkb;         // 64-wide k blocks
   int32_t kbox;        // k blocks per pipeline stage
+  int32_t w3d;         // 1: W0 / x stages are single 3-D boxes (K is a multiple of 64)
+  int32_t x_res;       // 1: x resident in shared memory for the whole call
+  int32_t xs_ld;       // row stride (elements) of resident x: round_up(K, 64) + 8
   int32_t tok_tile;    // 16 or 32
   int32_t r_total;
   int32_t t_ctas;      // CTAs [0, t_ctas) compute t; the rest stream W0
+  int32_t t_rows;      // rows of `in` a t CTA stages at a time (multiple of 8, <= 256)
+  int32_t r8_total;    // sum of r8 over the families
   int32_t stages;
   uint32_t stage_bytes;
-  uint32_t wbox_bytes; // bytes of one W0 box in a stage: round_up(max chunk_rows, 8) * 128
+  uint32_t wregion;    // bytes of the W0 part of a stage: kbox * wbox_bytes, 1 KB aligned
+  uint32_t wbox_bytes; // bytes of one 64-wide k block of W0 rows: round_up(max chunk_rows, 8) * 128
   uint32_t epi_bytes;  // epilogue staging: warp sums [8][16][tok_tile] + t [M][max r], 1 KB aligned
+  uint32_t xres_bytes; // resident x bytes (0 if !x_res), 1 KB aligned
   int32_t* counters;   // sync region: [0] t arrivals, [1] finished CTAs
   float* t_acc;        // sync region: [M][r_total]
   int32_t* status;

@@ -397,7 +397,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
-  pdl_launch_dependents();
+  // No early trigger of dependents here: the next call may read W_eff as its W0, and the
+  // linear kernels fetch W0 before their dependency wait. Without the trigger the next
+  // kernel starts only after every CTA has exited, its bulk stores complete.
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -372,6 +372,35 @@ def test_weight_then_dense_matches_identity():
     assert_close(y.double().cpu().numpy(), oracle.linear(*th.f64(), x_f64(xb, 1024)))
 
 
+@pytest.mark.parametrize("M", [1, 200])
+def test_precompute_then_linear_on_same_stream(M):
+    """W_eff built by aq_precompute serves as W0 of the very next call on the same stream
+    (no synchronisation, no kernel in between). The linear kernels fetch W0 before their
+    dependency wait, so this only holds because precompute does not release its
+    dependents early: a stale read would see the NaN fill."""
+    out, inp, r = 2304, 1536, 32
+    th = synth.make_theta(("pre-chain", M), out, inp, r)
+    xb = synth.make_x(("pre-chain", M), M, inp)
+    x = dev(xb)[:, :inp]
+    W = torch.full((out, inp), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ones = torch.ones(out, dtype=torch.bfloat16, device="cuda")
+    dense = aq.Theta(W0=W, s=ones)
+    ws = aq.new_workspace(aq.aq_linear_workspace_bytes(dense, M), "cuda")
+    y1 = torch.empty((M, out), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    aq.aq_precompute(dev_theta(th), W_eff=W)
+    aq.aq_linear(dense, x, y=y1, workspace=ws)
+    torch.cuda.synchronize()
+    y2 = aq.aq_linear(dense, x, workspace=ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(y1), bits(y2))
+    assert_weight_ok(W, th)
+    # the second call is a plain dense product over the W that was built
+    Wf = host_f64(W)
+    ref = oracle.linear(Wf, np.ones(out), np.zeros((out, 0)), np.zeros((inp, 0)), x_f64(xb, inp))
+    assert_close(host_f64(y1), ref)
+
+
 @pytest.mark.parametrize("shape", ["square", "wide"])
 def test_31b_band_precompute(shape):
     """60-layer stack with G = 4 bands: the first and last layer (bands 0 and 3) checked
