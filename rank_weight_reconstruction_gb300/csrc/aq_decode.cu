@@ -37,6 +37,12 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
+// Transposed load of two 8x8 b16 tiles (rows given by lanes 0..15): the B fragment of
+// m16n8k16 from a [k][n] row-major tile.
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -96,11 +102,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint64_t* cbar = empty + kMaxStages;
-  int* abort_flag = reinterpret_cast<int*>(cbar + 1);
+  uint64_t* vbar = cbar + 1;
+  int* abort_flag = reinterpret_cast<int*>(vbar + 1);
   int* bcast = abort_flag + 1;
   uint8_t* epi = smem + kHeaderBytes;
   uint8_t* xres = epi + p.epi_bytes;
-  uint8_t* ring = xres + p.xres_bytes;
+  uint8_t* vres = xres + p.xres_bytes;
+  uint8_t* ring = vres + p.vres_bytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -121,6 +129,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   // spreads those reads over the L2 slices instead of all SMs hitting one block at once.
   const int rot = t_cta ? 0 : (g * 7) % nstage;
   const uint32_t xbox_bytes = static_cast<uint32_t>(p.tok_tile) * 128u;
+  const bool local_t = !t_cta && p.t_local && sg.r > 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -128,6 +137,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       mbar_init(&empty[s], kDecConsumers / 32);
     }
     mbar_init(cbar, kDecConsumers);
+    mbar_init(vbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     } else {
       tma_prefetch_desc(&sg.tm_w);
       if (!p.x_res) tma_prefetch_desc(&p.tm_x);
+      if (local_t) tma_prefetch_desc(&sg.tm_v);
     }
   }
   // The next kernel in the stream may now be scheduled and start its own weight
@@ -183,10 +194,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
           }
         }
       };
-      // W0 of the first stages goes out before waiting on the previous grid.
+      // W0 of the first stages, and V when this CTA computes t itself, go out before
+      // waiting on the previous grid.
       for (int q = 0; q < pre; ++q) {
         issue(q, q, true, false);
         filled |= 1u << q;
+      }
+      if (local_t) {
+        const int nvb = (p.K + p.vbox - 1) / p.vbox;
+        const uint32_t vb = static_cast<uint32_t>(p.vbox) * sg.r8 * 2u;
+        mbar_arrive_expect_tx(vbar, nvb * vb);
+        for (int b = 0; b < nvb; ++b) tma_load_2d_plain(vres + b * vb, &sg.tm_v, 0, b * p.vbox, vbar);
       }
       pdl_wait_prior_grid();
       for (int q = 0; q < pre; ++q) issue(q, q, false, true);
@@ -214,6 +232,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               if (global_timer_ns() - t0 > 20000000ull) break;
           }
       }
+      if (local_t) {  // no copy may still be landing when the CTA exits
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(vbar, 0u))
+          if (global_timer_ns() - t0 > 20000000ull) break;
+      }
     }
   } else {
     const int cw = warp - 1;              // consumer warp 0..7
@@ -223,18 +246,41 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     bool ok = true;
 
     if (t_cta) {
-      // ---- t = V^T x over this CTA's slice of `in`, staged by TMA ----
+      // ---- t = V^T x over this CTA's slice of `in`: every box of V and x is requested
+      // at once (one round trip), V before the dependency wait ----
       // slices start on a multiple of 8 elements: a TMA box's innermost coordinate must
       // be 16-byte aligned
       const int ks = ((p.K + p.t_ctas - 1) / p.t_ctas + 7) & ~7;
       const int i0 = cta * ks;
       const int i1 = min(p.K, i0 + ks);
+      const int n = max(0, i1 - i0);
+      const int nvb = (ks + p.vbox - 1) / p.vbox;
+      const int trows = nvb * p.vbox;                                // staged rows of `in`
       const int ntot = p.M * p.r_total;
       float* tacc = reinterpret_cast<float*>(epi);                 // [M][r_total], fp32
       const int tacc_bytes = (ntot * 4 + 1023) & ~1023;
-      uint8_t* stage_area = epi + tacc_bytes;                        // V rows, then x rows
-      uint8_t* xsb = stage_area + p.t_rows * p.r8_total * 2;         // [M][t_rows] bf16
+      uint8_t* stage_area = epi + tacc_bytes;                        // per family [trows][r8]
+      const uint16_t* xsb =                                          // per box [M][vbox]
+          reinterpret_cast<const uint16_t*>(stage_area + static_cast<size_t>(trows) * p.r8_total * 2);
+      // TMA writes shared memory at 128-byte aligned addresses: x boxes are spaced so
+      const int xbs = ((p.vbox * p.M * 2 + 127) & ~127) / 2;        // elements per x box
       for (int idx = ct; idx < ntot; idx += kDecConsumers) tacc[idx] = 0.0f;
+      if (ct == 0 && n > 0) {
+        mbar_arrive_expect_tx(&full[0], static_cast<uint32_t>(trows) * (p.r8_total + p.M) * 2u);  // box bytes
+        int col = 0;
+        for (int j = 0; j < p.nseg; ++j) {
+          if (p.seg[j].r > 0)
+            for (int b = 0; b < nvb; ++b)
+              tma_load_2d_plain(stage_area + (static_cast<size_t>(trows) * col + b * p.vbox * p.seg[j].r8) * 2,
+                                &p.seg[j].tm_v, 0, i0 + b * p.vbox, &full[0]);
+          col += p.seg[j].r8;
+        }
+        pdl_wait_prior_grid();
+        for (int b = 0; b < nvb; ++b)
+          tma_load_2d_plain(const_cast<uint16_t*>(xsb) + b * xbs, &p.tm_xt, i0 + b * p.vbox, 0, &full[0]);
+      }
+      pdl_wait_prior_grid();
+      if (n > 0) ok = mbar_wait(&full[0], 0u, ctl);
       // thread -> (family, 4 tokens x 4 columns) block, and a residue class of rows
       const int mb = (p.M + 3) / 4;
       int blocks = 0;
@@ -243,13 +289,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       const int igroups = few ? kDecConsumers / blocks : 1;
       const int ig = few ? ct / blocks : 0;
       const bool worker = few ? ig < igroups : true;
-      const uint32_t vbytes = static_cast<uint32_t>(p.t_rows) * p.r8_total * 2u;
-      const uint32_t xbytes = static_cast<uint32_t>(p.t_rows) * p.M * 2u;
-      float acc[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
       int my_j = 0, my_m0 = 0, my_k0 = 0, my_vcol = 0;
       auto locate = [&](int blk) {
         int j = 0, rest = blk, vcol = 0;
@@ -263,74 +302,38 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         my_k0 = (rest % (p.seg[j].r8 / 4)) * 4;
         my_vcol = vcol;
       };
-      uint32_t tph = 0;
-      for (int a = i0, first = 1; ok && a < i1; a += p.t_rows, first = 0) {
-        const int n = min(p.t_rows, i1 - a);
-        if (!first && !(ok = cons_sync(cbar, cph, ctl))) break;   // staging free again
-        if (ct == 0) {
-          mbar_arrive_expect_tx(&full[0], vbytes + xbytes);
-          int col = 0;
-          for (int j = 0; j < p.nseg; ++j) {
-            if (p.seg[j].r > 0)
-              tma_load_2d_plain(stage_area + static_cast<size_t>(p.t_rows) * col * 2, &p.seg[j].tm_v, 0, a,
-                                &full[0]);
-            col += p.seg[j].r8;
-          }
-          if (first) pdl_wait_prior_grid();
-          tma_load_2d_plain(xsb, &p.tm_xt, a, 0, &full[0]);
-        }
-        if (first) pdl_wait_prior_grid();
-        if (!(ok = mbar_wait(&full[0], tph, ctl))) break;
-        tph ^= 1u;
-        for (int blk = (few ? ct % blocks : ct); worker && blk < blocks; blk += (few ? blocks : kDecConsumers)) {
-          locate(blk);
-          const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage_area) +
-                               static_cast<size_t>(p.t_rows) * my_vcol;     // [t_rows][r8_j]
-          const int r8 = p.seg[my_j].r8;
-          const uint16_t* xs = reinterpret_cast<const uint16_t*>(xsb);      // [M][t_rows]
-          float lacc[4][4];
+      for (int blk = (few ? ct % blocks : ct); ok && worker && blk < blocks; blk += (few ? blocks : kDecConsumers)) {
+        locate(blk);
+        const int r8 = p.seg[my_j].r8;
+        const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage_area) + static_cast<size_t>(trows) * my_vcol;
+        float lacc[4][4];
 #pragma unroll
-          for (int x0 = 0; x0 < 4; ++x0)
+        for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
-            for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = 0.0f;
-          for (int i = ig; i < n; i += igroups) {
+          for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = 0.0f;
+        for (int b = 0; b < nvb; ++b) {
+          const int lo = b * p.vbox;
+          const int hi = min(n, lo + p.vbox);
+          const uint16_t* xb = xsb + b * xbs;
+          for (int i = lo + ig; i < hi; i += igroups) {
             const uint2 vv = *reinterpret_cast<const uint2*>(vs + i * r8 + my_k0);
             const float va[4] = {__uint_as_float(vv.x << 16), __uint_as_float(vv.x & 0xFFFF0000u),
                                  __uint_as_float(vv.y << 16), __uint_as_float(vv.y & 0xFFFF0000u)};
 #pragma unroll
             for (int x0 = 0; x0 < 4; ++x0) {
               const int m = my_m0 + x0;
-              const float xv = m < p.M ? bf16_to_f32(xs[m * p.t_rows + i]) : 0.0f;
+              const float xv = m < p.M ? bf16_to_f32(xb[m * p.vbox + (i - lo)]) : 0.0f;
 #pragma unroll
               for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = fmaf(xv, va[y0], lacc[x0][y0]);
             }
           }
-          if (few) {
-#pragma unroll
-            for (int x0 = 0; x0 < 4; ++x0)
-#pragma unroll
-              for (int y0 = 0; y0 < 4; ++y0) acc[x0][y0] += lacc[x0][y0];
-          } else {
-#pragma unroll
-            for (int x0 = 0; x0 < 4; ++x0)
-#pragma unroll
-              for (int y0 = 0; y0 < 4; ++y0) {
-                const int m = my_m0 + x0, k = my_k0 + y0;
-                if (m < p.M && k < p.seg[my_j].r)
-                  atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
-              }
-          }
         }
-      }
-      if (i0 >= i1) pdl_wait_prior_grid();
-      if (ok && few && worker) {
-        locate(ct % blocks);
 #pragma unroll
         for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
           for (int y0 = 0; y0 < 4; ++y0) {
             const int m = my_m0 + x0, k = my_k0 + y0;
-            if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], acc[x0][y0]);
+            if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
           }
       }
       if (ok) ok = cons_sync(cbar, cph, ctl);
@@ -376,14 +379,71 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         }
         ok = cons_sync(cbar, cph, ctl);
       }
+      float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
+      float* ts = red + p.ts_off;                            // [M][r]
+      const uint32_t xres_base = smem_u32(xres);
+      // ---- t = V^T x of this CTA's family, from V staged before the dependency wait:
+      // warps split `in` in 16-wide steps, mma.sync per step, fixed-order sum over warps ----
+      if (ok && local_t) {
+        ok = warp_wait_all(vbar, 0u, ctl);
+        if (ok) {
+          float* part = red;                                   // [8][kTok][r8]
+          const int r8 = sg.r8;
+          const int ntn = r8 / 8;
+          const uint32_t vbase = smem_u32(vres);
+          float ta[NT / 2][kDecLocalMaxR8 / 8][4];
+#pragma unroll
+          for (int mt = 0; mt < NT / 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ta[mt][nt][e] = 0.0f;
+          const int nks = (p.K + 15) / 16;
+          for (int kk = cw; kk < nks; kk += 8) {
+            const int k0 = kk * 16;
+            uint32_t bf[kDecLocalMaxR8 / 8][2];
+#pragma unroll
+            for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
+              if (nt < ntn) ldsm_x2_trans(vbase + ((k0 + (lane & 15)) * r8 + nt * 8) * 2, bf[nt][0], bf[nt][1]);
+#pragma unroll
+            for (int mt = 0; mt < NT / 2; ++mt) {
+              if (mt * 16 < p.M) {
+                const int m = min(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, p.M - 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(xres_base + (m * p.xs_ld + k0 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
+                  if (nt < ntn) mma_16816(ta[mt][nt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
+              }
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < NT / 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
+              if (nt < ntn)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int m = mt * 16 + gq + 8 * h, c = nt * 8 + 2 * qq;
+                  part[(cw * kTok + m) * r8 + c] = ta[mt][nt][2 * h];
+                  part[(cw * kTok + m) * r8 + c + 1] = ta[mt][nt][2 * h + 1];
+                }
+          ok = cons_sync(cbar, cph, ctl);
+          if (ok) {
+            for (int idx = ct; idx < p.M * sg.r; idx += kDecConsumers) {
+              const int m = idx / sg.r, k = idx - m * sg.r;
+              float v = 0.0f;
+              for (int w = 0; w < 8; ++w) v += part[(w * kTok + m) * r8 + k];
+              ts[idx] = v;
+            }
+          }
+        }
+      }
       // ---- stream this CTA's rows of W0 ----
       const int nslab = (R + 15) / 16;
       const int kg = 8 / nslab;                 // warps sharing one slab (split over K)
       const bool active = cw < nslab * kg;
       const int slab = cw / kg, kgi = cw - slab * kg;
-      float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
-      float* ts = red + 8 * 16 * kTok;                       // [M][r]
-      const uint32_t xres_base = smem_u32(xres);
       int slot = 0;
       uint32_t phase = 0;
       for (int ch = 0; ok && ch < sg.chunks; ++ch) {
@@ -458,7 +518,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               my[rr * kTok + tok + 1] = acc[nt][2 * h + 1];
             }
         }
-        if (sg.r > 0) {
+        if (sg.r > 0 && !p.t_local) {
           if (ct == 0) {
             bool ready = true;
             const uint64_t t0 = global_timer_ns();
@@ -535,9 +595,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     }
 
     // The last CTA to finish clears the sync region for the next call (nothing to clear
-    // when no family has a rank-r term).
-    if (ok && p.r_total > 0) ok = cons_sync(cbar, cph, ctl);
-    if (ok && p.r_total > 0) {
+    // when no CTA computes t for the others).
+    if (ok && p.t_ctas > 0) ok = cons_sync(cbar, cph, ctl);
+    if (ok && p.t_ctas > 0) {
       if (ct == 0) {
         __threadfence();
         const int old = atomicAdd(&p.counters[1], 1);

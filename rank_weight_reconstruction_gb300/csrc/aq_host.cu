@@ -403,10 +403,23 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.tok_tile = M <= 16 ? 16 : 32;
     dp.r_total = wl.r_total;
     dp.w3d = (K % kBK) == 0 ? 1 : 0;
-    // t CTAs: about 32 KB of V each, at most kDecMaxTCtas, at least 8 rows of `in` each
+    int max_r8 = 0;
+    for (int j = 0; j < n; ++j) max_r8 = std::max(max_r8, static_cast<int>(round_up(th[j]->r, 8)));
+    const int64_t kp = static_cast<int64_t>(dp.nkb) * kBK;
+    dp.xs_ld = static_cast<int32_t>(kp + 8);
+    dp.x_res = M * (kp + 8) * 2 <= 64 * 1024 ? 1 : 0;
+    dp.xres_bytes = dp.x_res ? static_cast<uint32_t>(round_up(M * (kp + 8) * 2, 1024)) : 0u;
+    // t = V^T x: computed by every streaming CTA for its own family when that family's V
+    // is small (no cross-CTA dependency at all), else by t CTAs publishing through the
+    // workspace's sync region.
+    dp.vbox = static_cast<int32_t>(std::min<int64_t>(256, round_up(K, 16)));
+    const int64_t vres = round_up(ceil_div(K, dp.vbox) * dp.vbox * max_r8 * 2, 1024);
+    dp.t_local = (wl.r_total > 0 && dp.x_res && max_r8 <= kDecLocalMaxR8 && vres <= 40 * 1024) ? 1 : 0;
+    dp.vres_bytes = dp.t_local ? static_cast<uint32_t>(vres) : 0u;
     int64_t v_bytes = 0;
     for (int j = 0; j < n; ++j) v_bytes += static_cast<int64_t>(th[j]->r) * K * 2;
-    dp.t_ctas = wl.r_total > 0
+    // t CTAs: about 32 KB of V each, at most kDecMaxTCtas, at least 8 rows of `in` each
+    dp.t_ctas = (wl.r_total > 0 && !dp.t_local)
                     ? static_cast<int32_t>(std::max<int64_t>(
                           1, std::min<int64_t>({kDecMaxTCtas, ceil_div(v_bytes, 32 * 1024), ceil_div(K, 8)})))
                     : 0;
@@ -455,20 +468,18 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       dp.r8_total += sg.r8;
       max_share = std::max<int64_t>(max_share, static_cast<int64_t>(sg.chunk_rows) * sg.chunks * K * 2);
     }
-    const int64_t kp = static_cast<int64_t>(dp.nkb) * kBK;
-    dp.xs_ld = static_cast<int32_t>(kp + 8);
-    dp.x_res = M * (kp + 8) * 2 <= 64 * 1024 ? 1 : 0;
-    dp.xres_bytes = dp.x_res ? static_cast<uint32_t>(round_up(M * (kp + 8) * 2, 1024)) : 0u;
     // 2-D boxes must start on 1 KB (128-byte swizzle atoms of 8 rows): round rows to 8
     dp.wbox_bytes = static_cast<uint32_t>(round_up(max_rows, 8) * 128);
     dp.kbox = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>({8, (32 * 1024) / dp.wbox_bytes, dp.nkb})));
     dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
     dp.stage_bytes = static_cast<uint32_t>(
         round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
-    dp.epi_bytes = static_cast<uint32_t>(round_up(8 * 16 * dp.tok_tile * 4 + M * max_r * 4, 1024));
+    // epilogue staging: the warps' row sums (or, first, their partial t) then t itself
+    dp.ts_off = std::max(8 * 16 * dp.tok_tile, dp.t_local ? 8 * dp.tok_tile * max_r8 : 0);
+    dp.epi_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.ts_off) * 4 + M * max_r * 4, 1024));
     // Two CTAs per SM when a CTA's W0 share is small (the next call's CTAs then stream W0
     // while this call's finish); one CTA with a deep ring when the share is large.
-    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes;
+    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes + dp.vres_bytes;
     const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
     const size_t half = cap / 2 - 1024;
     const int stages2 = fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
@@ -476,17 +487,32 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       dp.stages = std::min(stages2, kMaxStages);
     else
       dp.stages = stages_for(dp.stage_bytes, dev->smem_optin, fixed);
-    // t CTAs stage rows of V (all families) and of x in the same shared memory
-    const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
-    const int64_t tspace = static_cast<int64_t>(dp.epi_bytes) + dp.xres_bytes +
-                           static_cast<int64_t>(dp.stages) * dp.stage_bytes - tacc_bytes;
+    size_t smem = fixed + static_cast<size_t>(dp.stages) * dp.stage_bytes;
+    if (smem > cap) return fail(AQ_ERR_UNSUPPORTED, "%s: decode plan needs %zu bytes of shared memory", who, smem);
     if (dp.t_ctas > 0) {
-      const int64_t ks = round_up(ceil_div(K, dp.t_ctas), 8);   // the kernel's slice length
-      const int64_t fit = tspace / (dp.r8_total * 2 + M * 2);
-      dp.t_rows = static_cast<int32_t>(std::min<int64_t>({256, round_up(ks, 8), fit / 8 * 8}));
-      if (dp.t_rows < 8)
-        return fail(AQ_ERR_UNSUPPORTED, "%s: M x total rank too large for the decode kernel's shared memory", who);
-      if ((st = tmap_2d_plain(&dp.tm_xt, x, K, M, ldx, dp.t_rows, static_cast<int>(M), "x (t)")) != AQ_OK) return st;
+      // A t CTA stages its whole slice of V (all families) and x at once, in boxes of vbox
+      // rows, after its fp32 t [M][r_total]; add t CTAs until a slice fits, and when even
+      // the thinnest slice does not, give the launch the shared memory it needs.
+      const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
+      const int64_t tspace = static_cast<int64_t>(smem) - kHeaderBytes - kSmemSlack - tacc_bytes;
+      const int64_t max_t = std::max<int64_t>(1, ceil_div(K, 8));
+      for (;;) {
+        const int64_t ks = round_up(ceil_div(K, dp.t_ctas), 8);   // the kernel's slice length
+        const int64_t nvb = ceil_div(ks, 256);
+        dp.vbox = static_cast<int32_t>(round_up(ceil_div(ks, nvb), 16));
+        // per box: V rows of every family, then x [M][vbox] padded to 128 bytes
+        const int64_t per_box = static_cast<int64_t>(dp.vbox) * dp.r8_total * 2 + round_up(dp.vbox * M * 2, 128);
+        if (nvb * per_box <= tspace) break;
+        if (dp.t_ctas >= max_t) {
+          const size_t need = kHeaderBytes + kSmemSlack + static_cast<size_t>(tacc_bytes + nvb * per_box);
+          if (need > cap)
+            return fail(AQ_ERR_UNSUPPORTED, "%s: M x total rank too large for the decode kernel's shared memory", who);
+          smem = need;
+          break;
+        }
+        ++dp.t_ctas;
+      }
+      if ((st = tmap_2d_plain(&dp.tm_xt, x, K, M, ldx, dp.vbox, static_cast<int>(M), "x (t)")) != AQ_OK) return st;
     }
     for (int j = 0; j < n; ++j) {
       DecodeSeg& sg = dp.seg[j];
@@ -496,7 +522,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       } else if ((st = tmap_2d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, sg.chunk_rows, "W0")) != AQ_OK) {
         return st;
       }
-      if (th[j]->r > 0 && (st = tmap_2d_plain(&sg.tm_v, th[j]->V, th[j]->r, K, th[j]->ld_v, sg.r8, dp.t_rows, "V")) != AQ_OK)
+      if (th[j]->r > 0 && (st = tmap_2d_plain(&sg.tm_v, th[j]->V, th[j]->r, K, th[j]->ld_v, sg.r8, dp.vbox, "V")) != AQ_OK)
         return st;
     }
     if (!dp.x_res) {
@@ -510,8 +536,12 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.t_acc = reinterpret_cast<float*>(wsb + kSyncTAccOffset);
     dp.status = dev->status;
     dp.timeout_ns = kTimeoutNs;
+    // every TMA destination in shared memory must be 128-byte aligned (1 KB for the
+    // swizzled W0 / x stages): the regions above are sized so; refuse a plan that is not
+    if (dp.epi_bytes % 1024 || dp.xres_bytes % 1024 || dp.vres_bytes % 1024 || dp.stage_bytes % 1024 ||
+        dp.wregion % 1024 || dp.wbox_bytes % 1024 || (static_cast<int64_t>(dp.vbox) * 8 * 2) % 128)
+      return fail(AQ_ERR_UNSUPPORTED, "%s: decode plan breaks shared-memory alignment", who);
     const int grid = dp.t_ctas + cta_begin;
-    const size_t smem = fixed + static_cast<size_t>(dp.stages) * dp.stage_bytes;
     if ((st = launch_or_fail(launch_decode(dp, grid, smem, cs, true), "launch decode kernel")) != AQ_OK) return st;
     t_last_path = AQ_PATH_DECODE;
     return AQ_OK;

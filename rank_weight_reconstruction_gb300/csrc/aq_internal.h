@@ -60,6 +60,7 @@ constexpr int kDecConsumers = 256;
 constexpr int kDecMaxTok = 32;          // tokens the decode kernel handles
 constexpr int kDecMaxEpiBytes = 48 * 1024;  // largest epilogue staging (sums + t)
 constexpr int kDecMaxTCtas = 16;        // most CTAs that compute t = V^T x
+constexpr int kDecLocalMaxR8 = 32;      // largest r8 for which streaming CTAs compute t themselves
 // Workspace: [0, kSyncBytes) must be zero before first use and is left zero by every decode
 // call (counters and the fp32 t accumulator); scratch that needs no initialisation follows.
 constexpr size_t kSyncBytes = 128 * 1024;
@@ -69,7 +70,7 @@ constexpr int kMaxTAcc = static_cast<int>((kSyncBytes - kSyncTAccOffset) / 4);
 struct DecodeSeg {
   CUtensorMap tm_w;    // W0: 3-D view {64, K/64, rows} with box {64, kbox, chunk_rows} when w3d,
                        // else 2-D [rows, K] with box {64, chunk_rows}; 128-byte swizzle
-  CUtensorMap tm_v;    // V [in, r]: 2-D, no swizzle, box {r8, t_rows} (t CTAs)
+  CUtensorMap tm_v;    // V [in, r]: 2-D, no swizzle, box {r8, vbox}
   const uint16_t* s;
   const uint16_t* U;
   int64_t ldu;
@@ -88,7 +89,7 @@ struct DecodeSeg {
 
 struct DecodeParams {
   CUtensorMap tm_x;    // x per stage (when !x_res): like tm_w with M rows
-  CUtensorMap tm_xt;   // x for t CTAs: 2-D, no swizzle, box {t_rows, M}
+  CUtensorMap tm_xt;   // x for t CTAs: 2-D, no swizzle, box {vbox, M}
   DecodeSeg seg[kMaxSeg];
   const uint16_t* x;
   int64_t ldx;
@@ -102,15 +103,20 @@ struct DecodeParams {
   int32_t xs_ld;       // row stride (elements) of resident x: round_up(K, 64) + 8
   int32_t tok_tile;    // 16 or 32
   int32_t r_total;
-  int32_t t_ctas;      // CTAs [0, t_ctas) compute t; the rest stream W0
-  int32_t t_rows;      // rows of `in` a t CTA stages at a time (multiple of 8, <= 256)
+  int32_t t_local;     // 1: every streaming CTA computes its family's t itself from V staged
+                       // in its shared memory (small V); 0: t CTAs, see t_ctas
+  int32_t t_ctas;      // CTAs [0, t_ctas) compute t into the sync region; the rest stream W0
+  int32_t vbox;        // rows of `in` per V (and t-CTA x) box: a multiple of 16, <= 256
   int32_t r8_total;    // sum of r8 over the families
+  int32_t ts_off;      // float offset of t [M][r] in the epilogue staging
   int32_t stages;
   uint32_t stage_bytes;
   uint32_t wregion;    // bytes of the W0 part of a stage: kbox * wbox_bytes, 1 KB aligned
   uint32_t wbox_bytes; // bytes of one 64-wide k block of W0 rows: round_up(max chunk_rows, 8) * 128
-  uint32_t epi_bytes;  // epilogue staging: warp sums [8][16][tok_tile] + t [M][max r], 1 KB aligned
+  uint32_t epi_bytes;  // epilogue staging: warp sums [8][16][tok_tile] (or, when t_local, the
+                       // warps' partial t [8][tok_tile][r8]) then t [M][max r], 1 KB aligned
   uint32_t xres_bytes; // resident x bytes (0 if !x_res), 1 KB aligned
+  uint32_t vres_bytes; // staged V of the CTA's family when t_local: [ceil(in/vbox)*vbox][r8]
   int32_t* counters;   // sync region: [0] t arrivals, [1] finished CTAs
   float* t_acc;        // sync region: [M][r_total]
   int32_t* status;
