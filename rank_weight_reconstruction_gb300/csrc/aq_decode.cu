@@ -95,6 +95,11 @@ __device__ __forceinline__ uint32_t stage_addr(uint32_t base, int w3d, int kbox,
   return base + b * box_bytes + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
+// header: full[kMaxStages], empty[kMaxStages], cbar, vbar, two ints, then the s buffers
+static_assert((2 * kMaxStages + 2) * 8 + 8 <= kSBufOffset, "s buffers overlap the barriers");
+static_assert(kSBufOffset + 2 * kSBufBytes <= kHeaderBytes, "s buffers exceed the header");
+static_assert(((kMmaM + 14) / 8) * 16 <= kSBufBytes, "s buffer too small for a 128-row chunk");
+
 template <int NT>
 __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -108,7 +113,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   uint8_t* epi = smem + kHeaderBytes;
   uint8_t* xres = epi + p.epi_bytes;
   uint8_t* vres = xres + p.xres_bytes;
-  uint8_t* ring = vres + p.vres_bytes;
+  uint8_t* ures = vres + p.vres_bytes;
+  uint8_t* ring = ures + p.ures_bytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -344,6 +350,34 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         if (ok && ct == 0) atomicAdd(&p.counters[0], 1);
       }
     } else {
+      // s and the U rows of a chunk go to shared memory with cp.async when the chunk
+      // starts (the first chunk's before the dependency wait: both are weights), so the
+      // epilogue reads nothing from global memory. A load issued there would wait behind
+      // this SM's whole queue of W0 traffic.
+      auto sbuf = [&](int ch) { return reinterpret_cast<uint16_t*>(smem + kSBufOffset + (ch & 1) * kSBufBytes); };
+      auto stage_ch = [&](int ch) {
+        const int row0 = (l * sg.chunks + ch) * R;
+        // s[row0 - (row0 & 7) ...] in 16-byte pieces, zero past the last row
+        const int sb = row0 & ~7;
+        const int spieces = (row0 + R - sb + 7) / 8;
+        for (int idx = ct; idx < spieces; idx += kDecConsumers) {
+          const int e0 = sb + idx * 8;
+          cp_async_16_zfill(smem_u32(sbuf(ch)) + idx * 16, sg.s + e0, max(0, min(16, (sg.rows - e0) * 2)));
+        }
+        if (sg.r > 0) {   // U rows [R][r16], zero past r
+          const uint32_t ub = smem_u32(ures) + (ch & 1) * p.ubuf_bytes;
+          const int pieces = sg.r16 / 8;
+          for (int idx = ct; idx < R * pieces; idx += kDecConsumers) {
+            const int rr = idx / pieces, c = idx - rr * pieces;
+            const int o = row0 + rr;
+            if (o < sg.rows)
+              cp_async_16_zfill(ub + (rr * sg.r16 + c * 8) * 2, sg.U + static_cast<int64_t>(o) * sg.ldu + c * 8,
+                                max(0, min(16, (sg.r - c * 8) * 2)));
+          }
+        }
+        cp_async_commit();
+      };
+      stage_ch(0);
       pdl_wait_prior_grid();
       // ---- x resident in shared memory (dense rows, zero beyond K) ----
       if (p.x_res) {
@@ -380,7 +414,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         ok = cons_sync(cbar, cph, ctl);
       }
       float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
-      float* ts = red + p.ts_off;                            // [M][r]
+      // t of this CTA's family as a bf16 pair, t = t_hi + t_lo to about 16 significant
+      // bits, each [kTok][r16] and zero past M and r: the B operand of U t in the epilogue
+      uint16_t* tbh = reinterpret_cast<uint16_t*>(red + p.ts_off);
+      uint16_t* tbl = tbh + kTok * sg.r16;
+      auto put_t = [&](int idx, float v) {
+        const uint16_t h = f32_to_bf16_rn(v);
+        tbh[idx] = h;
+        tbl[idx] = f32_to_bf16_rn(v - bf16_to_f32(h));
+      };
       const uint32_t xres_base = smem_u32(xres);
       // ---- t = V^T x of this CTA's family, from V staged before the dependency wait:
       // warps split `in` in 16-wide steps, mma.sync per step, fixed-order sum over warps ----
@@ -430,11 +472,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
                 }
           ok = cons_sync(cbar, cph, ctl);
           if (ok) {
-            for (int idx = ct; idx < p.M * sg.r; idx += kDecConsumers) {
-              const int m = idx / sg.r, k = idx - m * sg.r;
+            for (int idx = ct; idx < kTok * sg.r16; idx += kDecConsumers) {
+              const int m = idx / sg.r16, k = idx - m * sg.r16;
               float v = 0.0f;
-              for (int w = 0; w < 8; ++w) v += part[(w * kTok + m) * r8 + k];
-              ts[idx] = v;
+              if (m < p.M && k < sg.r)
+                for (int w = 0; w < 8; ++w) v += part[(w * kTok + m) * r8 + k];
+              put_t(idx, v);
             }
           }
         }
@@ -449,6 +492,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       for (int ch = 0; ok && ch < sg.chunks; ++ch) {
         const int row0 = (l * sg.chunks + ch) * R;
         if (row0 >= sg.rows) break;
+        if (ch > 0) stage_ch(ch);
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -505,9 +549,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
           }
         }
         if (!ok) break;
-        // ---- epilogue of this chunk ----
-        if (!(ok = cons_sync(cbar, cph, ctl))) break;   // red / ts free
-        if (active) {
+        // ---- epilogue of this chunk: the lead warp of each slab (kgi == 0) adds its
+        // partners' partial sums, runs U t on the tensor cores from the staged U rows and
+        // t_hi / t_lo, and writes y = RN(s z + U t) straight from the mma fragments ----
+        if (!(ok = cons_sync(cbar, cph, ctl))) break;   // red free
+        if (active && kgi > 0) {
           float* my = red + (slab * kg + kgi) * 16 * kTok;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -518,7 +564,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               my[rr * kTok + tok + 1] = acc[nt][2 * h + 1];
             }
         }
-        if (sg.r > 0 && !p.t_local) {
+        if (sg.r > 0 && !p.t_local && ch == 0) {   // t stays in shared memory for later chunks
           if (ct == 0) {
             bool ready = true;
             const uint64_t t0 = global_timer_ns();
@@ -537,63 +583,84 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             ok = false;
             break;
           }
-          for (int idx = ct; idx < p.M * sg.r; idx += kDecConsumers) {
-            const int m = idx / sg.r, k = idx - m * sg.r;
-            ts[idx] = __ldcg(&p.t_acc[m * p.r_total + sg.t_col + k]);
+          const int nt_el = kTok * sg.r16;
+          for (int base = ct; base < nt_el; base += 8 * kDecConsumers) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {   // eight loads in flight per thread
+              const int idx = base + u * kDecConsumers;
+              const int m = idx / sg.r16, k = idx - m * sg.r16;
+              v[u] = (idx < nt_el && m < p.M && k < sg.r) ? __ldcg(&p.t_acc[m * p.r_total + sg.t_col + k]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + u * kDecConsumers;
+              if (idx < nt_el) put_t(idx, v[u]);
+            }
           }
         }
+        cp_async_wait_all();
         if (!(ok = cons_sync(cbar, cph, ctl))) break;
-        const int row = ct & 127;
-        const int half = ct >> 7;
-        const int o = row0 + row;
-        if (row < R && o < sg.rows) {
-          const int rs = row >> 4, rr = row & 15;
-          float z[kTok / 2];
+        if (active && kgi == 0) {
+          for (int k2 = 1; k2 < kg; ++k2) {
+            const float* pr = red + (slab * kg + k2) * 16 * kTok;
 #pragma unroll
-          for (int mi = 0; mi < kTok / 2; ++mi) z[mi] = 0.0f;
-          for (int k2 = 0; k2 < kg; ++k2) {
-            const float* pr = red + (rs * kg + k2) * 16 * kTok + rr * kTok;
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int mi = 0; mi < kTok / 2; ++mi) z[mi] += pr[half + 2 * mi];
+              for (int h = 0; h < 2; ++h) {
+                const int rr = gq + 8 * h, tok = 8 * nt + 2 * qq;
+                acc[nt][2 * h] += pr[rr * kTok + tok];
+                acc[nt][2 * h + 1] += pr[rr * kTok + tok + 1];
+              }
           }
-          float low[kTok / 2];
+          float lw[NT][4];
 #pragma unroll
-          for (int mi = 0; mi < kTok / 2; ++mi) low[mi] = 0.0f;
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) lw[nt][e] = 0.0f;
           if (sg.r > 0) {
-            const uint16_t* urow = sg.U + static_cast<int64_t>(o) * sg.ldu;
-            int k = 0;
-            for (; k + 8 <= sg.r; k += 8) {
-              const uint4 uv = __ldg(reinterpret_cast<const uint4*>(urow + k));
-              const uint32_t w[4] = {uv.x, uv.y, uv.z, uv.w};
+            const uint32_t ub = smem_u32(ures) + (ch & 1) * p.ubuf_bytes;
+            const uint32_t th_base = smem_u32(tbh), tl_base = smem_u32(tbl);
+            const int arow = min(16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8, R - 1);
+            for (int k0 = 0; k0 < sg.r16; k0 += 16) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(ub + (arow * sg.r16 + k0 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float u = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-#pragma unroll
-                for (int mi = 0; mi < kTok / 2; ++mi) {
-                  const int m = half + 2 * mi;
-                  if (m < p.M) low[mi] = fmaf(u, ts[m * sg.r + k + e], low[mi]);
-                }
-              }
-            }
-            for (; k < sg.r; ++k) {
-              const float u = bf16_to_f32(urow[k]);
-#pragma unroll
-              for (int mi = 0; mi < kTok / 2; ++mi) {
-                const int m = half + 2 * mi;
-                if (m < p.M) low[mi] = fmaf(u, ts[m * sg.r + k], low[mi]);
+              for (int np = 0; np < NT / 2; ++np) {
+                const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
+                const uint32_t boff = (brow * sg.r16 + k0 + ((lane >> 3) & 1) * 8) * 2;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(th_base + boff, b0, b1, b2, b3);
+                mma_16816(lw[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_16816(lw[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                ldsm_x4(tl_base + boff, b0, b1, b2, b3);
+                mma_16816(lw[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_16816(lw[2 * np + 1], a0, a1, a2, a3, b2, b3);
               }
             }
           }
-          const float sc = bf16_to_f32(sg.s[o]);
+          const uint16_t* sv = sbuf(ch);
 #pragma unroll
-          for (int mi = 0; mi < kTok / 2; ++mi) {
-            const int m = half + 2 * mi;
-            if (m < p.M) sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, z[mi], low[mi]));
+          for (int h = 0; h < 2; ++h) {
+            const int row = 16 * slab + gq + 8 * h;
+            const int o = row0 + row;
+            if (row < R && o < sg.rows) {
+              const float sc = bf16_to_f32(sv[o - (row0 & ~7)]);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int m = 8 * nt + 2 * qq + e;
+                  if (m < p.M)
+                    sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, acc[nt][2 * h + e], lw[nt][2 * h + e]));
+                }
+            }
           }
         }
       }
     }
 
+    if (!t_cta) cp_async_wait_all();   // no copy may still be landing when the CTA exits
     // The last CTA to finish clears the sync region for the next call (nothing to clear
     // when no CTA computes t for the others).
     if (ok && p.t_ctas > 0) ok = cons_sync(cbar, cph, ctl);

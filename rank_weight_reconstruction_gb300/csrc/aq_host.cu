@@ -447,7 +447,14 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     for (int j = 0; j < n; ++j) {
       DecodeSeg& sg = dp.seg[dp.nseg++];
       const int64_t per = ceil_div(th[j]->out, cnt[j]);
-      sg.chunks = static_cast<int32_t>(ceil_div(per, kMmaM));
+      // A CTA whose share of W0 is many rings deep streams it in chunks of at most 32
+      // rows, so that a stage can span 8 k blocks: 1 KB contiguous per row, which is what
+      // keeps HBM near its copy rate. Smaller shares keep one chunk (one epilogue).
+      // and U rows of a chunk staged in shared memory stay within 16 KB
+      const int64_t r16 = round_up(th[j]->r, 16);
+      const int64_t u_cap = r16 > 0 ? std::max<int64_t>(16, (16 * 1024) / (r16 * 2) / 16 * 16) : kMmaM;
+      const int64_t row_cap = std::min<int64_t>(per * K * 2 > 256 * 1024 ? 32 : kMmaM, u_cap);
+      sg.chunks = static_cast<int32_t>(ceil_div(per, row_cap));
       sg.chunk_rows = static_cast<int32_t>(ceil_div(th[j]->out, static_cast<int64_t>(cnt[j]) * sg.chunks));
       cnt[j] = static_cast<int>(ceil_div(th[j]->out, static_cast<int64_t>(sg.chunk_rows) * sg.chunks));  // CTAs with rows
       sg.s = static_cast<const uint16_t*>(th[j]->s);
@@ -460,6 +467,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       sg.rows = th[j]->out;
       sg.r = th[j]->r;
       sg.r8 = static_cast<int32_t>(round_up(th[j]->r, 8));
+      sg.r16 = static_cast<int32_t>(r16);
       sg.t_col = wl.dec_t_col[j];
       sg.cta_begin = cta_begin;
       cta_begin += cnt[j];
@@ -470,23 +478,42 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     }
     // 2-D boxes must start on 1 KB (128-byte swizzle atoms of 8 rows): round rows to 8
     dp.wbox_bytes = static_cast<uint32_t>(round_up(max_rows, 8) * 128);
-    dp.kbox = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>({8, (32 * 1024) / dp.wbox_bytes, dp.nkb})));
-    dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
-    dp.stage_bytes = static_cast<uint32_t>(
-        round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
     // epilogue staging: the warps' row sums (or, first, their partial t) then t itself
     dp.ts_off = std::max(8 * 16 * dp.tok_tile, dp.t_local ? 8 * dp.tok_tile * max_r8 : 0);
-    dp.epi_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.ts_off) * 4 + M * max_r * 4, 1024));
+    const int64_t max_r16 = round_up(max_r, 16);
+    dp.epi_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.ts_off) * 4 + 2 * dp.tok_tile * max_r16 * 2, 1024));
+    // U rows of a chunk staged in shared memory (two buffers when CTAs have several chunks)
+    int max_chunks = 1;
+    for (int j = 0; j < n; ++j) max_chunks = std::max(max_chunks, static_cast<int>(dp.seg[j].chunks));
+    dp.ubuf_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(max_rows) * max_r16 * 2, 128));
+    dp.ures_bytes = max_r > 0 ? static_cast<uint32_t>(round_up((max_chunks > 1 ? 2 : 1) * dp.ubuf_bytes, 1024)) : 0u;
     // Two CTAs per SM when a CTA's W0 share is small (the next call's CTAs then stream W0
-    // while this call's finish); one CTA with a deep ring when the share is large.
-    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes + dp.vres_bytes;
+    // while this call's finish), with smaller stages if that is what it takes to fit three;
+    // one CTA with a deep ring when the share is large.
+    const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes + dp.vres_bytes + dp.ures_bytes;
     const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
     const size_t half = cap / 2 - 1024;
-    const int stages2 = fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
-    if (max_share <= 128 * 1024 && stages2 >= 2)
+    auto set_kbox = [&](int64_t kb) {
+      dp.kbox = static_cast<int32_t>(ceil_div(dp.nkb, ceil_div(dp.nkb, kb)));   // even stages
+      dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
+      dp.stage_bytes = static_cast<uint32_t>(
+          round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
+      return fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
+    };
+    const int64_t kb0 = std::max<int64_t>(1, std::min<int64_t>({8, (32 * 1024) / dp.wbox_bytes, dp.nkb}));
+    int stages2 = 0;
+    bool two = false;
+    if (max_share <= 128 * 1024)
+      for (int64_t kb = kb0; kb >= 1 && !two; --kb) {
+        stages2 = set_kbox(kb);
+        two = stages2 >= 3 || (stages2 >= 2 && kb == 1);
+      }
+    if (two) {
       dp.stages = std::min(stages2, kMaxStages);
-    else
+    } else {
+      set_kbox(kb0);
       dp.stages = stages_for(dp.stage_bytes, dev->smem_optin, fixed);
+    }
     size_t smem = fixed + static_cast<size_t>(dp.stages) * dp.stage_bytes;
     if (smem > cap) return fail(AQ_ERR_UNSUPPORTED, "%s: decode plan needs %zu bytes of shared memory", who, smem);
     if (dp.t_ctas > 0) {
@@ -538,7 +565,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.timeout_ns = kTimeoutNs;
     // every TMA destination in shared memory must be 128-byte aligned (1 KB for the
     // swizzled W0 / x stages): the regions above are sized so; refuse a plan that is not
-    if (dp.epi_bytes % 1024 || dp.xres_bytes % 1024 || dp.vres_bytes % 1024 || dp.stage_bytes % 1024 ||
+    if (dp.epi_bytes % 1024 || dp.xres_bytes % 1024 || dp.vres_bytes % 1024 || dp.ures_bytes % 1024 ||
+        dp.ubuf_bytes % 16 || dp.stage_bytes % 1024 ||
         dp.wregion % 1024 || dp.wbox_bytes % 1024 || (static_cast<int64_t>(dp.vbox) * 8 * 2) % 128)
       return fail(AQ_ERR_UNSUPPORTED, "%s: decode plan breaks shared-memory alignment", who);
     const int grid = dp.t_ctas + cta_begin;

@@ -61,6 +61,10 @@ constexpr int kDecMaxTok = 32;          // tokens the decode kernel handles
 constexpr int kDecMaxEpiBytes = 48 * 1024;  // largest epilogue staging (sums + t)
 constexpr int kDecMaxTCtas = 16;        // most CTAs that compute t = V^T x
 constexpr int kDecLocalMaxR8 = 32;      // largest r8 for which streaming CTAs compute t themselves
+// Two buffers for a chunk's s (up to 128 rows + 8 of alignment) in the kernel's header,
+// after its mbarriers and flags.
+constexpr int kSBufOffset = 384;
+constexpr int kSBufBytes = 320;
 // Workspace: [0, kSyncBytes) must be zero before first use and is left zero by every decode
 // call (counters and the fp32 t accumulator); scratch that needs no initialisation follows.
 constexpr size_t kSyncBytes = 128 * 1024;
@@ -81,6 +85,7 @@ struct DecodeSeg {
   int32_t rows;
   int32_t r;
   int32_t r8;          // round_up(r, 8): width of this family's V rows in a t CTA's staging
+  int32_t r16;         // round_up(r, 16): K of the U t mma (staged U rows and t_hi / t_lo)
   int32_t t_col;       // first column of this family in t [M, r_total]
   int32_t cta_begin;   // first W0-streaming CTA of this family (counted after the t CTAs)
   int32_t chunk_rows;  // rows per chunk (TMA box rows), <= 128
@@ -108,15 +113,19 @@ struct DecodeParams {
   int32_t t_ctas;      // CTAs [0, t_ctas) compute t into the sync region; the rest stream W0
   int32_t vbox;        // rows of `in` per V (and t-CTA x) box: a multiple of 16, <= 256
   int32_t r8_total;    // sum of r8 over the families
-  int32_t ts_off;      // float offset of t [M][r] in the epilogue staging
+  int32_t ts_off;      // float offset of t_hi in the epilogue staging
   int32_t stages;
   uint32_t stage_bytes;
   uint32_t wregion;    // bytes of the W0 part of a stage: kbox * wbox_bytes, 1 KB aligned
   uint32_t wbox_bytes; // bytes of one 64-wide k block of W0 rows: round_up(max chunk_rows, 8) * 128
   uint32_t epi_bytes;  // epilogue staging: warp sums [8][16][tok_tile] (or, when t_local, the
-                       // warps' partial t [8][tok_tile][r8]) then t [M][max r], 1 KB aligned
+                       // warps' partial t [8][tok_tile][r8]), then at ts_off t_hi and t_lo,
+                       // bf16 [tok_tile][r16] each; 1 KB aligned
   uint32_t xres_bytes; // resident x bytes (0 if !x_res), 1 KB aligned
   uint32_t vres_bytes; // staged V of the CTA's family when t_local: [ceil(in/vbox)*vbox][r8]
+  uint32_t ures_bytes; // staged U rows of a chunk, [chunk_rows][r16] per buffer, two buffers
+                       // when a CTA has several chunks
+  uint32_t ubuf_bytes; // bytes of one U buffer
   int32_t* counters;   // sync region: [0] t arrivals, [1] finished CTAs
   float* t_acc;        // sync region: [M][r_total]
   int32_t* status;
