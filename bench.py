@@ -203,6 +203,35 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+KERNEL_SOURCES = ("aq_decode.cu", "aq_kernels.cu", "aq_host.cu", "aq_internal.h", "aq_ptx.cuh")
+
+
+def kernel_source_hash():
+    """sha256 over the CUDA sources: a profiler figure counts only for the code it measured."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "rank_weight_reconstruction_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(key):
+    """DRAM bytes (read + write) of one launch of `key` from the committed profiler summary
+    profiles/dram_traffic.json, or None when that capture predates the current sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no capture"
+    ent = rec.get("launches", {}).get(key)
+    if ent is None:
+        return None, "no capture of this call type"
+    if rec.get("source_hash") != kernel_source_hash():
+        return None, "capture predates the current kernel sources"
+    return int(ent["dram_bytes"]), f"ncu capture ({ent.get('command', '')})"
+
+
 def time_graph(g, reps, stream=None):
     """Average milliseconds of one replay of graph g over `reps` back-to-back replays."""
     import torch
@@ -337,7 +366,7 @@ def run_ours(args, dist: Dist):
         g.replay()
     torch.cuda.synchronize()
     if args.profile:
-        # kernel-profiler mode: the eager warm-up (one launch pair per call), W warm-up
+        # kernel-profiler mode: the eager warm-up (one launch per call), W warm-up
         # replays and K replays of the step, nothing else
         for _ in range(args.steps):
             g.replay()
@@ -398,10 +427,13 @@ def run_ours(args, dist: Dist):
     dom = max(total, key=total.get)
     d = per_type[dom]
     ach = d["bytes_per_call"] / (d["ms_per_call"] * 1e-3) / 1e9
+    traffic, traffic_src = captured_traffic(f"decode:{dom[0]}:M{dom[1]}")
     result["roofline"] = {
-        "bound": "hbm", "kernel": f"aq_linear decode ({dom[0]}, M={dom[1]}): down-projection + swap-AB tcgen05 GEMM",
+        "bound": "hbm",
+        "kernel": f"aq_decode_kernel ({dom[0]}, M={dom[1]}): row-owning CTAs, TMA W0 ring, mma.sync, "
+                  "fused s scale and U t epilogue",
         "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-        "peak_source": f"{pk['source']} copy bandwidth (burst)", "traffic": None,
+        "peak_source": f"{pk['source']} copy bandwidth (burst)", "traffic": traffic, "traffic_source": traffic_src,
         "note": "algorithmic bytes of one call / average time per call over 26 back-to-back calls, each on its "
                 "own W0 copy (L2-cold)"}
     result["decode_calls"] = {f"{k}@M{M}": {"GB_s": round(v["bytes_per_call"] / (v["ms_per_call"] * 1e-3) / 1e9, 1),
@@ -633,6 +665,59 @@ def cpu_baseline(args, budget_s=15.0, steps=1):
             "seconds": round(spent, 3)}
 
 
+def run_case(args, dist: Dist):
+    """One aq_* call repeated: W eager warm-up calls, then K timed calls back to back on
+    one stream (the single-kernel workload that kernel-profiler captures use).
+
+    ``linear:out,in,r,M`` times aq_linear on a seeded theta bundle and x [M, in];
+    ``precompute:out,in,r`` times aq_precompute. Prints one JSON line with the average
+    microseconds per call and its algorithmic bytes or flops."""
+    import torch
+    import rank_weight_reconstruction_gb300 as aq
+    from rank_weight_reconstruction_gb300 import build_lib, synth
+
+    if dist.rank != 0:
+        return None
+    kind, _, dims = args.case.partition(":")
+    vals = [int(v) for v in dims.split(",")]
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    aq.load()
+    out, inp, r = vals[:3]
+    th = synth.make_theta(("case", out, inp, r), out, inp, r)
+    theta = aq.Theta(W0=dev_bits(th.W0, device)[:, :inp], s=dev_bits(th.s, device),
+                     U=dev_bits(th.U, device)[:, :r] if r else None, V=dev_bits(th.V, device)[:, :r] if r else None)
+    if kind == "linear":
+        M = vals[3]
+        x = dev_bits(synth.make_x(("case", M), M, inp), device)[:, :inp]
+        y = torch.empty(M, (out + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :out]
+        ws = aq.new_workspace(aq.aq_linear_workspace_bytes(theta, M), device)
+        run = lambda: aq.aq_linear(theta, x, y=y, workspace=ws)
+        work = {"bytes": linear_bytes(out, inp, r, M), "flops": linear_flops(out, inp, r, M)}
+    elif kind == "precompute":
+        W = torch.empty(out, (inp + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :inp]
+        run = lambda: aq.aq_precompute(theta, W_eff=W)
+        work = {"bytes": precompute_bytes(out, inp, r)}
+    else:
+        raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M or precompute:out,in,r)")
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / max(1, args.steps)
+    res = {"case": args.case, "us_per_call": round(us, 3), "steps": args.steps, "warmup": args.warmup,
+           "status": aq.aq_device_status(), **work}
+    res["GB_s" if kind == "precompute" or vals[3] <= 32 else "TFLOP_s"] = round(
+        (work["bytes"] / us * 1e-3) if (kind == "precompute" or vals[3] <= 32) else (work["flops"] / us * 1e-6), 1)
+    return res
+
+
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
@@ -665,12 +750,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", action="store_true",
                     help="run only the captured decode step (for kernel-profiler launch lists)")
+    ap.add_argument("--case", default=None,
+                    help="time one call instead: linear:out,in,r,M or precompute:out,in,r (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     dist = Dist()
     if args.impl == "reference":
         res = run_reference(args, dist)
+    elif args.case:
+        res = run_case(args, dist)
     else:
         res = run_ours(args, dist)
     if dist.rank == 0 and res is not None:

@@ -43,6 +43,10 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint3
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -122,7 +126,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   const int cta = blockIdx.x;
   const bool t_cta = cta < p.t_ctas;
   const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
-  constexpr int kTok = NT * 8;
+  constexpr int kTok = NT * 8;          // tokens per CTA tile: 8, 16 or 32
+  constexpr int kMT = (NT + 1) / 2;      // 16-row tiles of tokens (local t, where tokens are rows)
 
   // this CTA's family and rows (streaming CTAs only)
   const int g = cta - p.t_ctas;
@@ -367,11 +372,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         if (sg.r > 0) {   // U rows [R][r16], zero past r
           const uint32_t ub = smem_u32(ures) + (ch & 1) * p.ubuf_bytes;
           const int pieces = sg.r16 / 8;
+          const int rs16 = sg.r16 + 8;   // row stride: 16 bytes of padding keep ldmatrix conflict-free
           for (int idx = ct; idx < R * pieces; idx += kDecConsumers) {
             const int rr = idx / pieces, c = idx - rr * pieces;
             const int o = row0 + rr;
             if (o < sg.rows)
-              cp_async_16_zfill(ub + (rr * sg.r16 + c * 8) * 2, sg.U + static_cast<int64_t>(o) * sg.ldu + c * 8,
+              cp_async_16_zfill(ub + (rr * rs16 + c * 8) * 2, sg.U + static_cast<int64_t>(o) * sg.ldu + c * 8,
                                 max(0, min(16, (sg.r - c * 8) * 2)));
           }
         }
@@ -416,12 +422,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
       // t of this CTA's family as a bf16 pair, t = t_hi + t_lo to about 16 significant
       // bits, each [kTok][r16] and zero past M and r: the B operand of U t in the epilogue
+      // (rows padded by 16 bytes, like the staged U rows, so ldmatrix is conflict-free)
+      const int rs16 = sg.r16 + 8;
       uint16_t* tbh = reinterpret_cast<uint16_t*>(red + p.ts_off);
-      uint16_t* tbl = tbh + kTok * sg.r16;
-      auto put_t = [&](int idx, float v) {
+      uint16_t* tbl = tbh + kTok * rs16;
+      auto put_t = [&](int m, int k, float v) {
         const uint16_t h = f32_to_bf16_rn(v);
-        tbh[idx] = h;
-        tbl[idx] = f32_to_bf16_rn(v - bf16_to_f32(h));
+        tbh[m * rs16 + k] = h;
+        tbl[m * rs16 + k] = f32_to_bf16_rn(v - bf16_to_f32(h));
       };
       const uint32_t xres_base = smem_u32(xres);
       // ---- t = V^T x of this CTA's family, from V staged before the dependency wait:
@@ -429,13 +437,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       if (ok && local_t) {
         ok = warp_wait_all(vbar, 0u, ctl);
         if (ok) {
-          float* part = red;                                   // [8][kTok][r8]
+          float* part = red;                                   // [8][kMT * 16][r8]
           const int r8 = sg.r8;
           const int ntn = r8 / 8;
           const uint32_t vbase = smem_u32(vres);
-          float ta[NT / 2][kDecLocalMaxR8 / 8][4];
+          float ta[kMT][kDecLocalMaxR8 / 8][4];
 #pragma unroll
-          for (int mt = 0; mt < NT / 2; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
 #pragma unroll
@@ -448,7 +456,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
               if (nt < ntn) ldsm_x2_trans(vbase + ((k0 + (lane & 15)) * r8 + nt * 8) * 2, bf[nt][0], bf[nt][1]);
 #pragma unroll
-            for (int mt = 0; mt < NT / 2; ++mt) {
+            for (int mt = 0; mt < kMT; ++mt) {
               if (mt * 16 < p.M) {
                 const int m = min(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, p.M - 1);
                 uint32_t a0, a1, a2, a3;
@@ -460,15 +468,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             }
           }
 #pragma unroll
-          for (int mt = 0; mt < NT / 2; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < kDecLocalMaxR8 / 8; ++nt)
               if (nt < ntn)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int m = mt * 16 + gq + 8 * h, c = nt * 8 + 2 * qq;
-                  part[(cw * kTok + m) * r8 + c] = ta[mt][nt][2 * h];
-                  part[(cw * kTok + m) * r8 + c + 1] = ta[mt][nt][2 * h + 1];
+                  part[(cw * kMT * 16 + m) * r8 + c] = ta[mt][nt][2 * h];
+                  part[(cw * kMT * 16 + m) * r8 + c + 1] = ta[mt][nt][2 * h + 1];
                 }
           ok = cons_sync(cbar, cph, ctl);
           if (ok) {
@@ -476,8 +484,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               const int m = idx / sg.r16, k = idx - m * sg.r16;
               float v = 0.0f;
               if (m < p.M && k < sg.r)
-                for (int w = 0; w < 8; ++w) v += part[(w * kTok + m) * r8 + k];
-              put_t(idx, v);
+                for (int w = 0; w < 8; ++w) v += part[(w * kMT * 16 + m) * r8 + k];
+              put_t(m, k, v);
             }
           }
         }
@@ -487,6 +495,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       const int kg = 8 / nslab;                 // warps sharing one slab (split over K)
       const bool active = cw < nslab * kg;
       const int slab = cw / kg, kgi = cw - slab * kg;
+      // B from resident x: this lane's token row in each n tile (rows past M repeat row
+      // M-1, so every read stays inside x; those output columns are dropped) and k pair
+      uint32_t xl[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) xl[nt] = xres_base + (min(8 * nt + gq, p.M - 1) * p.xs_ld + 2 * qq) * 2;
+
       int slot = 0;
       uint32_t phase = 0;
       for (int ch = 0; ok && ch < sg.chunks; ++ch) {
@@ -498,6 +512,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        // this lane's A row (rows past the chunk read row R-1 again; their sums are dropped,
+        // so a stage holds exactly the chunk's rows)
+        const int arow = min(16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8, R - 1);
+        const int ahi = lane >> 4;                                  // 8-wide half of a 16-wide step
+        const int arowk = arow * p.kbox;
+        const uint32_t arow_off = (arow << 7) + ((ahi ^ (arow & 7)) << 4);
         for (int sq = 0; sq < nstage; ++sq) {
           if (!warp_wait_all(&full[slot], phase, ctl)) {
             ok = false;
@@ -508,35 +528,55 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
           if (active) {
             const uint32_t wbase = smem_u32(ring + static_cast<size_t>(slot) * p.stage_bytes);
             const uint32_t xbase = wbase + p.wregion;
-            for (int step = kgi; step < nb * 4; step += kg) {
-              const int b = step >> 2, j = step & 3;
-              // rows past the chunk read row R-1 again (their sums are dropped), so a
-              // stage holds exactly the chunk's rows
-              const int arow = min(16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8, R - 1);
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(stage_addr(wbase, p.w3d, p.kbox, p.wbox_bytes, arow, b, 2 * j + (lane >> 4)), a0, a1, a2, a3);
+            const int kb_base = st * p.kbox;
+            // The kg warps of a slab take whole 64-wide k blocks in turn by their index
+            // in K (so the split stays balanced across stages), all four 16-wide steps of
+            // each. Per block the swizzled row address is computed once; the steps differ
+            // only in bits 5-6 of it.
+            for (int b = (kgi - kb_base % kg + kg) % kg; b < nb; b += kg) {
+              uint32_t rowaddr;
+              if (p.w3d) {
+                const int srow = arowk + b;
+                rowaddr = wbase + (srow << 7) + ((ahi ^ (srow & 7)) << 4);
+              } else {
+                rowaddr = wbase + b * p.wbox_bytes + arow_off;
+              }
               if (p.x_res) {
-                const int k0 = (st * p.kbox + b) * kBK + j * 16 + 2 * qq;
+                const uint32_t xk = static_cast<uint32_t>(kb_base + b) << 7;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  const int m = 8 * nt + gq;
-                  uint32_t b0 = 0, b1 = 0;
-                  if (m < p.M) {
-                    const uint32_t ad = xres_base + (m * p.xs_ld + k0) * 2;
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t a0, a1, a2, a3;
+                  ldsm_x4(rowaddr ^ (j << 5), a0, a1, a2, a3);
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t b0, b1;
+                    const uint32_t ad = xl[nt] + xk + j * 32;
                     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(ad));
                     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(ad + 16));
+                    mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
                   }
-                  mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
                 }
               } else {
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                  const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
-                  uint32_t b0, b1, b2, b3;
-                  ldsm_x4(stage_addr(xbase, p.w3d, p.kbox, xbox_bytes, brow, b, 2 * j + ((lane >> 3) & 1)), b0, b1,
-                          b2, b3);
-                  mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-                  mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t a0, a1, a2, a3;
+                  ldsm_x4(rowaddr ^ (j << 5), a0, a1, a2, a3);
+                  if constexpr (NT == 1) {
+                    uint32_t b0, b1;
+                    ldsm_x2(stage_addr(xbase, p.w3d, p.kbox, xbox_bytes, lane & 7, b, 2 * j + ((lane >> 3) & 1)), b0,
+                            b1);
+                    mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                  } else {
+#pragma unroll
+                    for (int np = 0; np < NT / 2; ++np) {
+                      const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
+                      uint32_t b0, b1, b2, b3;
+                      ldsm_x4(stage_addr(xbase, p.w3d, p.kbox, xbox_bytes, brow, b, 2 * j + ((lane >> 3) & 1)), b0,
+                              b1, b2, b3);
+                      mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                      mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    }
+                  }
                 }
               }
             }
@@ -595,7 +635,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const int idx = base + u * kDecConsumers;
-              if (idx < nt_el) put_t(idx, v[u]);
+              const int m = idx / sg.r16, k = idx - m * sg.r16;
+              if (idx < nt_el) put_t(m, k, v[u]);
             }
           }
         }
@@ -624,11 +665,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             const int arow = min(16 * slab + (lane & 7) + ((lane >> 3) & 1) * 8, R - 1);
             for (int k0 = 0; k0 < sg.r16; k0 += 16) {
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(ub + (arow * sg.r16 + k0 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+              ldsm_x4(ub + (arow * rs16 + k0 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+              if constexpr (NT == 1) {
+                const uint32_t boff = ((lane & 7) * rs16 + k0 + ((lane >> 3) & 1) * 8) * 2;
+                uint32_t b0, b1;
+                ldsm_x2(th_base + boff, b0, b1);
+                mma_16816(lw[0], a0, a1, a2, a3, b0, b1);
+                ldsm_x2(tl_base + boff, b0, b1);
+                mma_16816(lw[0], a0, a1, a2, a3, b0, b1);
+              }
 #pragma unroll
               for (int np = 0; np < NT / 2; ++np) {
                 const int brow = 16 * np + (lane & 7) + (lane >> 4) * 8;
-                const uint32_t boff = (brow * sg.r16 + k0 + ((lane >> 3) & 1) * 8) * 2;
+                const uint32_t boff = (brow * rs16 + k0 + ((lane >> 3) & 1) * 8) * 2;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(th_base + boff, b0, b1, b2, b3);
                 mma_16816(lw[2 * np], a0, a1, a2, a3, b0, b1);
@@ -689,8 +738,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
 
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<DecodeParams*>(&p)};
-  const void* fn = p.tok_tile > 16 ? reinterpret_cast<const void*>(&aq_decode_kernel<4>)
-                                   : reinterpret_cast<const void*>(&aq_decode_kernel<2>);
+  const void* fn = p.tok_tile > 16  ? reinterpret_cast<const void*>(&aq_decode_kernel<4>)
+                   : p.tok_tile > 8 ? reinterpret_cast<const void*>(&aq_decode_kernel<2>)
+                                    : reinterpret_cast<const void*>(&aq_decode_kernel<1>);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);
@@ -707,6 +757,7 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStre
 cudaError_t configure_decode(size_t max_smem) {
   cudaError_t e;
   const int s = static_cast<int>(max_smem);
+  if ((e = cudaFuncSetAttribute(aq_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = cudaFuncSetAttribute(aq_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   return cudaFuncSetAttribute(aq_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, s);
 }

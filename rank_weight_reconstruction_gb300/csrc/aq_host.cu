@@ -400,7 +400,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.M = static_cast<int32_t>(M);
     dp.K = K;
     dp.nkb = static_cast<int32_t>(ceil_div(K, kBK));
-    dp.tok_tile = M <= 16 ? 16 : 32;
+    // tokens per mma tile: every 8 tokens cost one more mma per 16 x 16 slice of W0
+    dp.tok_tile = M <= 8 ? 8 : M <= 16 ? 16 : 32;
     dp.r_total = wl.r_total;
     dp.w3d = (K % kBK) == 0 ? 1 : 0;
     int max_r8 = 0;
@@ -427,7 +428,13 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     for (int j = 0; j < n; ++j) rows_total += th[j]->out;
     // streaming CTAs: one per remaining SM, at least 8 rows each, shared among the families
     // in proportion to their rows (every family gets at least one)
-    const int G = static_cast<int>(std::max<int64_t>(n, std::min<int64_t>(dev->sms - dp.t_ctas, ceil_div(rows_total, 8))));
+    // A call whose W0 is many MB deep runs two of its own CTAs per SM: the mma.sync loop is
+    // latency-bound at one CTA (8 consumer warps) per SM, and two halve-size rings keep
+    // the same bytes in flight.
+    const bool dual = ceil_div(rows_total, 8) >= 2 * dev->sms && rows_total * K * 2 > 64ll * 1024 * 1024 &&
+                      M * (round_up(K, kBK) + 8) * 2 <= 64 * 1024;   // x resident: stages hold only W0
+    const int G = static_cast<int>(std::max<int64_t>(
+        n, std::min<int64_t>((dual ? 2 : 1) * dev->sms - dp.t_ctas, ceil_div(rows_total, 8))));
     int cnt[kMaxSeg] = {};
     int used = 0;
     for (int j = 0; j < n; ++j) {
@@ -479,13 +486,15 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     // 2-D boxes must start on 1 KB (128-byte swizzle atoms of 8 rows): round rows to 8
     dp.wbox_bytes = static_cast<uint32_t>(round_up(max_rows, 8) * 128);
     // epilogue staging: the warps' row sums (or, first, their partial t) then t itself
-    dp.ts_off = std::max(8 * 16 * dp.tok_tile, dp.t_local ? 8 * dp.tok_tile * max_r8 : 0);
+    dp.ts_off = std::max<int32_t>(8 * 16 * dp.tok_tile, dp.t_local ? 8 * round_up(dp.tok_tile, 16) * max_r8 : 0);
     const int64_t max_r16 = round_up(max_r, 16);
-    dp.epi_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.ts_off) * 4 + 2 * dp.tok_tile * max_r16 * 2, 1024));
+    // t_hi / t_lo and staged U rows are r16 wide plus 8 elements of padding (bank spread)
+    const int64_t rs16 = max_r > 0 ? max_r16 + 8 : 0;
+    dp.epi_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.ts_off) * 4 + 2 * dp.tok_tile * rs16 * 2, 1024));
     // U rows of a chunk staged in shared memory (two buffers when CTAs have several chunks)
     int max_chunks = 1;
     for (int j = 0; j < n; ++j) max_chunks = std::max(max_chunks, static_cast<int>(dp.seg[j].chunks));
-    dp.ubuf_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(max_rows) * max_r16 * 2, 128));
+    dp.ubuf_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(max_rows) * rs16 * 2, 128));
     dp.ures_bytes = max_r > 0 ? static_cast<uint32_t>(round_up((max_chunks > 1 ? 2 : 1) * dp.ubuf_bytes, 1024)) : 0u;
     // Two CTAs per SM when a CTA's W0 share is small (the next call's CTAs then stream W0
     // while this call's finish), with smaller stages if that is what it takes to fit three;
@@ -493,17 +502,29 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     const size_t fixed = kHeaderBytes + kSmemSlack + dp.epi_bytes + dp.xres_bytes + dp.vres_bytes + dp.ures_bytes;
     const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
     const size_t half = cap / 2 - 1024;
+    // With 3-D boxes a stage row is (row, k block) = row * kbox + b and the 128-byte
+    // swizzle keys on that index mod 8; ldmatrix reads 8 rows at one k block, which land
+    // on 8 different bank groups only when kbox is odd. 2-D boxes split K evenly.
+    auto pick_kbox = [&](int64_t kb) -> int64_t {
+      if (!dp.w3d) return ceil_div(dp.nkb, ceil_div(dp.nkb, kb));
+      int64_t best = 1, best_waste = INT64_MAX;
+      for (int64_t k = (kb % 2) ? kb : kb - 1; k >= std::max<int64_t>(1, kb - 4); k -= 2) {
+        const int64_t waste = ceil_div(dp.nkb, k) * k - dp.nkb;
+        if (waste < best_waste) best = k, best_waste = waste;
+      }
+      return best;
+    };
     auto set_kbox = [&](int64_t kb) {
-      dp.kbox = static_cast<int32_t>(ceil_div(dp.nkb, ceil_div(dp.nkb, kb)));   // even stages
+      dp.kbox = static_cast<int32_t>(pick_kbox(kb));
       dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
       dp.stage_bytes = static_cast<uint32_t>(
           round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
       return fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
     };
-    const int64_t kb0 = std::max<int64_t>(1, std::min<int64_t>({8, (32 * 1024) / dp.wbox_bytes, dp.nkb}));
+    const int64_t kb0 = std::max<int64_t>(1, std::min<int64_t>({9, (36 * 1024) / dp.wbox_bytes, dp.nkb}));
     int stages2 = 0;
     bool two = false;
-    if (max_share <= 128 * 1024)
+    if (max_share <= 128 * 1024 || dual)
       for (int64_t kb = kb0; kb >= 1 && !two; --kb) {
         stages2 = set_kbox(kb);
         two = stages2 >= 3 || (stages2 >= 2 && kb == 1);
