@@ -313,6 +313,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         my_k0 = (rest % (p.seg[j].r8 / 4)) * 4;
         my_vcol = vcol;
       };
+      float park[16];
+      float* park_ptr = nullptr;
       for (int blk = (few ? ct % blocks : ct); ok && worker && blk < blocks; blk += (few ? blocks : kDecConsumers)) {
         locate(blk);
         const int r8 = p.seg[my_j].r8;
@@ -339,13 +341,45 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             }
           }
         }
+        if (few) {
+          // one 4 x 4 block per (residue class, block): no two threads share a word
+          float* pb = reinterpret_cast<float*>(stage_area) + (static_cast<size_t>(ig) * blocks + blk) * 16;
+          // the staging is still being read by other threads: the partials wait in
+          // registers until everyone is done (written below)
 #pragma unroll
-        for (int x0 = 0; x0 < 4; ++x0)
+          for (int x0 = 0; x0 < 4; ++x0)
 #pragma unroll
-          for (int y0 = 0; y0 < 4; ++y0) {
-            const int m = my_m0 + x0, k = my_k0 + y0;
-            if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
+            for (int y0 = 0; y0 < 4; ++y0) park[x0 * 4 + y0] = lacc[x0][y0];
+          park_ptr = pb;
+        } else {
+#pragma unroll
+          for (int x0 = 0; x0 < 4; ++x0)
+#pragma unroll
+            for (int y0 = 0; y0 < 4; ++y0) {
+              const int m = my_m0 + x0, k = my_k0 + y0;
+              if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
+            }
+        }
+      }
+      if (few) {
+        // fixed-order sum over the residue classes through the (now free) staging area
+        if (ok) ok = cons_sync(cbar, cph, ctl);
+        if (ok && park_ptr) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) park_ptr[e] = park[e];
+        }
+        if (ok) ok = cons_sync(cbar, cph, ctl);
+        if (ok) {
+          const float* pall = reinterpret_cast<const float*>(stage_area);
+          for (int idx = ct; idx < blocks * 16; idx += kDecConsumers) {
+            float v = 0.0f;
+            for (int g2 = 0; g2 < igroups; ++g2) v += pall[g2 * blocks * 16 + idx];
+            const int blk = idx >> 4, e = idx & 15;
+            locate(blk);
+            const int m = my_m0 + (e >> 2), k = my_k0 + (e & 3);
+            if (m < p.M && k < p.seg[my_j].r) tacc[m * p.r_total + p.seg[my_j].t_col + k] = v;
           }
+        }
       }
       if (ok) ok = cons_sync(cbar, cph, ctl);
       if (ok) {

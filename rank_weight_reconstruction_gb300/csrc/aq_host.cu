@@ -560,6 +560,9 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
         }
         ++dp.t_ctas;
       }
+      // the t CTAs' fixed-order reduction parks up to 256 x 16 fp32 partials after t
+      smem = std::max<size_t>(smem, kHeaderBytes + kSmemSlack + static_cast<size_t>(tacc_bytes) + 256 * 16 * 4);
+      if (smem > cap) return fail(AQ_ERR_UNSUPPORTED, "%s: decode plan needs %zu bytes of shared memory", who, smem);
       if ((st = tmap_2d_plain(&dp.tm_xt, x, K, M, ldx, dp.vbox, static_cast<int>(M), "x (t)")) != AQ_OK) return st;
     }
     for (int j = 0; j < n; ++j) {
