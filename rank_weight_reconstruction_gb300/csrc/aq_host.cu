@@ -643,11 +643,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     gp.total_tiles = tiles;
     gp.prefetch_w = 0;  // V^T comes from the transpose kernel just before
     gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
-    gp.tmem_cols = tmem_cols_for(gp.n_mma);
+    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
+    gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);
     gp.status = dev->status;
     gp.timeout_ns = kTimeoutNs;
-    const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+    const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
     const int grid = std::min(tiles, dev->sms);
     if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch t GEMM")) != AQ_OK) return st;
   }
@@ -662,12 +662,10 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.n_mma = gp.row_tile;
   if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, gp.tok_tile, "x")) != AQ_OK) return st;
   int tiles = 0;
-  bool any_lr = false;
   for (int j = 0; j < n; ++j) {
     GemmSeg& s = gp.seg[gp.nseg++];
     if ((st = tmap_2d(&s.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, gp.row_tile, "W0")) != AQ_OK) return st;
     if (th[j]->r > 0) {
-      any_lr = true;
       if ((st = tmap_2d(&s.tm_u, th[j]->U, th[j]->r, th[j]->out, th[j]->ld_u, gp.row_tile, "U")) != AQ_OK) return st;
       if ((st = tmap_2d(&s.tm_t, tbuf + wl.t_col[j], th[j]->r, M, wl.ld_t, gp.tok_tile, "t")) != AQ_OK) return st;
     }
@@ -683,11 +681,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.total_tiles = tiles;
   gp.prefetch_w = 1;
   gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kSmemSlack);
-  gp.tmem_cols = tmem_cols_for(any_lr ? 2 * gp.n_mma : gp.n_mma);
+  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
+  gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);   // two accumulator buffers
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;
-  const size_t smem = kSmemSlack + kHeaderBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+  const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
   const int grid = std::min(tiles, dev->sms);
   if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK) return st;
   t_last_path = AQ_PATH_PREFILL;

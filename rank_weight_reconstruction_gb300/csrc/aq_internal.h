@@ -15,6 +15,7 @@ constexpr int kMaxSeg = 3;         // projection families batched into one launc
 constexpr int kGemmThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
 constexpr int kStageA = kMmaM * 128;  // bytes of the A tile of one stage (128 rows x 128 B)
 constexpr int kHeaderBytes = 1024;    // barriers + TMEM address at the start of shared memory
+constexpr int kGemmSBufBytes = 1024;  // prefill GEMM: s of the current tile (fp32, n_mma <= 256)
 constexpr int kMaxStages = 16;
 
 // One projection family (segment) of a batched GEMM launch.
@@ -48,7 +49,7 @@ struct GemmParams {
   int32_t prefetch_w;   // 1: the row operand is a weight and may be loaded before the
                         //    previous grid completes; 0: it is produced by that grid
   uint32_t stage_bytes; // kStageA + n_mma * 128, rounded to 1024
-  uint32_t tmem_cols;   // power of two >= 2 * n_mma (or n_mma without a low-rank term)
+  uint32_t tmem_cols;   // power of two >= 2 * n_mma: two accumulator buffers
   int32_t* status;      // device status word
   uint64_t timeout_ns;
 };

@@ -4,9 +4,11 @@
 //
 // aq_gemm_kernel         prefill (M > 32): tcgen05 GEMM over the K = in loop with a TMA-fed
 //                        shared-memory ring, 128 tokens per tile as accumulator lanes and
-//                        output rows as N; the rank-r up-projection runs as extra K blocks
-//                        into a second TMEM accumulator and the epilogue forms
-//                        s * D_main + D_low, rounded once. Also the t = x V GEMM.
+//                        output rows as N, two accumulator buffers so a tile's epilogue
+//                        overlaps the next tile's MMAs; the epilogue scales the W0 x sum by
+//                        s in TMEM, the rank-r up-projection is then added as extra K blocks
+//                        into the same accumulator, and y is rounded once. Also the t = x V
+//                        GEMM.
 // aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
 // aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
 //                        epilogue, W_eff written back with TMA stores.
@@ -67,17 +69,27 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
   return c;
 }
 
+// Two accumulator buffers of n_mma TMEM columns each, so a tile's epilogue overlaps the next
+// tile's MMAs. The rank-r term needs no buffer of its own: once the W0 K loop of tile i is
+// done, the epilogue scales the accumulator by s in place, and the MMA warp adds U t into it
+// after the next tile's W0 loop. Work items therefore reach the pipeline in the order
+//   main(0), main(1), low(0), main(2), low(1), ..., low(last)
+// which the producer and the MMA warp both walk with the same loop.
 __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* tmem_full = empty + kMaxStages;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* mma_done = tmem_empty + 1;
+  uint64_t* acc_full = empty + kMaxStages;   // [2] W0 loop of a tile done (MMA commit)
+  uint64_t* acc_scaled = acc_full + 2;       // [2] accumulator scaled by s (epilogue, 128)
+  uint64_t* acc_done = acc_scaled + 2;       // [2] rank-r blocks added (MMA commit)
+  uint64_t* acc_empty = acc_done + 2;        // [2] accumulator drained (epilogue, 128)
+  uint64_t* epi_bar = acc_empty + 2;         // epilogue warps' own barrier (128)
+  uint64_t* mma_done = epi_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  uint8_t* ring = smem + kHeaderBytes;
+  float* sbuf = reinterpret_cast<float*>(smem + kHeaderBytes);   // s of the current tile, fp32
+  uint8_t* ring = smem + kHeaderBytes + kGemmSBufBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -88,8 +100,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4 * 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_scaled[b], 4 * 32);
+      mbar_init(&acc_done[b], 1);
+      mbar_init(&acc_empty[b], 4 * 32);
+    }
+    mbar_init(epi_bar, 4 * 32);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -117,6 +134,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   const uint32_t tmem_base = *tmem_slot;
   const int nkb_main = ceil_div_i(p.K, kBK);
   const uint32_t tx_bytes = static_cast<uint32_t>(p.row_tile + p.tok_tile) * 128u;
+  const int n_it = blockIdx.x < p.total_tiles ? (p.total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto tile_of = [&](int it) { return blockIdx.x + it * gridDim.x; };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -126,51 +145,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       uint32_t phase = 0;
       uint32_t filled = 0, fill_par = 0;
       bool ok = true;
-      int it = 0;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-        const TileCoord tc = tile_coord(p, tile);
-        const GemmSeg& sg = p.seg[tc.seg];
-        const int nkb = nkb_main + (sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0);
-        int kb = 0;
-        if (it == 0 && !p.prefetch_w) pdl_wait_prior_grid();
-        if (it == 0 && p.prefetch_w) {
-          // Weight tiles of the first stages go out before waiting on the previous grid.
-          const int pre = nkb_main < p.stages ? nkb_main : p.stages;
-          for (; kb < pre; ++kb) {
-            uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
-            mbar_arrive_expect_tx(&full[kb], tx_bytes);
-            tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
-            filled |= 1u << kb;
-          }
-          pdl_wait_prior_grid();
-          for (int j = 0; j < pre; ++j) {
-            uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-            tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
-          }
-          stage = pre;
-          if (stage == p.stages) {
-            stage = 0;
-            phase ^= 1;
-          }
+      // one k block of work item (tile, low) into the next stage
+      auto push = [&](const TileCoord& tc, const GemmSeg& sg, bool low, int kb) -> bool {
+        if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) return false;
+        uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+        // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
+        tma_load_2d(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage], pol);
+        tma_load_2d(st + kStageA, low ? &sg.tm_u : &sg.tm_w, kb * kBK, tc.row0, &full[stage], pol);
+        filled |= 1u << stage;
+        fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1;
         }
-        for (; kb < nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) {
-            ok = false;
-            break;
+        return true;
+      };
+      if (!p.prefetch_w || n_it == 0) pdl_wait_prior_grid();
+      for (int it = 0; ok && it <= n_it; ++it) {
+        if (it < n_it) {
+          const TileCoord tc = tile_coord(p, tile_of(it));
+          const GemmSeg& sg = p.seg[tc.seg];
+          int kb = 0;
+          if (it == 0 && p.prefetch_w) {
+            // Weight tiles of the first stages go out before waiting on the previous grid.
+            const int pre = nkb_main < p.stages ? nkb_main : p.stages;
+            for (; kb < pre; ++kb) {
+              uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
+              mbar_arrive_expect_tx(&full[kb], tx_bytes);
+              tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
+              filled |= 1u << kb;
+            }
+            pdl_wait_prior_grid();
+            for (int j = 0; j < pre; ++j) {
+              uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
+              tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
+            }
+            stage = pre;
+            if (stage == p.stages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], tx_bytes);
-          // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
-          const bool main_blk = kb < nkb_main;
-          const int ka = main_blk ? kb * kBK : (kb - nkb_main) * kBK;
-          tma_load_2d(st, main_blk ? &p.tm_x : &sg.tm_t, ka, tc.tok0, &full[stage], pol);
-          tma_load_2d(st + kStageA, main_blk ? &sg.tm_w : &sg.tm_u, ka, tc.row0, &full[stage], pol);
-          filled |= 1u << stage;
-          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1;
-          }
+          for (; ok && kb < nkb_main; ++kb) ok = push(tc, sg, false, kb);
+        }
+        if (ok && it >= 1) {
+          const TileCoord tc = tile_coord(p, tile_of(it - 1));
+          const GemmSeg& sg = p.seg[tc.seg];
+          const int nkb_low = sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0;
+          for (int kb = 0; ok && kb < nkb_low; ++kb) ok = push(tc, sg, true, kb);
         }
       }
       if (!ok) {
@@ -184,38 +207,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     const uint32_t idesc = idesc_bf16_f32(kMmaM, p.n_mma);
     int stage = 0;
     uint32_t phase = 0;
-    int it = 0;
     bool ok = true;
-    // Start the bounded waits only once the previous grid is done, so that a long
-    // predecessor cannot be mistaken for a stalled pipeline.
-    pdl_wait_prior_grid();
-    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(p, tile);
-      const GemmSeg& sg = p.seg[tc.seg];
-      const int nkb = nkb_main + (sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0);
-      if (!warp_wait(tmem_empty, (it & 1) ^ 1, ctl)) break;
-      tc_fence_after();
+    // k blocks of one work item into accumulator buffer b; `acc` = 1 adds to what is there
+    auto run = [&](int nkb, int rem_last, uint32_t b, uint32_t acc) -> bool {
+      const uint32_t d = tmem_base + b * static_cast<uint32_t>(p.n_mma);
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!warp_wait(&full[stage], phase, ctl)) {
-          ok = false;
-          break;
-        }
+        if (!warp_wait(&full[stage], phase, ctl)) return false;
         tc_fence_after();
         if (lane == 0) {
-          const bool low = kb >= nkb_main;
-          const int kb_local = low ? kb - nkb_main : kb;
-          const uint32_t d = tmem_base + (low ? static_cast<uint32_t>(p.n_mma) : 0u);
           const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t b_addr = a_addr + kStageA;
-          int nk = kBK / kUmmaK;
-          if (low) {
-            const int rem = sg.r - kb_local * kBK;
-            nk = rem >= kBK ? nk : ceil_div_i(rem, kUmmaK);
-          }
-          for (int j = 0; j < nk; ++j) {
+          const int nk = (kb == nkb - 1 && rem_last > 0) ? ceil_div_i(rem_last, kUmmaK) : kBK / kUmmaK;
+          for (int j = 0; j < nk; ++j)
             tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc,
-                        (kb_local > 0 || j > 0) ? 1u : 0u);
-          }
+                        (acc || kb > 0 || j > 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
         }
         __syncwarp();
@@ -224,8 +229,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           phase ^= 1;
         }
       }
-      if (ok && lane == 0) tc_commit(tmem_full);
-      __syncwarp();
+      return true;
+    };
+    // Start the bounded waits only once the previous grid is done, so that a long
+    // predecessor cannot be mistaken for a stalled pipeline.
+    pdl_wait_prior_grid();
+    for (int it = 0; ok && it <= n_it; ++it) {
+      if (it < n_it) {
+        const uint32_t b = it & 1;
+        if (!warp_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, ctl)) break;
+        tc_fence_after();
+        ok = run(nkb_main, 0, b, 0u);
+        if (ok && lane == 0) tc_commit(&acc_full[b]);
+        __syncwarp();
+      }
+      if (ok && it >= 1) {
+        const TileCoord tc = tile_coord(p, tile_of(it - 1));
+        const GemmSeg& sg = p.seg[tc.seg];
+        if (sg.r > 0) {
+          const uint32_t b = (it - 1) & 1;
+          if (!warp_wait(&acc_scaled[b], ((it - 1) >> 1) & 1, ctl)) break;
+          tc_fence_after();
+          ok = run(ceil_div_i(sg.r, kBK), sg.r % kBK, b, 1u);
+          if (ok && lane == 0) tc_commit(&acc_done[b]);
+          __syncwarp();
+        }
+      }
     }
     if (lane == 0) {
       tc_commit(mma_done);
@@ -235,70 +264,82 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   } else {
     // ---------------- epilogue: warps 2..5, one TMEM lane quadrant each ----------------
     const int q = warp & 3;
-    const int lrow = q * 32 + lane;
+    const int et = q * 32 + lane;                 // 0..127: TMEM lane = token of the tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t ephase = 0;
+    auto epi_sync = [&]() {
+      mbar_arrive(epi_bar);
+      const bool r = mbar_wait(epi_bar, ephase, ctl);
+      ephase ^= 1u;
+      return r;
+    };
     pdl_wait_prior_grid();
-    int it = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(p, tile);
+    for (int it = 0; it < n_it; ++it) {
+      const TileCoord tc = tile_coord(p, tile_of(it));
       const GemmSeg& sg = p.seg[tc.seg];
       const bool has_lr = sg.r > 0;
-      if (!warp_wait(tmem_full, it & 1, ctl)) break;
+      const uint32_t b = it & 1;
+      const uint32_t par = (it >> 1) & 1;
+      const uint32_t acc = t_lane + b * static_cast<uint32_t>(p.n_mma);
+      // s of this tile's rows into shared memory (fp32, zero past the tile) while the
+      // tensor core works on it
+      if (!epi_sync()) break;   // every epilogue warp is done with the previous tile's s
+      for (int c = et; c < p.n_mma; c += 4 * 32) {
+        const int o = tc.row0 + c;
+        sbuf[c] = (c < p.row_tile && o < sg.rows) ? (sg.s ? bf16_to_f32(sg.s[o]) : 1.0f) : 0.0f;
+      }
+      if (!epi_sync()) break;
+      if (!warp_wait(&acc_full[b], par, ctl)) break;
       tc_fence_after();
-      {
-        const int tok = tc.tok0 + lrow;
-        const bool tok_ok = tok < p.M;
-        uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
+      if (has_lr) {
+        // scale the W0 x accumulator by s in place; the MMA warp then adds U t
         for (int c = 0; c < p.n_mma; c += 16) {
-          float a[16], b[16];
-          tmem_ld_16(t_lane + c, a);
-          if (has_lr) tmem_ld_16(t_lane + p.n_mma + c, b);
-          tmem_ld_wait();
-          const int o0 = tc.row0 + c;
-          if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
-          float sc[16];
-          const bool full_chunk = (c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows);
-          if (sg.s == nullptr) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sc[j] = 1.0f;
-          } else if (full_chunk) {
-            const uint4 s0 = __ldg(reinterpret_cast<const uint4*>(sg.s + o0));
-            const uint4 s1 = __ldg(reinterpret_cast<const uint4*>(sg.s + o0 + 8));
-            const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              sc[2 * j] = __uint_as_float(sw[j] << 16);
-              sc[2 * j + 1] = __uint_as_float(sw[j] & 0xFFFF0000u);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              sc[j] = (c + j < p.row_tile && o0 + j < sg.rows) ? bf16_to_f32(sg.s[o0 + j]) : 0.0f;
-          }
           float v[16];
+          tmem_ld_16(acc + c, v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = fmaf(sc[j], a[j], has_lr ? b[j] : 0.0f);
-          if (full_chunk) {
-            uint4 w0, w1;
-            w0.x = pack_bf16x2(v[0], v[1]);
-            w0.y = pack_bf16x2(v[2], v[3]);
-            w0.z = pack_bf16x2(v[4], v[5]);
-            w0.w = pack_bf16x2(v[6], v[7]);
-            w1.x = pack_bf16x2(v[8], v[9]);
-            w1.y = pack_bf16x2(v[10], v[11]);
-            w1.z = pack_bf16x2(v[12], v[13]);
-            w1.w = pack_bf16x2(v[14], v[15]);
-            *reinterpret_cast<uint4*>(yrow + o0) = w0;
-            *reinterpret_cast<uint4*>(yrow + o0 + 8) = w1;
-          } else {
+          for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
+          tmem_st_16(acc + c, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&acc_scaled[b]);
+        if (!warp_wait(&acc_done[b], par, ctl)) break;
+        tc_fence_after();
+      }
+      const int tok = tc.tok0 + et;
+      const bool tok_ok = tok < p.M;
+      uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
+      for (int c = 0; c < p.n_mma; c += 16) {
+        float v[16];
+        tmem_ld_16(acc + c, v);
+        tmem_ld_wait();
+        const int o0 = tc.row0 + c;
+        if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
+        if (!has_lr) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < p.row_tile && o0 + j < sg.rows) yrow[o0 + j] = f32_to_bf16_rn(v[j]);
-          }
+          for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
+        }
+        if ((c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows)) {
+          uint4 w0, w1;
+          w0.x = pack_bf16x2(v[0], v[1]);
+          w0.y = pack_bf16x2(v[2], v[3]);
+          w0.z = pack_bf16x2(v[4], v[5]);
+          w0.w = pack_bf16x2(v[6], v[7]);
+          w1.x = pack_bf16x2(v[8], v[9]);
+          w1.y = pack_bf16x2(v[10], v[11]);
+          w1.z = pack_bf16x2(v[12], v[13]);
+          w1.w = pack_bf16x2(v[14], v[15]);
+          *reinterpret_cast<uint4*>(yrow + o0) = w0;
+          *reinterpret_cast<uint4*>(yrow + o0 + 8) = w1;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < p.row_tile && o0 + j < sg.rows) yrow[o0 + j] = f32_to_bf16_rn(v[j]);
         }
       }
       tc_fence_before();
-      mbar_arrive(tmem_empty);
+      mbar_arrive(&acc_empty[b]);
     }
   }
 
@@ -307,7 +348,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
-
 // ------------------------------------------------------------------------------------
 // V [in, r] -> V^T [r, in]
 // ------------------------------------------------------------------------------------
