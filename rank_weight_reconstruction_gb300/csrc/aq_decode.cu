@@ -211,6 +211,22 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         issue(q, q, true, false);
         filled |= 1u << q;
       }
+      if (p.l2_prefetch) {
+        // the rest of this CTA's W0 share streams into L2 now, while the previous call
+        // finishes; after the dependency wait its stages then load from L2
+        for (int q = pre; q < total; ++q) {
+          const int ch = q / nstage;
+          const int st = (q - ch * nstage + rot) % nstage;
+          const int row0 = (l * sg.chunks + ch) * R;
+          const int kb0 = st * p.kbox;
+          if (p.w3d) {
+            tma_prefetch_l2_3d(&sg.tm_w, 0, kb0, row0);
+          } else {
+            const int nb = min(p.kbox, p.nkb - kb0);
+            for (int b = 0; b < nb; ++b) tma_prefetch_l2_2d(&sg.tm_w, (kb0 + b) * kBK, row0);
+          }
+        }
+      }
       if (local_t) {
         const int nvb = (p.K + p.vbox - 1) / p.vbox;
         const uint32_t vb = static_cast<uint32_t>(p.vbox) * sg.r8 * 2u;

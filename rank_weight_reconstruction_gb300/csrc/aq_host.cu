@@ -302,7 +302,7 @@ int stages_for(uint32_t stage_bytes, size_t smem_cap, size_t fixed) {
   return std::max(2, std::min(st, kMaxStages));
 }
 
-// Prefill N tile: minimise (waves x tile width + per-tile overhead).
+// Prefill N tile: minimise waves x the cost of one tile.
 int prefill_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int sms) {
   static const int cand[] = {256, 224, 192, 160, 128, 112, 96, 80, 64, 48, 32, 16};
   int best = 256;
@@ -310,7 +310,10 @@ int prefill_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int 
   for (int bn : cand) {
     int64_t tiles = 0;
     for (int j = 0; j < n; ++j) tiles += n_tok_tiles * ceil_div(th[j]->out, bn);
-    const double cost = static_cast<double>(ceil_div(tiles, sms)) * (bn + 32);
+    // A tcgen05.mma of M = 128, K = 16 costs about (N + 230) / 486 of an N = 256 one on this
+    // part (measured on the 31B-class prefill: 128-wide tiles take 1.48x, 64-wide 2.8x the
+    // time of 256-wide ones for the same work), so narrow tiles only pay when they save waves.
+    const double cost = static_cast<double>(ceil_div(tiles, sms)) * (bn + 230);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = bn;
@@ -409,6 +412,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     const int64_t kp = static_cast<int64_t>(dp.nkb) * kBK;
     dp.xs_ld = static_cast<int32_t>(kp + 8);
     dp.x_res = M * (kp + 8) * 2 <= 64 * 1024 ? 1 : 0;
+    {
+      int64_t w0_bytes = 0;
+      for (int j = 0; j < n; ++j) w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
+      dp.l2_prefetch = w0_bytes <= 48ll * 1024 * 1024 ? 1 : 0;   // L2 is 126 MB
+    }
     dp.xres_bytes = dp.x_res ? static_cast<uint32_t>(round_up(M * (kp + 8) * 2, 1024)) : 0u;
     // t = V^T x: computed by every streaming CTA for its own family when that family's V
     // is small (no cross-CTA dependency at all), else by t CTAs publishing through the
@@ -524,10 +532,12 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     const int64_t kb0 = std::max<int64_t>(1, std::min<int64_t>({9, (36 * 1024) / dp.wbox_bytes, dp.nkb}));
     int stages2 = 0;
     bool two = false;
+    // (boxes of fewer than 3 k blocks stall TMA on request rate: below that, one CTA per SM)
+    const int64_t kb_min = std::min<int64_t>(3, kb0);
     if (max_share <= 128 * 1024 || dual)
-      for (int64_t kb = kb0; kb >= 1 && !two; --kb) {
+      for (int64_t kb = kb0; kb >= kb_min && !two; --kb) {
         stages2 = set_kbox(kb);
-        two = stages2 >= 3 || (stages2 >= 2 && kb == 1);
+        two = stages2 >= 3 || (stages2 >= 2 && kb == kb_min);
       }
     if (two) {
       dp.stages = std::min(stages2, kMaxStages);

@@ -106,6 +106,8 @@ struct DecodeParams {
   int32_t kbox;        // k blocks per pipeline stage
   int32_t w3d;         // 1: W0 / x stages are single 3-D boxes (K is a multiple of 64)
   int32_t x_res;       // 1: x resident in shared memory for the whole call
+  int32_t l2_prefetch; // 1: before the dependency wait, pull the W0 stages that do not fit the
+                       // ring into L2 (calls whose W0 fits comfortably in L2)
   int32_t xs_ld;       // row stride (elements) of resident x: round_up(K, 64) + 8
   int32_t tok_tile;    // 16 or 32
   int32_t r_total;
