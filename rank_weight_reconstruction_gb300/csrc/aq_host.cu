@@ -773,12 +773,17 @@ aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* 
     if ((st = tmap_2d(&pp.tm_v, th->V, th->r, th->in, th->ld_v, pp.bn, "V")) != AQ_OK) return st;
   }
   pp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + pp.bn * 128, 1024));
-  pp.stages = 3;
+  pp.stages = th->r > 0 ? 2 : 0;   // U / V chunks come from L2; a short ring suffices
+  // the rest of shared memory holds W0 / W_eff tiles: the W0 reads in flight are what keep
+  // this stream near the HBM rate
+  const size_t cbuf_bytes = static_cast<size_t>(pp.bn) * 256u;
+  const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
+  const size_t fixed = kSmemSlack + kHeaderBytes + static_cast<size_t>(pp.stages) * pp.stage_bytes;
+  pp.cbufs = static_cast<int32_t>(std::min<size_t>(8, (cap - fixed) / cbuf_bytes));
   pp.tmem_cols = th->r > 0 ? tmem_cols_for(2 * pp.bn) : 32;
   pp.status = dev->status;
   pp.timeout_ns = kTimeoutNs;
-  const size_t smem = kSmemSlack + kHeaderBytes + 3u * static_cast<size_t>(pp.bn) * 256u +
-                      static_cast<size_t>(pp.stages) * pp.stage_bytes;
+  const size_t smem = fixed + static_cast<size_t>(pp.cbufs) * cbuf_bytes;
   if (smem > dev->smem_optin) return fail(AQ_ERR_UNSUPPORTED, "aq_precompute: needs %zu bytes of shared memory", smem);
   const int grid = std::min(pp.total_tiles, dev->sms);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

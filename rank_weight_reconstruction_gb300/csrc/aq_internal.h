@@ -13,6 +13,7 @@ constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
 constexpr int kMmaM = 128;         // accumulator lanes (tokens or output rows)
 constexpr int kMaxSeg = 3;         // projection families batched into one launch
 constexpr int kGemmThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kPreThreads = 320;   // precompute: warps 2-9 epilogue, two per TMEM lane quadrant
 constexpr int kStageA = kMmaM * 128;  // bytes of the A tile of one stage (128 rows x 128 B)
 constexpr int kHeaderBytes = 1024;    // barriers + TMEM address at the start of shared memory
 constexpr int kGemmSBufBytes = 1024;  // prefill GEMM: s of the current tile (fp32, n_mma <= 256)
@@ -165,6 +166,8 @@ struct PrecomputeParams {
   int32_t n_col_tiles;
   int32_t total_tiles;
   int32_t stages;      // operand ring depth (U/V chunks)
+  int32_t cbufs;       // W0 / W_eff tile buffers (<= 8): W0 tiles in flight while others are
+                       // in the epilogue or being stored
   uint32_t stage_bytes;
   uint32_t tmem_cols;
   int32_t* status;

@@ -379,26 +379,26 @@ __global__ void __launch_bounds__(256) aq_transpose_kernel(const __grid_constant
 // ------------------------------------------------------------------------------------
 // W_eff = s * W0 + U V^T
 // ------------------------------------------------------------------------------------
-constexpr int kPreCBufs = 3;   // W0 / W_eff tiles in flight per CTA
+constexpr int kPreMaxCBufs = 8;   // W0 / W_eff tile buffers per CTA (p.cbufs of them used)
 constexpr int kPreAcc = 2;     // TMEM accumulators
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kPreThreads, 1)
     aq_precompute_kernel(const __grid_constant__ PrecomputeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint64_t* c_full = empty + kMaxStages;
-  uint64_t* c_empty = c_full + kPreCBufs;
-  uint64_t* acc_full = c_empty + kPreCBufs;
+  uint64_t* c_empty = c_full + kPreMaxCBufs;
+  uint64_t* acc_full = c_empty + kPreMaxCBufs;
   uint64_t* acc_empty = acc_full + kPreAcc;
   uint64_t* epi_done = acc_empty + kPreAcc;
-  uint64_t* mma_done = epi_done + kPreCBufs;
+  uint64_t* mma_done = epi_done + kPreMaxCBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t cbuf_bytes = static_cast<uint32_t>(p.bn) * 256u;  // bn/64 boxes of 128 x 128 B
   uint8_t* cbuf = smem + kHeaderBytes;
-  uint8_t* ring = cbuf + kPreCBufs * cbuf_bytes;
+  uint8_t* ring = cbuf + p.cbufs * cbuf_bytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -412,14 +412,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < kPreCBufs; ++b) {
+    for (int b = 0; b < p.cbufs; ++b) {
       mbar_init(&c_full[b], 1);
       mbar_init(&c_empty[b], 1);
-      mbar_init(&epi_done[b], 4 * 32);
+      mbar_init(&epi_done[b], kPreThreads - 64);
     }
     for (int b = 0; b < kPreAcc; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4 * 32);
+      mbar_init(&acc_empty[b], kPreThreads - 64);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -446,20 +446,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
+    // Two independent producers: lane 0 streams W0 tiles as far ahead as the tile buffers
+    // allow, lane 1 feeds the U / V chunks of the MMA. One thread doing both would tie the
+    // W0 prefetch depth to the MMA's progress through the short U / V ring.
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t filled = 0, fill_par = 0, cfilled = 0, cfill_par = 0;
+      uint32_t cfilled = 0, cfill_par = 0;
       bool ok = true;
       pdl_wait_prior_grid();
       int it = 0;
       for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
         const int o0 = (tile / p.n_col_tiles) * kMmaM;
         const int i0 = (tile % p.n_col_tiles) * p.bn;
-        const int cb = it % kPreCBufs;
-        const uint32_t cph = static_cast<uint32_t>(it / kPreCBufs) & 1u;
+        const int cb = it % p.cbufs;
+        const uint32_t cph = static_cast<uint32_t>(it / p.cbufs) & 1u;
         if (!mbar_wait(&c_empty[cb], cph ^ 1u, ctl)) {
           ok = false;
           break;
@@ -470,6 +470,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       pol_stream);
         cfilled |= 1u << cb;
         cfill_par = (cfill_par & ~(1u << cb)) | (cph << cb);
+      }
+      if (!ok) {
+        for (int b = 0; b < p.cbufs; ++b)
+          if (cfilled & (1u << b)) mbar_wait_drain(&c_full[b], (cfill_par >> b) & 1u, kDrainNs);
+      }
+    } else if (lane == 1 && has_mma) {
+      const uint64_t pol_keep = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, fill_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const int o0 = (tile / p.n_col_tiles) * kMmaM;
+        const int i0 = (tile % p.n_col_tiles) * p.bn;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) {
             ok = false;
@@ -490,8 +504,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         for (int s = 0; s < p.stages; ++s)
           if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_par >> s) & 1u, kDrainNs);
-        for (int b = 0; b < kPreCBufs; ++b)
-          if (cfilled & (1u << b)) mbar_wait_drain(&c_full[b], (cfill_par >> b) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -543,12 +555,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lrow = q * 32 + lane;  // row of the tile (TMEM lane) this thread owns
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const bool leader = (warp == 2 && lane == 0);
+    const int chalf = (warp - 2) >> 2;  // which half of the tile's columns this warp does
     int it = 0;
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
       const int o0 = (tile / p.n_col_tiles) * kMmaM;
       const int i0 = (tile % p.n_col_tiles) * p.bn;
-      const int cb = it % kPreCBufs;
-      const uint32_t cph = static_cast<uint32_t>(it / kPreCBufs) & 1u;
+      const int cb = it % p.cbufs;
+      const uint32_t cph = static_cast<uint32_t>(it / p.cbufs) & 1u;
       const int ab = it & 1;
       const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
       if (!warp_wait(&c_full[cb], cph, ctl)) break;
@@ -559,20 +572,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int o = o0 + lrow;
       const float sc = (o < p.out) ? bf16_to_f32(p.s[o]) : 0.0f;
       uint8_t* ctile = cbuf + cb * cbuf_bytes;
-      for (int c = 0; c < p.bn; c += 16) {
-        float d[16];
+      const int cw = p.bn / 2;   // columns per warp of the pair, a multiple of 32
+      for (int c = chalf * cw; c < (chalf + 1) * cw; c += 32) {
+        float d[32];
         if (has_mma) {
-          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c), d);
+          float d0[16], d1[16];
+          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c), d0);
+          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c + 16), d1);
           tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            d[j] = d0[j];
+            d[16 + j] = d1[j];
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) d[j] = 0.0f;
+          for (int j = 0; j < 32; ++j) d[j] = 0.0f;
         }
-        // W0 row segment: box (c / 64), two 16-byte chunks at swizzled positions.
+        // W0 row segment: box (c / 64), four 16-byte chunks at swizzled positions.
         uint8_t* rowp = ctile + (c / 64) * kStageA + lrow * 128;
         const int ch0 = (c % 64) / 8;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 4; ++h) {
           uint4* cp = reinterpret_cast<uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4));
           const uint4 w = *cp;
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -598,8 +619,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!mbar_wait(&epi_done[cb], cph, ctl)) break;
         for (int j = 0; j < nbox; ++j) tma_store_2d(&p.tm_we, ctile + j * kStageA, i0 + 64 * j, o0);
         tma_store_commit();
-        tma_store_wait_read_all();
-        mbar_arrive(&c_empty[cb]);
+        // one store group may still be reading its buffer: release the previous tile's
+        if (it > 0) {
+          tma_store_wait_read_but_one();
+          mbar_arrive(&c_empty[(it - 1) % p.cbufs]);
+        }
       }
     }
     if (leader) tma_store_wait_all();
@@ -673,7 +697,7 @@ cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t s
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
                               bool pdl) {
   void* args[] = {const_cast<PrecomputeParams*>(&p)};
-  return launch_ex(reinterpret_cast<const void*>(&aq_precompute_kernel), dim3(grid), dim3(kGemmThreads),
+  return launch_ex(reinterpret_cast<const void*>(&aq_precompute_kernel), dim3(grid), dim3(kPreThreads),
                    smem, st, pdl, args);
 }
 
