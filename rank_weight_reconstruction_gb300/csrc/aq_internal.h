@@ -13,7 +13,7 @@ constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
 constexpr int kMmaM = 128;         // accumulator lanes (tokens or output rows)
 constexpr int kMaxSeg = 3;         // projection families batched into one launch
 constexpr int kGemmThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
-constexpr int kPreThreads = 320;   // precompute: warps 2-9 epilogue, two per TMEM lane quadrant
+constexpr int kPreThreads = 576;   // precompute: warps 2-17 epilogue, four per TMEM lane quadrant
 constexpr int kStageA = kMmaM * 128;  // bytes of the A tile of one stage (128 rows x 128 B)
 constexpr int kHeaderBytes = 1024;    // barriers + TMEM address at the start of shared memory
 constexpr int kGemmSBufBytes = 1024;  // prefill GEMM: s of the current tile (fp32, n_mma <= 256)

@@ -555,7 +555,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const int lrow = q * 32 + lane;  // row of the tile (TMEM lane) this thread owns
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const bool leader = (warp == 2 && lane == 0);
-    const int chalf = (warp - 2) >> 2;  // which half of the tile's columns this warp does
+    const int chalf = (warp - 2) >> 2;  // which part of the tile's columns this warp does
+    constexpr int kParts = (kPreThreads - 64) / 128;
     int it = 0;
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
       const int o0 = (tile / p.n_col_tiles) * kMmaM;
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const int o = o0 + lrow;
       const float sc = (o < p.out) ? bf16_to_f32(p.s[o]) : 0.0f;
       uint8_t* ctile = cbuf + cb * cbuf_bytes;
-      const int cw = p.bn / 2;   // columns per warp of the pair, a multiple of 32
+      const int cw = p.bn / kParts;   // columns per warp, a multiple of 32
       for (int c = chalf * cw; c < (chalf + 1) * cw; c += 32) {
         float d[32];
         if (has_mma) {
