@@ -524,7 +524,10 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     };
     auto set_kbox = [&](int64_t kb) {
       dp.kbox = static_cast<int32_t>(pick_kbox(kb));
-      dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) * dp.wbox_bytes, 1024));
+      // a 3-D box is kbox x rows lines of 128 bytes, packed; 2-D boxes start on 1 KB each
+      dp.wregion = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.kbox) *
+                                                      (dp.w3d ? static_cast<int64_t>(max_rows) * 128 : dp.wbox_bytes),
+                                                  1024));
       dp.stage_bytes = static_cast<uint32_t>(
           round_up(dp.wregion + (dp.x_res ? 0 : static_cast<int64_t>(dp.kbox) * dp.tok_tile * 128), 1024));
       return fixed < half ? static_cast<int>((half - fixed) / dp.stage_bytes) : 0;
