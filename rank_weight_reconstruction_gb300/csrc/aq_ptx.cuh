@@ -49,21 +49,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
-// Like mbar_try_wait, but the thread may sleep up to 20 us (or until the phase completes)
-// instead of returning at once: a waiting warp then takes no issue slots from the warps
-// that do the work.
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -89,7 +74,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*reinterpret_cast<volatile int*>(ctl.abort_flag)) return false;
       if (global_timer_ns() - t0 > ctl.timeout_ns) {
