@@ -303,10 +303,12 @@ class DecodeStack:
             ws = max(ws, aq.aq_linear_workspace_bytes([th0["q_proj"], th0["k_proj"], th0["v_proj"]], M))
             for f in ("o_proj", "gate_proj", "up_proj", "down_proj"):
                 ws = max(ws, aq.aq_linear_workspace_bytes(th0[f], M))
+            ws = max(ws, aq.aq_linear_workspace_bytes([th0["gate_proj"], th0["up_proj"]], M))
         self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)   # sync part must start at 0
 
-    def calls(self, only=None):
-        """List of (family key, callable) in step order."""
+    def calls(self, only=None, fuse_gateup=False):
+        """List of (family key, callable) in step order. fuse_gateup: gate and up of a layer
+        go through one aq_linear_multi call (the pages' gate-up fusion)."""
         import rank_weight_reconstruction_gb300 as aq
         out = []
         for (M, layer, xv), yv in zip(self.x_views, self.y_views):
@@ -315,16 +317,25 @@ class DecodeStack:
                 out.append(("qkv", M, lambda th=th, xv=xv, yv=yv: aq.aq_linear_qkv(
                     [th["q_proj"], th["k_proj"], th["v_proj"]], xv["qkv"],
                     ys=[yv["q_proj"], yv["k_proj"], yv["v_proj"]], workspace=self.ws)))
-            for f, key in (("o_proj", "o"), ("gate_proj", "mlp"), ("up_proj", "mlp"), ("down_proj", "down")):
+            fams = (("o_proj", "o"), ("gate_proj", "mlp"), ("up_proj", "mlp"), ("down_proj", "down"))
+            for f, key in fams:
+                if fuse_gateup and f == "up_proj":
+                    continue
+                if fuse_gateup and f == "gate_proj":
+                    if only is None:
+                        out.append(("gate_up", M, lambda th=th, xv=xv, yv=yv: aq.aq_linear_multi(
+                            [th["gate_proj"], th["up_proj"]], xv["mlp"], ys=[yv["gate_proj"], yv["up_proj"]],
+                            workspace=self.ws)))
+                    continue
                 if only in (None, f):
                     out.append((f, M, lambda th=th, f=f, key=key, xv=xv, yv=yv: aq.aq_linear(
                         th[f], xv[key], y=yv[f], workspace=self.ws)))
         return out
 
-    def capture(self, only=None, M=None):
+    def capture(self, only=None, M=None, fuse_gateup=False):
         import torch
         import rank_weight_reconstruction_gb300 as aq
-        calls = [c for c in self.calls(only) if M is None or c[1] == M]
+        calls = [c for c in self.calls(only, fuse_gateup) if M is None or c[1] == M]
         for _, _, fn in calls:          # eager warm-up: device set-up happens outside capture
             fn()
         torch.cuda.synchronize()
@@ -486,6 +497,16 @@ def extras(result, args, dist, stack, device, pk):
     import torch
     import rank_weight_reconstruction_gb300 as aq
     from rank_weight_reconstruction_gb300 import Theta
+
+    # ---- the same step with gate and up of each layer in one aq_linear_multi call ----
+    gf, lf, _ = stack.capture(fuse_gateup=True)
+    t = time_graph(gf, max(3, args.steps))
+    result["decode_gateup_fused"] = {"GB_s": round(step_bytes() / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4),
+                                     "launches_per_step": lf,
+                                     "note": "same step and bytes, gate and up of a layer batched (Q/K/V and gate-up "
+                                             "fusion of the pages' production path)"}
+    del gf
+    torch.cuda.empty_cache()
 
     # ---- as served at G = 1: one shared W0 per family (L2-resident) ----
     shared = DecodeStack(device, copies=False, seed_tag="bench")

@@ -97,8 +97,8 @@ typedef struct aq_theta {
  * (aq_device_status() == AQ_ERR_TIMEOUT) the sync part must be zeroed again. */
 #define AQ_WORKSPACE_SYNC_BYTES (128u * 1024u)
 
-/* Bytes of device workspace aq_linear (n_theta == 1) or aq_linear_qkv (n_theta == 3,
- * pass the three bundles) needs for M tokens, on either path. Returns 0 if none is
+/* Bytes of device workspace aq_linear (n_theta == 1), aq_linear_qkv (n_theta == 3, pass
+ * the three bundles) or aq_linear_multi (n_theta == n) needs for M tokens, on either path. Returns 0 if none is
  * needed (M == 0, or M above the decode limit with r == 0) and (size_t)-1 for invalid
  * arguments. */
 size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
@@ -131,6 +131,17 @@ aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
 aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t ldx,
                         void* const y[3], const int64_t ldy[3],
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Up to AQ_MAX_FAMILIES projections over the same x in one pass: aq_linear_qkv for any
+ * n in [1, AQ_MAX_FAMILIES] -- gate and up of an MLP (n = 2) are the other pair the pages
+ * batch ("Execution paths", "Precompute-outside: the production path": Q/K/V and gate-up
+ * fusion). th[0..n-1] share `in`; y[j] is [M, th[j].out] with row stride ldy[j]; outputs
+ * must not overlap each other or any input. workspace: aq_linear_workspace_bytes(th, n, M).
+ * n outside [1, AQ_MAX_FAMILIES] returns AQ_ERR_INVALID_ARG. */
+#define AQ_MAX_FAMILIES 3
+aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t M, int64_t ldx,
+                          void* const* y, const int64_t* ldy, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* aq_linear for callers that may not allocate device memory. The paper has no
  * counterpart: this entry point exists for callers such as plugins inside a runtime that

@@ -6,6 +6,7 @@ binding, the banded-stack bookkeeping and the seeded input generator.
 """
 from .binding import (  # noqa: F401
     AQ_ERR_TIMEOUT,
+    AQ_MAX_FAMILIES,
     AQ_MAX_RANK,
     AQ_OK,
     AQ_PATH_AUTO,
@@ -18,6 +19,7 @@ from .binding import (  # noqa: F401
     aq_last_launch_count,
     aq_last_path,
     aq_linear,
+    aq_linear_multi,
     aq_linear_qkv,
     aq_linear_workspace_bytes,
     aq_precompute,

@@ -32,8 +32,9 @@ EXPORTED_SYMBOLS = [
     "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
     "aq_device_status", "aq_selftest_bounded_wait", "aq_set_path", "aq_decode_max_m",
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
-    "aq_abi_version", "aq_linear_noalloc",
+    "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi",
 ]
+AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
 AQ_WORKSPACE_SYNC_BYTES = 128 * 1024
 
@@ -80,6 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_linear.restype = ctypes.c_int
     lib.aq_linear_qkv.argtypes = [th_p, vp, i64, i64, ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
     lib.aq_linear_qkv.restype = ctypes.c_int
+    lib.aq_linear_multi.argtypes = [th_p, i32, vp, i64, i64, ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
+    lib.aq_linear_multi.restype = ctypes.c_int
     lib.aq_linear_noalloc.argtypes = [th_p, vp, i64, i64, vp, i64, vp]
     lib.aq_linear_noalloc.restype = ctypes.c_int
     lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
@@ -243,6 +246,25 @@ def aq_linear_qkv(thetas, x, ys=None, workspace=None, stream=None):
     _check(load().aq_linear_qkv(arr, _ptr(x), M, _ld(x), yp, ldy, _ptr(workspace),
                                 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                 _stream(stream)))
+    return ys
+
+
+def aq_linear_multi(thetas, x, ys=None, workspace=None, stream=None):
+    """1..3 projections sharing one x (e.g. gate and up) in one pass; returns the outputs."""
+    thetas = list(thetas)
+    n = len(thetas)
+    M = int(x.size(0))
+    if ys is None:
+        ys = [_padded_empty(M, t.out, x.device) for t in thetas]
+    nbytes = aq_linear_workspace_bytes(thetas, M)
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    arr = (c_theta * max(1, n))(*[t.c() for t in thetas])
+    yp = (ctypes.c_void_p * max(1, n))(*[_ptr(y) for y in ys])
+    ldy = (ctypes.c_int64 * max(1, n))(*[_ld(y) for y in ys])
+    _check(load().aq_linear_multi(arr, n, _ptr(x), M, _ld(x), yp, ldy, _ptr(workspace),
+                                  0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
     return ys
 
 

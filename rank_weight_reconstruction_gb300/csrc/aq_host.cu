@@ -718,7 +718,7 @@ int aq::set_last_error(int status, const char* message) {
 extern "C" {
 
 size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M) {
-  if (!th || (n_theta != 1 && n_theta != 3) || M < 0) return static_cast<size_t>(-1);
+  if (!th || n_theta < 1 || n_theta > AQ_MAX_FAMILIES || M < 0) return static_cast<size_t>(-1);
   const aq_theta* ptrs[kMaxSeg];
   for (int j = 0; j < n_theta; ++j) {
     if (th[j].r < 0 || th[j].r > AQ_MAX_RANK || th[j].in < 1) return static_cast<size_t>(-1);
@@ -741,6 +741,16 @@ aq_status aq_linear_qkv(const aq_theta th[3], const void* x, int64_t M, int64_t 
   if (!th || !y || !ldy) return fail(AQ_ERR_INVALID_ARG, "aq_linear_qkv: NULL array argument");
   const aq_theta* ptrs[3] = {&th[0], &th[1], &th[2]};
   return linear_impl(ptrs, 3, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
+}
+
+aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t M, int64_t ldx, void* const* y,
+                          const int64_t* ldy, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!th || !y || !ldy) return fail(AQ_ERR_INVALID_ARG, "aq_linear_multi: NULL array argument");
+  if (n < 1 || n > AQ_MAX_FAMILIES)
+    return fail(AQ_ERR_INVALID_ARG, "aq_linear_multi: n=%d outside [1, %d]", n, AQ_MAX_FAMILIES);
+  const aq_theta* ptrs[AQ_MAX_FAMILIES] = {};
+  for (int j = 0; j < n; ++j) ptrs[j] = &th[j];
+  return linear_impl(ptrs, n, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
 }
 
 aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream) {

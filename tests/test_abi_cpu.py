@@ -129,6 +129,26 @@ def test_qkv_validation(lib):
     assert lib.aq_linear_qkv(th_in, 0x100000, 4, 40, ys, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_SHAPE
 
 
+def test_multi_validation(lib):
+    th = (binding.c_theta * 3)(_theta(out=16, r=4, W0=0x10000), _theta(out=8, r=4, W0=0x20000),
+                               _theta(out=8, r=4, W0=0x30000))
+    ys = (ctypes.c_void_p * 3)(0x200000, 0x200000 + 32, 0x200000 + 48)
+    ld = (ctypes.c_int64 * 3)(32, 32, 32)
+    for n in (0, 4, -1):
+        assert lib.aq_linear_multi(th, n, 0x100000, 4, 32, ys, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_INVALID_ARG
+    assert "n=" in binding.aq_last_error()
+    assert lib.aq_linear_multi(None, 2, 0x100000, 4, 32, ys, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_INVALID_ARG
+    # two families whose outputs overlap are refused like aq_linear_qkv's
+    ys_bad = (ctypes.c_void_p * 3)(0x200000, 0x200000 + 16, 0)
+    assert lib.aq_linear_multi(th, 2, 0x100000, 4, 32, ys_bad, ld, 0x300000, 1 << 20, None) == binding.AQ_ERR_OVERLAP
+    # n == 2 needs the workspace of the two bundles together; n outside [1, 3] is invalid
+    invalid = ctypes.c_size_t(-1).value
+    two, one = lib.aq_linear_workspace_bytes(th, 2, 100), lib.aq_linear_workspace_bytes(th, 1, 100)
+    assert invalid not in (two, one) and two > one
+    assert lib.aq_linear_workspace_bytes(th, 4, 100) == invalid
+    assert lib.aq_linear_workspace_bytes(th, 0, 100) == invalid
+
+
 def test_precompute_validation(lib):
     th = _theta()
     assert lib.aq_precompute(ctypes.byref(th), 0, 32, None) == binding.AQ_ERR_INVALID_ARG

@@ -251,6 +251,24 @@ def test_qkv_mixed_ranks():
             assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xb, 256)))
 
 
+@pytest.mark.parametrize("M", [1, 4, 16, 512])
+def test_gate_up_batched(M):
+    """gate and up of one layer over the same x in one aq_linear_multi call (n = 2), and
+    n = 1 bit-identical to aq_linear."""
+    thetas, xs = _gemma_layer(4, 16, M)
+    pair = [thetas["gate_proj"], thetas["up_proj"]]
+    x = dev(xs[1152])[:, :1152]
+    ys = aq.aq_linear_multi([dev_theta(t) for t in pair], x)
+    torch.cuda.synchronize()
+    xf = x_f64(xs[1152], 1152)
+    for t, y in zip(pair, ys):
+        assert_close(host_f64(y), oracle.linear(*t.f64(), xf))
+    one = aq.aq_linear_multi([dev_theta(pair[0])], x)[0]
+    ref = aq.aq_linear(dev_theta(pair[0]), x)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(one), bits(ref))
+
+
 # ----------------------------------------------------------------------------------
 # Gemma-3-1B shapes at prefill (r = 64, rows of x scaled by U(0.5, 2))
 # ----------------------------------------------------------------------------------
