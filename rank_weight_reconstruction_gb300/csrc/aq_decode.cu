@@ -56,12 +56,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Every lane waits; the outcome is made warp-uniform because ldmatrix and mma.sync that
 // follow are warp-collective.
 __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, const AbortCtl& ctl) {
@@ -163,9 +157,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       if (local_t) tma_prefetch_desc(&sg.tm_v);
     }
   }
-  // The next kernel in the stream may now be scheduled and start its own weight
-  // prefetch; it touches activations and workspace only after this grid completes.
-  pdl_launch_dependents();
+  // Release of the next kernel in the stream (griddepcontrol.launch_dependents; the first
+  // thread of a CTA that issues it releases the whole CTA). Its CTAs then start their own
+  // weight prefetch, which competes with this call's activation reads. Where those reads are
+  // few and the rest of the call runs from shared memory (x resident, t computed locally),
+  // the next call's weights are better on their way early: release now. Where x rides with
+  // every W0 stage, or t comes from the t CTAs' reads of x, release only once this CTA's
+  // activations have arrived (late_release).
+  if (!p.late_release) pdl_launch_dependents();
   __syncthreads();
 
   if (warp == 0) {
@@ -308,6 +307,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       }
       pdl_wait_prior_grid();
       if (n > 0) ok = mbar_wait(&full[0], 0u, ctl);
+      if (p.late_release) pdl_launch_dependents();
       // thread -> (family, 4 tokens x 4 columns) block, and a residue class of rows
       const int mb = (p.M + 3) / 4;
       int blocks = 0;
@@ -468,6 +468,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
           }
         }
         ok = cons_sync(cbar, cph, ctl);
+        if (p.late_release) pdl_launch_dependents();
       }
       float* red = reinterpret_cast<float*>(epi);          // [nslab * kg][16][kTok]
       // t of this CTA's family as a bf16 pair, t = t_hi + t_lo to about 16 significant
@@ -573,6 +574,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
             ok = false;
             break;
           }
+          if (p.late_release && !p.x_res && ch == 0 && sq == 0) pdl_launch_dependents();
           const int st = (sq + rot) % nstage;
           const int nb = min(p.kbox, p.nkb - st * p.kbox);
           if (active) {

@@ -50,6 +50,7 @@ struct DevInfo {
   bool ready = false;
   int sms = 0;
   size_t smem_optin = 0;
+  int gemm_pairs = 0;   // CTA pairs of the prefill GEMM that fit at once (0: no pairs)
   int32_t* status = nullptr;
 };
 
@@ -77,6 +78,11 @@ aq_status device_info(DevInfo** out) {
       return cuda_fail(e, "cudaFuncSetAttribute");
     int32_t* st = device_status_ptr(dev, &e);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    int pairs = 0;
+    if (static_cast<size_t>(smem) < kGemmPairMinSmem || gemm_max_clusters(kGemmPairMinSmem, 2, &pairs) != cudaSuccess)
+      pairs = 0;
+    cudaGetLastError();   // a failed occupancy query only disables the pairs
+    d.gemm_pairs = pairs;
     d.sms = sms;
     d.smem_optin = static_cast<size_t>(smem);
     d.status = st;
@@ -432,6 +438,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
                     ? static_cast<int32_t>(std::max<int64_t>(
                           1, std::min<int64_t>({kDecMaxTCtas, ceil_div(v_bytes, 32 * 1024), ceil_div(K, 8)})))
                     : 0;
+    // x streamed with every stage, or read by the t CTAs: the next call's weight prefetch
+    // would delay those reads, so it is released after them (measured: down projections and
+    // the 31B-class call at M = 32 gain 0.4-14 us; calls running from resident x and local t
+    // lose up to 1.6 us and keep the early release)
+    dp.late_release = (!dp.x_res || dp.t_ctas > 0) ? 1 : 0;
     int64_t rows_total = 0;
     for (int j = 0; j < n; ++j) rows_total += th[j]->out;
     // streaming CTAs: one per remaining SM, at least 8 rows each, shared among the families
@@ -613,8 +624,30 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   }
 
   uint16_t* tbuf = reinterpret_cast<uint16_t*>(wsb + kSyncBytes);
-  // ---- t = x V for every family with r > 0: V^T into the workspace, then a tcgen05 GEMM ----
+  // ---- plan of the prefill GEMM with the fused reconstruction epilogue ----
+  GemmParams gp = {};
+  gp.M = static_cast<int32_t>(M);
+  gp.K = K;
+  gp.tok_tile = kMmaM;
+  gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+  gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
+  gp.n_mma = gp.row_tile;
+  gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
+  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
+  const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+  // CTA pairs on adjacent token tiles share the row operand (each loads half, multicast to
+  // both): a third less L2 -> SM traffic per MMA, which bounds this GEMM. Pairs need two
+  // token tiles and one CTA per SM; each half is a whole number of 8-row swizzle atoms.
+  gp.cluster = (gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && smem >= kGemmPairMinSmem && gp.row_tile % 16 == 0) ? 2 : 1;
+  gp.n_tok_units = static_cast<int32_t>(ceil_div(gp.n_tok_tiles, gp.cluster));
+  const int box_rows = gp.row_tile / gp.cluster;
+  // t = x V as the first tiles of the same launch, when the sync region holds a flag per
+  // token tile; otherwise as a GEMM launch of its own before it
+  const int64_t n_flags = static_cast<int64_t>(gp.n_tok_units) * gp.cluster;
+  const bool fused_t = wl.any_r && 1 + n_flags <= static_cast<int64_t>(kSyncBytes / 4);
+
   if (wl.any_r) {
+    // V^T into the workspace: the t tiles read it K-major
     TransposeParams tp = {};
     tp.K = K;
     int max_r = 0;
@@ -629,20 +662,22 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       max_r = std::max(max_r, th[j]->r);
     }
     if ((st = launch_or_fail(launch_transpose(tp, max_r, cs, true), "launch V transpose")) != AQ_OK) return st;
-    GemmParams gp = {};
-    gp.M = static_cast<int32_t>(M);
-    gp.K = K;
-    gp.tok_tile = kMmaM;
-    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+  }
+  if (wl.any_r && !fused_t) {
+    GemmParams tg = {};
+    tg.M = static_cast<int32_t>(M);
+    tg.K = K;
+    tg.tok_tile = kMmaM;
+    tg.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
     int rt = 16;
     for (int j = 0; j < n; ++j) rt = std::max<int>(rt, static_cast<int>(round_up(th[j]->r, 16)));
-    gp.row_tile = rt;
-    gp.n_mma = rt;
-    if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, kMmaM, "x")) != AQ_OK) return st;
+    tg.row_tile = rt;
+    tg.n_mma = rt;
+    if ((st = tmap_2d(&tg.tm_x, x, K, M, ldx, kMmaM, "x")) != AQ_OK) return st;
     int tiles = 0;
     for (int j = 0; j < n; ++j) {
       if (th[j]->r == 0) continue;
-      GemmSeg& s = gp.seg[gp.nseg++];
+      GemmSeg& s = tg.seg[tg.nseg++];
       if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, rt, "V^T")) != AQ_OK) return st;
       s.s = nullptr;
       s.y = tbuf + wl.t_col[j];
@@ -651,35 +686,51 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       s.r = 0;
       s.n_row_tiles = 1;
       s.tile_begin = tiles;
-      tiles += gp.n_tok_tiles;
+      s.n_mma = rt;
+      tiles += tg.n_tok_tiles;
     }
-    gp.total_tiles = tiles;
-    gp.prefetch_w = 0;  // V^T comes from the transpose kernel just before
-    gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
-    gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);
-    gp.status = dev->status;
-    gp.timeout_ns = kTimeoutNs;
-    const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
-    const int grid = std::min(tiles, dev->sms);
-    if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch t GEMM")) != AQ_OK) return st;
+    tg.cluster = 1;
+    tg.n_tok_units = tg.n_tok_tiles;
+    tg.total_tiles = tiles;
+    tg.prefetch_w = 0;  // V^T comes from the transpose kernel just before
+    tg.stage_bytes = static_cast<uint32_t>(round_up(kStageA + tg.n_mma * 128, 1024));
+    tg.stages = stages_for(tg.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
+    tg.tmem_cols = tmem_cols_for(2 * tg.n_mma);
+    tg.status = dev->status;
+    tg.timeout_ns = kTimeoutNs;
+    const size_t tsmem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(tg.stages) * tg.stage_bytes;
+    const int tgrid = std::min(tiles, dev->sms);
+    if ((st = launch_or_fail(launch_gemm(tg, tgrid, tsmem, cs, true), "launch t GEMM")) != AQ_OK) return st;
   }
 
-  // ---- prefill GEMM with the fused reconstruction epilogue ----
-  GemmParams gp = {};
-  gp.M = static_cast<int32_t>(M);
-  gp.K = K;
-  gp.tok_tile = kMmaM;
-  gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
-  gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
-  gp.n_mma = gp.row_tile;
   if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, gp.tok_tile, "x")) != AQ_OK) return st;
   int tiles = 0;
+  if (fused_t) {
+    // t segments first: t [M, r_j] = x V_j, row operand V_j^T, no scale, no rank-r part
+    for (int j = 0; j < n; ++j) {
+      if (th[j]->r == 0) continue;
+      GemmSeg& s = gp.seg[gp.nseg++];
+      if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, box_rows, "V^T")) != AQ_OK) return st;
+      s.s = nullptr;
+      s.y = tbuf + wl.t_col[j];
+      s.ldy = wl.ld_t;
+      s.rows = th[j]->r;
+      s.r = 0;
+      s.t_seg = 1;
+      s.n_row_tiles = static_cast<int32_t>(ceil_div(th[j]->r, gp.row_tile));
+      s.n_mma = static_cast<int32_t>(std::min<int64_t>(round_up(th[j]->r, 16), gp.row_tile));
+      s.tile_begin = tiles;
+      tiles += s.n_row_tiles * gp.n_tok_units;
+      gp.t_need += s.n_row_tiles;
+    }
+    gp.t_flags = reinterpret_cast<int32_t*>(wsb);
+    gp.n_flags = static_cast<int32_t>(n_flags);
+  }
   for (int j = 0; j < n; ++j) {
     GemmSeg& s = gp.seg[gp.nseg++];
-    if ((st = tmap_2d(&s.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, gp.row_tile, "W0")) != AQ_OK) return st;
+    if ((st = tmap_2d(&s.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, box_rows, "W0")) != AQ_OK) return st;
     if (th[j]->r > 0) {
-      if ((st = tmap_2d(&s.tm_u, th[j]->U, th[j]->r, th[j]->out, th[j]->ld_u, gp.row_tile, "U")) != AQ_OK) return st;
+      if ((st = tmap_2d(&s.tm_u, th[j]->U, th[j]->r, th[j]->out, th[j]->ld_u, box_rows, "U")) != AQ_OK) return st;
       if ((st = tmap_2d(&s.tm_t, tbuf + wl.t_col[j], th[j]->r, M, wl.ld_t, gp.tok_tile, "t")) != AQ_OK) return st;
     }
     s.s = static_cast<const uint16_t*>(th[j]->s);
@@ -688,18 +739,16 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     s.rows = th[j]->out;
     s.r = th[j]->r;
     s.n_row_tiles = static_cast<int32_t>(ceil_div(th[j]->out, gp.row_tile));
+    s.n_mma = gp.n_mma;
     s.tile_begin = tiles;
-    tiles += s.n_row_tiles * gp.n_tok_tiles;
+    tiles += s.n_row_tiles * gp.n_tok_units;
   }
   gp.total_tiles = tiles;
   gp.prefetch_w = 1;
-  gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
   gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);   // two accumulator buffers
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;
-  const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
-  const int grid = std::min(tiles, dev->sms);
+  const int grid = gp.cluster > 1 ? 2 * std::min(tiles, dev->gemm_pairs) : std::min(tiles, dev->sms);
   if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK) return st;
   t_last_path = AQ_PATH_PREFILL;
   return AQ_OK;

@@ -31,29 +31,43 @@ struct GemmSeg {
   int32_t r;         // rank (0: no low-rank blocks)
   int32_t n_row_tiles;
   int32_t tile_begin;  // first global tile index of this segment
+  int32_t n_mma;     // MMA N of this segment's tiles (<= GemmParams::n_mma)
+  int32_t t_seg;     // 1: computes t = x V (row operand V^T from the workspace, written by the
+                     //    previous kernel); its tiles publish per-token-tile flags
 };
+
+// Segments of one prefill GEMM launch: the families, and before them their t = x V parts.
+constexpr int kMaxGemmSeg = 2 * kMaxSeg;
 
 // Tile mapping: the accumulator is D[token, col] = sum_k x[token, k] * W[col, k], with 128
 // tokens per tile as the accumulator lanes and `row_tile` rows of the row operand as N.
 struct GemmParams {
   CUtensorMap tm_x;  // tokens operand x [M, K]
-  GemmSeg seg[kMaxSeg];
+  GemmSeg seg[kMaxGemmSeg];
   int32_t nseg;
   int32_t M;
   int32_t K;
   int32_t row_tile;     // rows of the row operand per tile (box rows of tm_w / tm_u)
   int32_t tok_tile;     // tokens per tile (box rows of tm_x / tm_t)
   int32_t n_tok_tiles;
-  int32_t total_tiles;
+  int32_t cluster;      // 1, or 2: CTA pairs take adjacent token tiles of one row tile and
+                        //    each loads half of the row operand for both (TMA multicast)
+  int32_t n_tok_units;  // ceil(n_tok_tiles / cluster): token tiles per row tile, in pairs
+  int32_t total_tiles;  // work units: row tiles x n_tok_units, summed over the segments
   int32_t n_mma;        // MMA N: round_up(row_tile, 16)
   int32_t stages;
   int32_t prefetch_w;   // 1: the row operand is a weight and may be loaded before the
                         //    previous grid completes; 0: it is produced by that grid
   uint32_t stage_bytes; // kStageA + n_mma * 128, rounded to 1024
   uint32_t tmem_cols;   // power of two >= 2 * n_mma: two accumulator buffers
+  int32_t* t_flags;     // t segments present: [0] CTAs finished, [1 + i] t tiles done for
+                        // token tile i (workspace sync region; zero before, zero after)
+  int32_t t_need;       // t tiles per token tile (summed over the t segments)
+  int32_t n_flags;      // token tiles with a flag: n_tok_units * cluster
   int32_t* status;      // device status word
   uint64_t timeout_ns;
 };
+static_assert(sizeof(GemmParams) <= 4096, "kernel parameters are limited to 4 KB");
 
 // Decode (M <= kDecMaxTok tokens): each W0-streaming CTA owns a contiguous range of
 // output rows of one family over the full K; a few extra CTAs compute t = V^T x.
@@ -107,6 +121,7 @@ struct DecodeParams {
   int32_t kbox;        // k blocks per pipeline stage
   int32_t w3d;         // 1: W0 / x stages are single 3-D boxes (K is a multiple of 64)
   int32_t x_res;       // 1: x resident in shared memory for the whole call
+  int32_t late_release; // 1: release the next kernel only once this CTA's activations arrived
   int32_t l2_prefetch; // 1: before the dependency wait, pull the W0 stages that do not fit the
                        // ring into L2 (calls whose W0 fits comfortably in L2)
   int32_t xs_ld;       // row stride (elements) of resident x: round_up(K, 64) + 8
@@ -176,6 +191,11 @@ struct PrecomputeParams {
 
 // Launch helpers implemented in aq_kernels.cu; each returns the CUDA error of the launch.
 cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
+// Most clusters of `cluster` aq_gemm_kernel CTAs with `smem` bytes each that fit at once.
+cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n);
+// Shared memory from which one aq_gemm_kernel CTA fills an SM (CTA pairs need that: the pair
+// count is taken at this size).
+constexpr size_t kGemmPairMinSmem = 120 * 1024;
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);

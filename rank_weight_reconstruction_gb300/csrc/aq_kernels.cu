@@ -7,8 +7,10 @@
 //                        output rows as N, two accumulator buffers so a tile's epilogue
 //                        overlaps the next tile's MMAs; the epilogue scales the W0 x sum by
 //                        s in TMEM, the rank-r up-projection is then added as extra K blocks
-//                        into the same accumulator, and y is rounded once. Also the t = x V
-//                        GEMM.
+//                        into the same accumulator, and y is rounded once. t = x V runs as
+//                        the first tiles of the same launch (or, for very large M, as a
+//                        launch of its own). CTA pairs share the W0 / U tiles by TMA
+//                        multicast.
 // aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
 // aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
 //                        epilogue, W_eff written back with TMA stores.
@@ -56,16 +58,18 @@ struct TileCoord {
   int tok0;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
+// Work unit -> tile of this CTA: a unit is one row tile and `cluster` adjacent token tiles,
+// one per CTA of the cluster (rank crank), token tiles fastest.
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, int crank) {
   int si = 0;
 #pragma unroll
-  for (int j = 1; j < kMaxSeg; ++j)
-    if (j < p.nseg && tile >= p.seg[j].tile_begin) si = j;
-  const int local = tile - p.seg[si].tile_begin;
+  for (int j = 1; j < kMaxGemmSeg; ++j)
+    if (j < p.nseg && unit >= p.seg[j].tile_begin) si = j;
+  const int local = unit - p.seg[si].tile_begin;
   TileCoord c;
   c.seg = si;
-  c.tok0 = (local % p.n_tok_tiles) * p.tok_tile;
-  c.row0 = (local / p.n_tok_tiles) * p.row_tile;
+  c.tok0 = ((local % p.n_tok_units) * p.cluster + crank) * p.tok_tile;
+  c.row0 = (local / p.n_tok_units) * p.row_tile;
   return c;
 }
 
@@ -75,6 +79,18 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
 // after the next tile's W0 loop. Work items therefore reach the pipeline in the order
 //   main(0), main(1), low(0), main(2), low(1), ..., low(last)
 // which the producer and the MMA warp both walk with the same loop.
+//
+// t = x V can run in the same launch: its segments come first in the unit order, so every
+// cluster finishes its t tiles before any tile of its own that needs t. A t tile writes its
+// rows of t (bf16, workspace) and bumps the flag of its token tile; the producer waits for
+// the flag of a tile's token tile (bounded) before it loads t for the rank-r blocks. The
+// last CTA to finish zeroes the flags again.
+//
+// With cluster = 2 the two CTAs of a cluster work in lockstep on adjacent token tiles of the
+// same row tile: each loads its own token operand and half of the row operand (W0 or U rows),
+// multicast to both, so the row operand crosses from L2 once per pair. A stage is free again
+// only when both CTAs' MMAs have read it: each MMA warp's commit arrives on the `empty`
+// barrier of both CTAs (initialised with count 2).
 __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -88,17 +104,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   uint64_t* mma_done = epi_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* last_cta = abort_flag + 1;
   float* sbuf = reinterpret_cast<float*>(smem + kHeaderBytes);   // s of the current tile, fp32
   uint8_t* ring = smem + kHeaderBytes + kGemmSBufBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
+  const int cl = p.cluster;
+  const int crank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const uint16_t cl_mask = static_cast<uint16_t>((1u << cl) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(cl));
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -130,12 +150,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers are initialised before anything is multicast to them
+  if (cl > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nkb_main = ceil_div_i(p.K, kBK);
   const uint32_t tx_bytes = static_cast<uint32_t>(p.row_tile + p.tok_tile) * 128u;
-  const int n_it = blockIdx.x < p.total_tiles ? (p.total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  auto tile_of = [&](int it) { return blockIdx.x + it * gridDim.x; };
+  const int cid = static_cast<int>(blockIdx.x) / cl;
+  const int ncl = static_cast<int>(gridDim.x) / cl;
+  const int n_it = cid < p.total_tiles ? (p.total_tiles - 1 - cid) / ncl + 1 : 0;
+  auto tile_of = [&](int it) { return cid + it * ncl; };
+  const int half_rows = p.row_tile / cl;   // rows of the row operand this CTA loads
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -145,6 +170,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       uint32_t phase = 0;
       uint32_t filled = 0, fill_par = 0;
       bool ok = true;
+      // this CTA's part of the row operand of a stage: all of it, or its half for both CTAs
+      auto load_rows = [&](uint8_t* st, const CUtensorMap* m, int kb, int row0, uint64_t* bar) {
+        if (cl == 1) {
+          tma_load_2d(st + kStageA, m, kb * kBK, row0, bar, pol);
+        } else {
+          tma_load_2d_multicast(st + kStageA + static_cast<size_t>(crank) * half_rows * 128, m, kb * kBK,
+                                row0 + crank * half_rows, bar, cl_mask, pol);
+        }
+      };
       // one k block of work item (tile, low) into the next stage
       auto push = [&](const TileCoord& tc, const GemmSeg& sg, bool low, int kb) -> bool {
         if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) return false;
@@ -152,7 +186,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         mbar_arrive_expect_tx(&full[stage], tx_bytes);
         // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
         tma_load_2d(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage], pol);
-        tma_load_2d(st + kStageA, low ? &sg.tm_u : &sg.tm_w, kb * kBK, tc.row0, &full[stage], pol);
+        load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, &full[stage]);
         filled |= 1u << stage;
         fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
         if (++stage == p.stages) {
@@ -161,19 +195,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         }
         return true;
       };
-      if (!p.prefetch_w || n_it == 0) pdl_wait_prior_grid();
+      // the row operand of the first tile may be loaded before the previous grid completes
+      // only when it is a weight (V^T of a t tile is written by the previous kernel)
+      const bool pre_w = p.prefetch_w && n_it > 0 && !p.seg[tile_coord(p, tile_of(0), crank).seg].t_seg;
+      if (!pre_w) pdl_wait_prior_grid();
       for (int it = 0; ok && it <= n_it; ++it) {
         if (it < n_it) {
-          const TileCoord tc = tile_coord(p, tile_of(it));
+          const TileCoord tc = tile_coord(p, tile_of(it), crank);
           const GemmSeg& sg = p.seg[tc.seg];
           int kb = 0;
-          if (it == 0 && p.prefetch_w) {
+          if (it == 0 && pre_w) {
             // Weight tiles of the first stages go out before waiting on the previous grid.
             const int pre = nkb_main < p.stages ? nkb_main : p.stages;
             for (; kb < pre; ++kb) {
               uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
               mbar_arrive_expect_tx(&full[kb], tx_bytes);
-              tma_load_2d(st + kStageA, &sg.tm_w, kb * kBK, tc.row0, &full[kb], pol);
+              load_rows(st, &sg.tm_w, kb, tc.row0, &full[kb]);
               filled |= 1u << kb;
             }
             pdl_wait_prior_grid();
@@ -190,9 +227,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           for (; ok && kb < nkb_main; ++kb) ok = push(tc, sg, false, kb);
         }
         if (ok && it >= 1) {
-          const TileCoord tc = tile_coord(p, tile_of(it - 1));
+          const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
           const GemmSeg& sg = p.seg[tc.seg];
           const int nkb_low = sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0;
+          if (nkb_low > 0 && p.t_flags) {
+            // t of this token tile is written by t tiles of this launch
+            const int32_t* flag = p.t_flags + 1 + tc.tok0 / p.tok_tile;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(flag) < p.t_need) {
+              if (*reinterpret_cast<volatile int*>(abort_flag) || global_timer_ns() - t0 > p.timeout_ns) {
+                *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                atomicExch(p.status, kStatusTimeout);
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+            fence_proxy_async_global();   // the TMA reads of t follow the acquire
+          }
           for (int kb = 0; ok && kb < nkb_low; ++kb) ok = push(tc, sg, true, kb);
         }
       }
@@ -204,12 +256,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = idesc_bf16_f32(kMmaM, p.n_mma);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     // k blocks of one work item into accumulator buffer b; `acc` = 1 adds to what is there
-    auto run = [&](int nkb, int rem_last, uint32_t b, uint32_t acc) -> bool {
+    auto run = [&](int nkb, int rem_last, uint32_t b, uint32_t acc, uint32_t idesc) -> bool {
       const uint32_t d = tmem_base + b * static_cast<uint32_t>(p.n_mma);
       for (int kb = 0; kb < nkb; ++kb) {
         if (!warp_wait(&full[stage], phase, ctl)) return false;
@@ -221,7 +272,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           for (int j = 0; j < nk; ++j)
             tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc,
                         (acc || kb > 0 || j > 0) ? 1u : 0u);
-          tc_commit(&empty[stage]);
+          if (cl == 1) {
+            tc_commit(&empty[stage]);
+          } else {
+            tc_commit_multicast(&empty[stage], cl_mask);
+          }
         }
         __syncwarp();
         if (++stage == p.stages) {
@@ -234,23 +289,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     // Start the bounded waits only once the previous grid is done, so that a long
     // predecessor cannot be mistaken for a stalled pipeline.
     pdl_wait_prior_grid();
+    // acc_scaled / acc_done are used only by tiles with a rank-r part: their phases advance
+    // per use (bit b for buffer b), not per tile
+    uint32_t lr_phase = 0;
     for (int it = 0; ok && it <= n_it; ++it) {
       if (it < n_it) {
         const uint32_t b = it & 1;
         if (!warp_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, ctl)) break;
         tc_fence_after();
-        ok = run(nkb_main, 0, b, 0u);
+        const TileCoord tc = tile_coord(p, tile_of(it), crank);
+        ok = run(nkb_main, 0, b, 0u, idesc_bf16_f32(kMmaM, p.seg[tc.seg].n_mma));
         if (ok && lane == 0) tc_commit(&acc_full[b]);
         __syncwarp();
       }
       if (ok && it >= 1) {
-        const TileCoord tc = tile_coord(p, tile_of(it - 1));
+        const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
         const GemmSeg& sg = p.seg[tc.seg];
         if (sg.r > 0) {
           const uint32_t b = (it - 1) & 1;
-          if (!warp_wait(&acc_scaled[b], ((it - 1) >> 1) & 1, ctl)) break;
+          if (!warp_wait(&acc_scaled[b], (lr_phase >> b) & 1u, ctl)) break;
+          lr_phase ^= 1u << b;
           tc_fence_after();
-          ok = run(ceil_div_i(sg.r, kBK), sg.r % kBK, b, 1u);
+          ok = run(ceil_div_i(sg.r, kBK), sg.r % kBK, b, 1u, idesc_bf16_f32(kMmaM, sg.n_mma));
           if (ok && lane == 0) tc_commit(&acc_done[b]);
           __syncwarp();
         }
@@ -274,8 +334,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       return r;
     };
     pdl_wait_prior_grid();
+    uint32_t lr_phase = 0;   // phases of acc_done[b] (bit b), advanced per rank-r use
     for (int it = 0; it < n_it; ++it) {
-      const TileCoord tc = tile_coord(p, tile_of(it));
+      const TileCoord tc = tile_coord(p, tile_of(it), crank);
       const GemmSeg& sg = p.seg[tc.seg];
       const bool has_lr = sg.r > 0;
       const uint32_t b = it & 1;
@@ -293,7 +354,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       tc_fence_after();
       if (has_lr) {
         // scale the W0 x accumulator by s in place; the MMA warp then adds U t
-        for (int c = 0; c < p.n_mma; c += 16) {
+        for (int c = 0; c < sg.n_mma; c += 16) {
           float v[16];
           tmem_ld_16(acc + c, v);
           tmem_ld_wait();
@@ -304,13 +365,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&acc_scaled[b]);
-        if (!warp_wait(&acc_done[b], par, ctl)) break;
+        if (!warp_wait(&acc_done[b], (lr_phase >> b) & 1u, ctl)) break;
+        lr_phase ^= 1u << b;
         tc_fence_after();
       }
       const int tok = tc.tok0 + et;
       const bool tok_ok = tok < p.M;
       uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
-      for (int c = 0; c < p.n_mma; c += 16) {
+      for (int c = 0; c < sg.n_mma; c += 16) {
         float v[16];
         tmem_ld_16(acc + c, v);
         tmem_ld_wait();
@@ -340,6 +402,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
+      if (sg.t_seg) {
+        // publish this token tile's t: every thread's stores, then one release
+        __threadfence();
+        fence_proxy_async_global();
+        if (!epi_sync()) break;
+        if (et == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
+      }
     }
   }
 
@@ -347,6 +416,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+  if (p.t_flags) {
+    // every CTA is past its last flag wait once all have counted themselves here: the last
+    // one returns the flags to zero for the next call
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *last_cta = atomicAdd(p.t_flags, 1) == static_cast<int>(gridDim.x) - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_cta) {
+      for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.t_flags[1 + i] = 0;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        p.t_flags[0] = 0;
+        __threadfence();
+      }
+    }
+  }
+  // neither CTA of a pair exits while the other may still multicast into it or arrive on
+  // its barriers
+  if (cl > 1) cluster_sync_all();
 }
 // ------------------------------------------------------------------------------------
 // V [in, r] -> V^T [r, in]
@@ -685,7 +774,22 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
 cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<GemmParams*>(&p)};
   return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel), dim3(grid), dim3(kGemmThreads), smem, st, pdl,
-                   args);
+                   args, dim3(p.cluster > 1 ? p.cluster : 1, 1, 1));
+}
+
+cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel), &cfg);
 }
 
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl) {

@@ -251,6 +251,23 @@ def test_qkv_mixed_ranks():
             assert_close(host_f64(y), oracle.linear(*t.f64(), x_f64(xb, 256)))
 
 
+@pytest.mark.parametrize("M", [3000, 4096])
+def test_prefill_mixed_ranks_many_tiles(M):
+    """Prefill with families of rank 0, 16 and 40 in one launch, at token counts where every
+    CTA (pair) takes several tiles: tiles without a rank-r part (and the t = x V tiles) run
+    between tiles with one on the same accumulator buffer. 3000 tokens leave an odd number
+    of 128-token tiles."""
+    out_in = [(2048, 1152), (640, 1152), (1024, 1152)]
+    ths = [synth.make_theta(("mix-many", j), o, i, r) for j, ((o, i), r) in enumerate(zip(out_in, (16, 0, 40)))]
+    xb = synth.make_x(("mix-many", M), M, 1152)
+    ys = aq.aq_linear_qkv([dev_theta(t) for t in ths], dev(xb)[:, :1152])
+    torch.cuda.synchronize()
+    assert aq.aq_last_path() == aq.AQ_PATH_PREFILL
+    xf = x_f64(xb, 1152)
+    for t, y in zip(ths, ys):
+        assert_close(host_f64(y), oracle.linear(*t.f64(), xf), f"out={t.out} r={t.r}")
+
+
 @pytest.mark.parametrize("M", [1, 4, 16, 512])
 def test_gate_up_batched(M):
     """gate and up of one layer over the same x in one aq_linear_multi call (n = 2), and
