@@ -632,13 +632,18 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
   gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
   gp.n_mma = gp.row_tile;
-  gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + gp.n_mma * 128, 1024));
-  gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
-  const size_t smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
-  // CTA pairs on adjacent token tiles share the row operand (each loads half, multicast to
-  // both): a third less L2 -> SM traffic per MMA, which bounds this GEMM. Pairs need two
-  // token tiles and one CTA per SM; each half is a whole number of 8-row swizzle atoms.
-  gp.cluster = (gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && smem >= kGemmPairMinSmem && gp.row_tile % 16 == 0) ? 2 : 1;
+  // CTA pairs (2-SM MMAs, M = 256) on adjacent token tiles: each CTA holds half of the N
+  // rows of B, so a stage is 32 KB instead of 48 and shared memory moves a third less per
+  // MMA, which bounds this GEMM. Pairs need two token tiles and one CTA per SM; each half of
+  // B is a whole number of 8-row swizzle atoms.
+  size_t smem = 0;
+  for (int cl = (gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1; cl >= 1; --cl) {
+    gp.cluster = cl;
+    gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + (gp.n_mma / cl) * 128, 1024));
+    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
+    smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+    if (cl == 1 || smem >= kGemmPairMinSmem) break;
+  }
   gp.n_tok_units = static_cast<int32_t>(ceil_div(gp.n_tok_tiles, gp.cluster));
   const int box_rows = gp.row_tile / gp.cluster;
   // t = x V as the first tiles of the same launch, when the sync region holds a flag per
@@ -691,6 +696,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     }
     tg.cluster = 1;
     tg.n_tok_units = tg.n_tok_tiles;
+    tg.head_kb = kGemmHeadKb;
     tg.total_tiles = tiles;
     tg.prefetch_w = 0;  // V^T comes from the transpose kernel just before
     tg.stage_bytes = static_cast<uint32_t>(round_up(kStageA + tg.n_mma * 128, 1024));
@@ -745,6 +751,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   }
   gp.total_tiles = tiles;
   gp.prefetch_w = 1;
+  gp.head_kb = kGemmHeadKb;
   gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);   // two accumulator buffers
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;

@@ -64,6 +64,7 @@ struct GemmParams {
                         // token tile i (workspace sync region; zero before, zero after)
   int32_t t_need;       // t tiles per token tile (summed over the t segments)
   int32_t n_flags;      // token tiles with a flag: n_tok_units * cluster
+  int32_t head_kb;      // k blocks of tile i+1 issued before the rank-r blocks of tile i
   int32_t* status;      // device status word
   uint64_t timeout_ns;
 };
@@ -196,6 +197,9 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n);
 // Shared memory from which one aq_gemm_kernel CTA fills an SM (CTA pairs need that: the pair
 // count is taken at this size).
 constexpr size_t kGemmPairMinSmem = 120 * 1024;
+// k blocks of the next tile the MMA warp issues while the epilogue scales a tile by s (the
+// scale pass takes about as long as five 64-wide k blocks of a 256-wide tile)
+constexpr int kGemmHeadKb = 6;
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);

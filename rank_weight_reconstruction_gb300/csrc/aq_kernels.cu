@@ -76,9 +76,12 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, i
 // Two accumulator buffers of n_mma TMEM columns each, so a tile's epilogue overlaps the next
 // tile's MMAs. The rank-r term needs no buffer of its own: once the W0 K loop of tile i is
 // done, the epilogue scales the accumulator by s in place, and the MMA warp adds U t into it
-// after the next tile's W0 loop. Work items therefore reach the pipeline in the order
-//   main(0), main(1), low(0), main(2), low(1), ..., low(last)
-// which the producer and the MMA warp both walk with the same loop.
+// while the first head_kb k blocks of tile i+1 have covered the scale pass. Work items
+// therefore reach the pipeline in the order
+//   main(0), head(1), low(0), tail(1), head(2), low(1), tail(2), ..., low(last)
+// (head + tail = main), which the producer and the MMA warp both walk with the same loop. The
+// final pass of tile i then overlaps tail(i+1), so tile i+2, which reuses tile i's buffer,
+// rarely waits for it.
 //
 // t = x V can run in the same launch: its segments come first in the unit order, so every
 // cluster finishes its t tiles before any tile of its own that needs t. A t tile writes its
@@ -86,11 +89,15 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, i
 // the flag of a tile's token tile (bounded) before it loads t for the rank-r blocks. The
 // last CTA to finish zeroes the flags again.
 //
-// With cluster = 2 the two CTAs of a cluster work in lockstep on adjacent token tiles of the
-// same row tile: each loads its own token operand and half of the row operand (W0 or U rows),
-// multicast to both, so the row operand crosses from L2 once per pair. A stage is free again
-// only when both CTAs' MMAs have read it: each MMA warp's commit arrives on the `empty`
-// barrier of both CTAs (initialised with count 2).
+// With cluster = 2 the two CTAs of a cluster are one CTA pair of 2-SM MMAs (cta_group::2):
+// each holds the 128-token tile of its own (A) and half of the row operand's N rows (B) per
+// stage, and the even CTA issues M = 256 MMAs that read both CTAs' shared memory and write
+// each CTA's TMEM. Per MMA a CTA's shared memory then moves 8 KB of operands instead of 12,
+// and a stage takes 32 KB instead of 48. Both CTAs' TMA loads count on the even CTA's `full`
+// barrier; its MMA commits arrive on both CTAs' `empty`, `acc_full` and `acc_done`; both
+// CTAs' epilogue warps arrive on its `acc_scaled` and `acc_empty`.
+// kPair: the CTA-pair (cluster = 2) variant; a function may not mix cta_group::1 and ::2.
+template <bool kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -111,20 +118,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
-  const int cl = p.cluster;
-  const int crank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const uint16_t cl_mask = static_cast<uint16_t>((1u << cl) - 1u);
+  constexpr int cl = kPair ? 2 : 1;   // == p.cluster
+  const int crank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = crank == 0;   // issues the MMAs (the only CTA when unpaired)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(cl));
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_scaled[b], 4 * 32);
+      mbar_init(&acc_scaled[b], 4 * cl);   // one arrival per epilogue warp of each CTA
       mbar_init(&acc_done[b], 1);
-      mbar_init(&acc_empty[b], 4 * 32);
+      mbar_init(&acc_empty[b], 4 * cl);
     }
     mbar_init(epi_bar, 4 * 32);
     mbar_init(mma_done, 1);
@@ -142,25 +149,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, p.tmem_cols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, p.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, p.tmem_cols);
+      tmem_relinquish();
+    }
   }
   // The next kernel in the stream may now be scheduled and start its own weight
   // prefetch; it touches activations only after this grid has completed.
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
-  // the peer's barriers are initialised before anything is multicast to them
-  if (cl > 1) cluster_sync_all();
+  // the peer's barriers are initialised before either CTA signals the other's
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nkb_main = ceil_div_i(p.K, kBK);
-  const uint32_t tx_bytes = static_cast<uint32_t>(p.row_tile + p.tok_tile) * 128u;
+  // bytes of one stage over the whole pair: each CTA's token tile and its share of the rows
+  const uint32_t tx_bytes = static_cast<uint32_t>(cl) * static_cast<uint32_t>(p.row_tile / cl + p.tok_tile) * 128u;
   const int cid = static_cast<int>(blockIdx.x) / cl;
   const int ncl = static_cast<int>(gridDim.x) / cl;
   const int n_it = cid < p.total_tiles ? (p.total_tiles - 1 - cid) / ncl + 1 : 0;
   auto tile_of = [&](int it) { return cid + it * ncl; };
-  const int half_rows = p.row_tile / cl;   // rows of the row operand this CTA loads
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -170,23 +182,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       uint32_t phase = 0;
       uint32_t filled = 0, fill_par = 0;
       bool ok = true;
-      // this CTA's part of the row operand of a stage: all of it, or its half for both CTAs
-      auto load_rows = [&](uint8_t* st, const CUtensorMap* m, int kb, int row0, uint64_t* bar) {
-        if (cl == 1) {
-          tma_load_2d(st + kStageA, m, kb * kBK, row0, bar, pol);
+      // one box into this CTA's stage, counted on the even CTA's `full` barrier
+      auto load = [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+        if constexpr (kPair) {
+          tma_load_2d_pair(dst, m, c0, c1, cluster_map(bar, 0), pol);
         } else {
-          tma_load_2d_multicast(st + kStageA + static_cast<size_t>(crank) * half_rows * 128, m, kb * kBK,
-                                row0 + crank * half_rows, bar, cl_mask, pol);
+          tma_load_2d(dst, m, c0, c1, bar, pol);
         }
+      };
+      // B: the whole N rows, or this CTA's half of them (rows n_mma / 2 apart)
+      auto load_rows = [&](uint8_t* st, const CUtensorMap* m, int kb, int row0, int n_mma, uint64_t* bar) {
+        load(st + kStageA, m, kb * kBK, row0 + crank * (n_mma / cl), bar);
       };
       // one k block of work item (tile, low) into the next stage
       auto push = [&](const TileCoord& tc, const GemmSeg& sg, bool low, int kb) -> bool {
         if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) return false;
         uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+        if (leader) mbar_arrive_expect_tx(&full[stage], tx_bytes);
         // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
-        tma_load_2d(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage], pol);
-        load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, &full[stage]);
+        load(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
+        load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, sg.n_mma, &full[stage]);
         filled |= 1u << stage;
         fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
         if (++stage == p.stages) {
@@ -200,6 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       const bool pre_w = p.prefetch_w && n_it > 0 && !p.seg[tile_coord(p, tile_of(0), crank).seg].t_seg;
       if (!pre_w) pdl_wait_prior_grid();
       for (int it = 0; ok && it <= n_it; ++it) {
+        const int h = it == 0 ? nkb_main : min(p.head_kb, nkb_main);   // head k blocks of tile it
         if (it < n_it) {
           const TileCoord tc = tile_coord(p, tile_of(it), crank);
           const GemmSeg& sg = p.seg[tc.seg];
@@ -209,14 +225,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
             const int pre = nkb_main < p.stages ? nkb_main : p.stages;
             for (; kb < pre; ++kb) {
               uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
-              mbar_arrive_expect_tx(&full[kb], tx_bytes);
-              load_rows(st, &sg.tm_w, kb, tc.row0, &full[kb]);
+              if (leader) mbar_arrive_expect_tx(&full[kb], tx_bytes);
+              load_rows(st, &sg.tm_w, kb, tc.row0, sg.n_mma, &full[kb]);
               filled |= 1u << kb;
             }
             pdl_wait_prior_grid();
             for (int j = 0; j < pre; ++j) {
               uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-              tma_load_2d(st, &p.tm_x, j * kBK, tc.tok0, &full[j], pol);
+              load(st, &p.tm_x, j * kBK, tc.tok0, &full[j]);
             }
             stage = pre;
             if (stage == p.stages) {
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
               phase ^= 1;
             }
           }
-          for (; ok && kb < nkb_main; ++kb) ok = push(tc, sg, false, kb);
+          for (; ok && kb < h; ++kb) ok = push(tc, sg, false, kb);
         }
         if (ok && it >= 1) {
           const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
@@ -247,36 +263,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           }
           for (int kb = 0; ok && kb < nkb_low; ++kb) ok = push(tc, sg, true, kb);
         }
+        if (ok && it >= 1 && it < n_it) {
+          const TileCoord tc = tile_coord(p, tile_of(it), crank);
+          const GemmSeg& sg = p.seg[tc.seg];
+          for (int kb = h; ok && kb < nkb_main; ++kb) ok = push(tc, sg, false, kb);
+        }
       }
-      if (!ok) {
-        // Let every copy already issued land before the CTA can exit.
+      if (!ok && leader) {
+        // Let every copy already issued land before the CTA can exit (a pair's copies all
+        // count on the even CTA's barriers; both CTAs stay until the final cluster barrier).
         for (int s = 0; s < p.stages; ++s)
           if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_par >> s) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer (the even CTA of a pair) ----------------
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    // k blocks of one work item into accumulator buffer b; `acc` = 1 adds to what is there
-    auto run = [&](int nkb, int rem_last, uint32_t b, uint32_t acc, uint32_t idesc) -> bool {
+    bool ok = leader;
+    // arrival on `bar` in this CTA and, for a pair, in the peer, once the MMAs so far finish
+    auto commit_all = [&](uint64_t* bar) {
+      if constexpr (kPair) {
+        tc_commit_pair_multicast(bar, 0x3);
+      } else {
+        tc_commit(bar);
+      }
+    };
+    const int mma_m = kMmaM * cl;
+    // k blocks [kb0, kb1) of one work item into accumulator buffer b; `acc` = 1 adds to what
+    // is there; rem_last: valid K of the last block when it is partial (rank-r blocks)
+    auto run = [&](int kb0, int kb1, int rem_last, uint32_t b, uint32_t acc, uint32_t idesc) -> bool {
       const uint32_t d = tmem_base + b * static_cast<uint32_t>(p.n_mma);
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!warp_wait(&full[stage], phase, ctl)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t b_addr = a_addr + kStageA;
-          const int nk = (kb == nkb - 1 && rem_last > 0) ? ceil_div_i(rem_last, kUmmaK) : kBK / kUmmaK;
-          for (int j = 0; j < nk; ++j)
-            tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc,
-                        (acc || kb > 0 || j > 0) ? 1u : 0u);
-          if (cl == 1) {
-            tc_commit(&empty[stage]);
-          } else {
-            tc_commit_multicast(&empty[stage], cl_mask);
+          const int nk = (kb == kb1 - 1 && rem_last > 0) ? ceil_div_i(rem_last, kUmmaK) : kBK / kUmmaK;
+          for (int j = 0; j < nk; ++j) {
+            const uint32_t en = (acc || kb > 0 || j > 0) ? 1u : 0u;
+            if constexpr (kPair) {
+              tc_mma_bf16_pair(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc, en);
+            } else {
+              tc_mma_bf16(d, smem_desc_k128(a_addr + 32u * j), smem_desc_k128(b_addr + 32u * j), idesc, en);
+            }
           }
+          commit_all(&empty[stage]);
         }
         __syncwarp();
         if (++stage == p.stages) {
@@ -292,15 +325,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     // acc_scaled / acc_done are used only by tiles with a rank-r part: their phases advance
     // per use (bit b for buffer b), not per tile
     uint32_t lr_phase = 0;
-    for (int it = 0; ok && it <= n_it; ++it) {
+    for (int it = 0; ok && it <= n_it; ++it) {   // (the odd CTA of a pair issues nothing)
+      const int h = it == 0 ? nkb_main : min(p.head_kb, nkb_main);
       if (it < n_it) {
         const uint32_t b = it & 1;
         if (!warp_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, ctl)) break;
         tc_fence_after();
         const TileCoord tc = tile_coord(p, tile_of(it), crank);
-        ok = run(nkb_main, 0, b, 0u, idesc_bf16_f32(kMmaM, p.seg[tc.seg].n_mma));
-        if (ok && lane == 0) tc_commit(&acc_full[b]);
-        __syncwarp();
+        ok = run(0, h, 0, b, 0u, idesc_bf16_f32(mma_m, p.seg[tc.seg].n_mma));
       }
       if (ok && it >= 1) {
         const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
@@ -310,14 +342,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           if (!warp_wait(&acc_scaled[b], (lr_phase >> b) & 1u, ctl)) break;
           lr_phase ^= 1u << b;
           tc_fence_after();
-          ok = run(ceil_div_i(sg.r, kBK), sg.r % kBK, b, 1u, idesc_bf16_f32(kMmaM, sg.n_mma));
-          if (ok && lane == 0) tc_commit(&acc_done[b]);
+          ok = run(0, ceil_div_i(sg.r, kBK), sg.r % kBK, b, 1u, idesc_bf16_f32(mma_m, sg.n_mma));
+          if (ok && lane == 0) commit_all(&acc_done[b]);
           __syncwarp();
         }
       }
+      if (ok && it < n_it) {
+        const uint32_t b = it & 1;
+        const TileCoord tc = tile_coord(p, tile_of(it), crank);
+        ok = run(h, nkb_main, 0, b, 1u, idesc_bf16_f32(mma_m, p.seg[tc.seg].n_mma));
+        if (ok && lane == 0) commit_all(&acc_full[b]);
+        __syncwarp();
+      }
     }
-    if (lane == 0) {
-      tc_commit(mma_done);
+    if (leader && lane == 0) {
+      if constexpr (kPair) {
+        tc_commit_pair(mma_done);
+      } else {
+        tc_commit(mma_done);
+      }
       mbar_wait_drain(mma_done, 0, kDrainNs);
     }
     __syncwarp();
@@ -326,6 +369,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     const int q = warp & 3;
     const int et = q * 32 + lane;                 // 0..127: TMEM lane = token of the tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // one arrival per warp on the MMA-issuing CTA's barrier
+    auto mbar_arrive_lead = [&](uint64_t* bar) {
+      if constexpr (kPair) {
+        mbar_arrive_cluster(cluster_map(bar, 0));
+      } else {
+        mbar_arrive(bar);
+      }
+    };
     uint32_t ephase = 0;
     auto epi_sync = [&]() {
       mbar_arrive(epi_bar);
@@ -364,7 +415,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&acc_scaled[b]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_lead(&acc_scaled[b]);
         if (!warp_wait(&acc_done[b], (lr_phase >> b) & 1u, ctl)) break;
         lr_phase ^= 1u << b;
         tc_fence_after();
@@ -401,7 +453,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         }
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_lead(&acc_empty[b]);
       if (sg.t_seg) {
         // publish this token tile's t: every thread's stores, then one release
         __threadfence();
@@ -414,8 +467,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
+  // a pair: both CTAs are done with the accumulators and with each other's barriers
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+  if (warp == 1) {
+    if constexpr (kPair) {
+      tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    } else {
+      tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+  }
   if (p.t_flags) {
     // every CTA is past its last flag wait once all have counted themselves here: the last
     // one returns the flags to zero for the next call
@@ -433,9 +494,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       }
     }
   }
-  // neither CTA of a pair exits while the other may still multicast into it or arrive on
-  // its barriers
-  if (cl > 1) cluster_sync_all();
+  if constexpr (kPair) cluster_sync_all();
 }
 // ------------------------------------------------------------------------------------
 // V [in, r] -> V^T [r, in]
@@ -773,8 +832,11 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<GemmParams*>(&p)};
-  return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel), dim3(grid), dim3(kGemmThreads), smem, st, pdl,
-                   args, dim3(p.cluster > 1 ? p.cluster : 1, 1, 1));
+  if (p.cluster > 1)
+    return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<true>), dim3(grid), dim3(kGemmThreads), smem, st,
+                     pdl, args, dim3(2, 1, 1));
+  return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<false>), dim3(grid), dim3(kGemmThreads), smem, st,
+                   pdl, args);
 }
 
 cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
@@ -789,7 +851,7 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel), &cfg);
+  return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel<true>), &cfg);
 }
 
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl) {
@@ -816,7 +878,8 @@ cudaError_t configure_kernels(int device, size_t max_smem) {
   (void)device;
   cudaError_t e;
   const int s = static_cast<int>(max_smem);
-  if ((e = cudaFuncSetAttribute(aq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = configure_decode(max_smem))) return e;
   if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
     return e;
