@@ -640,8 +640,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   for (int cl = (gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1; cl >= 1; --cl) {
     gp.cluster = cl;
     gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + (gp.n_mma / cl) * 128, 1024));
-    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack);
-    smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack + kYStageTotal);
+    smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + kYStageTotal + static_cast<size_t>(gp.stages) * gp.stage_bytes;
     if (cl == 1 || smem >= kGemmPairMinSmem) break;
   }
   gp.n_tok_units = static_cast<int32_t>(ceil_div(gp.n_tok_tiles, gp.cluster));
@@ -746,6 +746,10 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     s.r = th[j]->r;
     s.n_row_tiles = static_cast<int32_t>(ceil_div(th[j]->out, gp.row_tile));
     s.n_mma = gp.n_mma;
+    // bulk tensor stores of y need whole 64-column boxes per tile: a partial box would write
+    // into the next tile's columns (the tensor map clips only at the family's last row)
+    s.tma_y = gp.row_tile % 64 == 0 ? 1 : 0;
+    if (s.tma_y && (st = tmap_2d(&s.tm_y, ys[j], th[j]->out, M, ldys[j], 32, "y")) != AQ_OK) return st;
     s.tile_begin = tiles;
     tiles += s.n_row_tiles * gp.n_tok_units;
   }

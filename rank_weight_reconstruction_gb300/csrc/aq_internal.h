@@ -24,6 +24,7 @@ struct GemmSeg {
   CUtensorMap tm_w;  // "row" operand over the K loop: W0 [rows, K] (or V^T for the t GEMM)
   CUtensorMap tm_u;  // low-rank row operand U [rows, r]
   CUtensorMap tm_t;  // low-rank token operand t [M, r]
+  CUtensorMap tm_y;  // output y for bulk stores: box {64 rows of the row operand, 32 tokens}
   const uint16_t* s; // [rows] bf16 scale, or nullptr for 1
   uint16_t* y;       // output [M, rows] bf16, row stride ldy
   int64_t ldy;
@@ -32,6 +33,7 @@ struct GemmSeg {
   int32_t n_row_tiles;
   int32_t tile_begin;  // first global tile index of this segment
   int32_t n_mma;     // MMA N of this segment's tiles (<= GemmParams::n_mma)
+  int32_t tma_y;     // 1: y leaves through shared memory and bulk tensor stores
   int32_t t_seg;     // 1: computes t = x V (row operand V^T from the workspace, written by the
                      //    previous kernel); its tiles publish per-token-tile flags
 };
@@ -200,6 +202,10 @@ constexpr size_t kGemmPairMinSmem = 120 * 1024;
 // k blocks of the next tile the MMA warp issues while the epilogue scales a tile by s (the
 // scale pass takes about as long as five 64-wide k blocks of a 256-wide tile)
 constexpr int kGemmHeadKb = 6;
+// Output staging of the prefill epilogue: per epilogue warp two buffers of 32 tokens x 64
+// columns of bf16 (128-byte swizzled rows), after the ring
+constexpr int kYStageBytes = 32 * 128;
+constexpr int kYStageTotal = 4 * 2 * kYStageBytes;
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);

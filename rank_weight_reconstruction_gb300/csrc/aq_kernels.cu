@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   int* last_cta = abort_flag + 1;
   float* sbuf = reinterpret_cast<float*>(smem + kHeaderBytes);   // s of the current tile, fp32
   uint8_t* ring = smem + kHeaderBytes + kGemmSBufBytes;
+  uint8_t* ystage = ring + static_cast<size_t>(p.stages) * p.stage_bytes;   // output staging
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -421,6 +422,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         lr_phase ^= 1u << b;
         tc_fence_after();
       }
+      if (sg.tma_y) {
+        // 64-column chunks through this warp's two staging buffers (row = token, 128-byte
+        // swizzle), each written out by one bulk tensor store; the tensor map clips rows
+        // past M and columns past the family's rows
+        uint8_t* wst = ystage + static_cast<size_t>(q) * 2 * kYStageBytes;
+        int nst = 0;
+        for (int c0 = 0; c0 < sg.n_mma; c0 += 64, ++nst) {
+          uint8_t* buf = wst + (nst & 1) * kYStageBytes;
+          if (nst >= 2 && lane == 0) tma_store_wait_read_but_one();   // this buffer's last store read it
+          __syncwarp();
+          uint8_t* row = buf + lane * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int c = c0 + q4 * 16;
+            float v[16];
+            tmem_ld_16(acc + c, v);
+            tmem_ld_wait();
+            if (!has_lr) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
+            }
+            uint4 w0, w1;
+            w0.x = pack_bf16x2(v[0], v[1]);
+            w0.y = pack_bf16x2(v[2], v[3]);
+            w0.z = pack_bf16x2(v[4], v[5]);
+            w0.w = pack_bf16x2(v[6], v[7]);
+            w1.x = pack_bf16x2(v[8], v[9]);
+            w1.y = pack_bf16x2(v[10], v[11]);
+            w1.z = pack_bf16x2(v[12], v[13]);
+            w1.w = pack_bf16x2(v[14], v[15]);
+            *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (lane & 7)) << 4)) = w0;
+            *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (lane & 7)) << 4)) = w1;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&sg.tm_y, buf, tc.row0 + c0, tc.tok0 + q * 32);
+            tma_store_commit();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_lead(&acc_empty[b]);
+        if (lane == 0) tma_store_wait_read_all();   // the staging is free for the next tile
+        __syncwarp();
+        continue;
+      }
       const int tok = tc.tok0 + et;
       const bool tok_ok = tok < p.M;
       uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
@@ -463,6 +511,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         if (et == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
       }
     }
+    if (lane == 0) tma_store_wait_all();   // this warp's bulk stores of y are complete
+    __syncwarp();
   }
 
   tc_fence_before();
