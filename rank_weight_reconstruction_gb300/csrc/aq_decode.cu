@@ -274,23 +274,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     if (t_cta) {
       // ---- t = V^T x over this CTA's slice of `in`: every box of V and x is requested
       // at once (one round trip), V before the dependency wait ----
-      // slices start on a multiple of 8 elements: a TMA box's innermost coordinate must
-      // be 16-byte aligned
-      const int ks = ((p.K + p.t_ctas - 1) / p.t_ctas + 7) & ~7;
+      // slices are whole 16-row k steps of the mma (and so start 16-byte aligned, as a TMA
+      // box's innermost coordinate must)
+      const int ks = ((p.K + p.t_ctas - 1) / p.t_ctas + 15) & ~15;
       const int i0 = cta * ks;
       const int i1 = min(p.K, i0 + ks);
       const int n = max(0, i1 - i0);
       const int nvb = (ks + p.vbox - 1) / p.vbox;
       const int trows = nvb * p.vbox;                                // staged rows of `in`
       const int ntot = p.M * p.r_total;
-      float* tacc = reinterpret_cast<float*>(epi);                 // [M][r_total], fp32
       const int tacc_bytes = (ntot * 4 + 1023) & ~1023;
       uint8_t* stage_area = epi + tacc_bytes;                        // per family [trows][r8]
       const uint16_t* xsb =                                          // per box [M][vbox]
           reinterpret_cast<const uint16_t*>(stage_area + static_cast<size_t>(trows) * p.r8_total * 2);
       // TMA writes shared memory at 128-byte aligned addresses: x boxes are spaced so
       const int xbs = ((p.vbox * p.M * 2 + 127) & ~127) / 2;        // elements per x box
-      for (int idx = ct; idx < ntot; idx += kDecConsumers) tacc[idx] = 0.0f;
       if (ct == 0 && n > 0) {
         mbar_arrive_expect_tx(&full[0], static_cast<uint32_t>(trows) * (p.r8_total + p.M) * 2u);  // box bytes
         int col = 0;
@@ -308,98 +306,88 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
       pdl_wait_prior_grid();
       if (n > 0) ok = mbar_wait(&full[0], 0u, ctl);
       if (p.late_release) pdl_launch_dependents();
-      // thread -> (family, 4 tokens x 4 columns) block, and a residue class of rows
-      const int mb = (p.M + 3) / 4;
-      int blocks = 0;
-      for (int j = 0; j < p.nseg; ++j) blocks += mb * (p.seg[j].r8 / 4);
-      const bool few = blocks <= kDecConsumers;
-      const int igroups = few ? kDecConsumers / blocks : 1;
-      const int ig = few ? ct / blocks : 0;
-      const bool worker = few ? ig < igroups : true;
-      int my_j = 0, my_m0 = 0, my_k0 = 0, my_vcol = 0;
-      auto locate = [&](int blk) {
-        int j = 0, rest = blk, vcol = 0;
-        while (j < p.nseg - 1 && rest >= mb * (p.seg[j].r8 / 4)) {
-          rest -= mb * (p.seg[j].r8 / 4);
+      // t on the tensor cores: work items are (family, 8-column n tile, 16-token tile); when
+      // there are fewer than 8 items, several warps split an item's k steps (ksplit) and
+      // their fragments are summed in a fixed order. A: x [tokens][k] per box; B: the V
+      // slice [k][r8] of a family (ldmatrix.trans). The slice length is a multiple of 16, so
+      // every k step is whole; rows past K read as zero.
+      const int kmt = (p.M + 15) / 16;
+      int items = 0;
+      for (int j = 0; j < p.nseg; ++j) items += (p.seg[j].r8 / 8) * kmt;
+      const int ksplit = items >= 8 ? 1 : 8 / items;
+      const int nsteps = (n + 15) / 16;
+      const uint32_t vbase0 = smem_u32(stage_area);
+      const uint32_t xbase0 = smem_u32(xsb);
+      float* part = reinterpret_cast<float*>(stage_area);   // [items * ksplit][32 lanes][4], after the loop
+      float fr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      int my_item = -1;
+      // item -> family, its column block in the staged V, n tile, token tile
+      auto locate = [&](int item, int& j, int& vcol, int& nt, int& mt) {
+        j = 0;
+        vcol = 0;
+        int rest = item;
+        while (j < p.nseg - 1 && rest >= (p.seg[j].r8 / 8) * kmt) {
+          rest -= (p.seg[j].r8 / 8) * kmt;
           vcol += p.seg[j].r8;
           ++j;
         }
-        my_j = j;
-        my_m0 = (rest / (p.seg[j].r8 / 4)) * 4;
-        my_k0 = (rest % (p.seg[j].r8 / 4)) * 4;
-        my_vcol = vcol;
+        nt = rest / kmt;
+        mt = rest - nt * kmt;
       };
-      float park[16];
-      float* park_ptr = nullptr;
-      for (int blk = (few ? ct % blocks : ct); ok && worker && blk < blocks; blk += (few ? blocks : kDecConsumers)) {
-        locate(blk);
-        const int r8 = p.seg[my_j].r8;
-        const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage_area) + static_cast<size_t>(trows) * my_vcol;
-        float lacc[4][4];
-#pragma unroll
-        for (int x0 = 0; x0 < 4; ++x0)
-#pragma unroll
-          for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = 0.0f;
-        for (int b = 0; b < nvb; ++b) {
-          const int lo = b * p.vbox;
-          const int hi = min(n, lo + p.vbox);
-          const uint16_t* xb = xsb + b * xbs;
-          for (int i = lo + ig; i < hi; i += igroups) {
-            const uint2 vv = *reinterpret_cast<const uint2*>(vs + i * r8 + my_k0);
-            const float va[4] = {__uint_as_float(vv.x << 16), __uint_as_float(vv.x & 0xFFFF0000u),
-                                 __uint_as_float(vv.y << 16), __uint_as_float(vv.y & 0xFFFF0000u)};
-#pragma unroll
-            for (int x0 = 0; x0 < 4; ++x0) {
-              const int m = my_m0 + x0;
-              const float xv = m < p.M ? bf16_to_f32(xb[m * p.vbox + (i - lo)]) : 0.0f;
-#pragma unroll
-              for (int y0 = 0; y0 < 4; ++y0) lacc[x0][y0] = fmaf(xv, va[y0], lacc[x0][y0]);
-            }
-          }
+      const int npairs = items * ksplit;
+      for (int pr = cw; ok && pr < npairs; pr += 8) {
+        const int item = pr / ksplit, kpart = pr - item * ksplit;
+        int j, vcol, nt, mt;
+        locate(item, j, vcol, nt, mt);
+        const int r8 = p.seg[j].r8;
+        const uint32_t vbase = vbase0 + static_cast<uint32_t>(trows) * vcol * 2;
+        const int m = min(mt * 16 + (lane & 15), p.M - 1);   // rows past M repeat M-1; dropped
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int st = kpart; st < nsteps; st += ksplit) {
+          const int k0 = st * 16;
+          const int b = k0 / p.vbox, kk = k0 - b * p.vbox;
+          uint32_t a0, a1, a2, a3, b0, b1;
+          ldsm_x4(xbase0 + (b * xbs + m * p.vbox + kk + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+          ldsm_x2_trans(vbase + ((k0 + (lane & 15)) * r8 + nt * 8) * 2, b0, b1);
+          mma_16816(acc, a0, a1, a2, a3, b0, b1);
         }
-        if (few) {
-          // one 4 x 4 block per (residue class, block): no two threads share a word
-          float* pb = reinterpret_cast<float*>(stage_area) + (static_cast<size_t>(ig) * blocks + blk) * 16;
-          // the staging is still being read by other threads: the partials wait in
-          // registers until everyone is done (written below)
+        if (ksplit == 1) {
+          // the only warp on this item: straight to the global accumulator
+          const int gq = lane >> 2, qq = lane & 3;
 #pragma unroll
-          for (int x0 = 0; x0 < 4; ++x0)
-#pragma unroll
-            for (int y0 = 0; y0 < 4; ++y0) park[x0 * 4 + y0] = lacc[x0][y0];
-          park_ptr = pb;
+          for (int e = 0; e < 4; ++e) {
+            const int mm = mt * 16 + gq + 8 * (e >> 1), kc = nt * 8 + 2 * qq + (e & 1);
+            if (mm < p.M && kc < p.seg[j].r) atomicAdd(&p.t_acc[mm * p.r_total + p.seg[j].t_col + kc], acc[e]);
+          }
         } else {
 #pragma unroll
-          for (int x0 = 0; x0 < 4; ++x0)
-#pragma unroll
-            for (int y0 = 0; y0 < 4; ++y0) {
-              const int m = my_m0 + x0, k = my_k0 + y0;
-              if (m < p.M && k < p.seg[my_j].r) atomicAdd(&tacc[m * p.r_total + p.seg[my_j].t_col + k], lacc[x0][y0]);
-            }
+          for (int e = 0; e < 4; ++e) fr[e] = acc[e];
+          my_item = pr;
         }
       }
-      if (few) {
-        // fixed-order sum over the residue classes through the (now free) staging area
+      if (ksplit > 1) {
+        // partial fragments over the (no longer read) staging, then a fixed-order sum
         if (ok) ok = cons_sync(cbar, cph, ctl);
-        if (ok && park_ptr) {
+        if (ok && my_item >= 0) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) park_ptr[e] = park[e];
+          for (int e = 0; e < 4; ++e) part[(my_item * 32 + lane) * 4 + e] = fr[e];
         }
         if (ok) ok = cons_sync(cbar, cph, ctl);
-        if (ok) {
-          const float* pall = reinterpret_cast<const float*>(stage_area);
-          for (int idx = ct; idx < blocks * 16; idx += kDecConsumers) {
+        if (ok && cw < items) {
+          const int item = cw;
+          int j, vcol, nt, mt;
+          locate(item, j, vcol, nt, mt);
+          const int gq = lane >> 2, qq = lane & 3;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
             float v = 0.0f;
-            for (int g2 = 0; g2 < igroups; ++g2) v += pall[g2 * blocks * 16 + idx];
-            const int blk = idx >> 4, e = idx & 15;
-            locate(blk);
-            const int m = my_m0 + (e >> 2), k = my_k0 + (e & 3);
-            if (m < p.M && k < p.seg[my_j].r) tacc[m * p.r_total + p.seg[my_j].t_col + k] = v;
+            for (int kp = 0; kp < ksplit; ++kp) v += part[((item * ksplit + kp) * 32 + lane) * 4 + e];
+            const int mm = mt * 16 + gq + 8 * (e >> 1), kc = nt * 8 + 2 * qq + (e & 1);
+            if (mm < p.M && kc < p.seg[j].r) atomicAdd(&p.t_acc[mm * p.r_total + p.seg[j].t_col + kc], v);
           }
         }
       }
-      if (ok) ok = cons_sync(cbar, cph, ctl);
       if (ok) {
-        for (int idx = ct; idx < ntot; idx += kDecConsumers) atomicAdd(&p.t_acc[idx], tacc[idx]);
         __threadfence();
         ok = cons_sync(cbar, cph, ctl);
         if (ok && ct == 0) atomicAdd(&p.counters[0], 1);

@@ -567,9 +567,9 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       // the thinnest slice does not, give the launch the shared memory it needs.
       const int64_t tacc_bytes = round_up(M * wl.r_total * 4, 1024);
       const int64_t tspace = static_cast<int64_t>(smem) - kHeaderBytes - kSmemSlack - tacc_bytes;
-      const int64_t max_t = std::max<int64_t>(1, ceil_div(K, 8));
+      const int64_t max_t = std::max<int64_t>(1, ceil_div(K, 16));
       for (;;) {
-        const int64_t ks = round_up(ceil_div(K, dp.t_ctas), 8);   // the kernel's slice length
+        const int64_t ks = round_up(ceil_div(K, dp.t_ctas), 16);   // the kernel's slice length
         const int64_t nvb = ceil_div(ks, 256);
         dp.vbox = static_cast<int32_t>(round_up(ceil_div(ks, nvb), 16));
         // per box: V rows of every family, then x [M][vbox] padded to 128 bytes
