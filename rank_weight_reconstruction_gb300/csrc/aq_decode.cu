@@ -93,8 +93,8 @@ __device__ __forceinline__ uint32_t stage_addr(uint32_t base, int w3d, int kbox,
   return base + b * box_bytes + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-// header: full[kMaxStages], empty[kMaxStages], cbar, vbar, two ints, then the s buffers
-static_assert((2 * kMaxStages + 2) * 8 + 8 <= kSBufOffset, "s buffers overlap the barriers");
+// header: full[kMaxStages], empty[kMaxStages], cbar, vbar, tbar, two ints, then the s buffers
+static_assert((2 * kMaxStages + 3) * 8 + 8 <= kSBufOffset, "s buffers overlap the barriers");
 static_assert(kSBufOffset + 2 * kSBufBytes <= kHeaderBytes, "s buffers exceed the header");
 static_assert(((kMmaM + 14) / 8) * 16 <= kSBufBytes, "s buffer too small for a 128-row chunk");
 
@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   uint64_t* empty = full + kMaxStages;
   uint64_t* cbar = empty + kMaxStages;
   uint64_t* vbar = cbar + 1;
-  int* abort_flag = reinterpret_cast<int*>(vbar + 1);
+  uint64_t* tbar = vbar + 1;   // t of this CTA's family is in shared memory (from the t CTAs)
+  int* abort_flag = reinterpret_cast<int*>(tbar + 1);
   int* bcast = abort_flag + 1;
   uint8_t* epi = smem + kHeaderBytes;
   uint8_t* xres = epi + p.epi_bytes;
@@ -135,6 +136,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
   const int rot = t_cta ? 0 : (g * 7) % nstage;
   const uint32_t xbox_bytes = static_cast<uint32_t>(p.tok_tile) * 128u;
   const bool local_t = !t_cta && p.t_local && sg.r > 0;
+  // t from the t CTAs: small tiles are fetched early by lanes 1-31 of warp 0, large ones
+  // (where 31 lanes would need many round trips) by all consumers in the first epilogue
+  const bool early_t = !t_cta && sg.r > 0 && p.t_ctas > 0 && kTok * sg.r16 <= kEarlyTMax;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     }
     mbar_init(cbar, kDecConsumers);
     mbar_init(vbar, 1);
+    mbar_init(tbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -262,6 +267,60 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(vbar, 0u))
           if (global_timer_ns() - t0 > 20000000ull) break;
+      }
+    }
+    if (!t_cta && lane > 0 && p.t_ctas > 0 && (early_t || sg.r == 0)) {
+      // ---- t from the t CTAs, fetched by lanes 1-31 of this warp while lane 0 feeds the
+      // ring and the consumers stream W0: wait for all t CTAs to publish, write t_hi / t_lo
+      // for the epilogue, then count this CTA as done with the accumulator (t CTA 0 clears
+      // it once every streaming CTA has) ----
+      constexpr uint32_t kLanes = 0xFFFFFFFEu;
+      pdl_wait_prior_grid();
+      if (early_t) {
+        bool got = true;
+        if (lane == 1) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(&p.counters[0]) < p.t_ctas) {
+            if (*reinterpret_cast<volatile int*>(abort_flag) || global_timer_ns() - t0 > p.timeout_ns) {
+              *reinterpret_cast<volatile int*>(abort_flag) = 1;
+              atomicExch(p.status, kStatusTimeout);
+              got = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        got = __shfl_sync(kLanes, got ? 1 : 0, 1) != 0;
+        if (got) {
+          const int rs16 = sg.r16 + 8;
+          uint16_t* tbh = reinterpret_cast<uint16_t*>(reinterpret_cast<float*>(epi) + p.ts_off);
+          uint16_t* tbl = tbh + kTok * rs16;
+          const int nt_el = kTok * sg.r16;
+          for (int base = lane - 1; base < nt_el; base += 4 * 31) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {   // four loads in flight per lane
+              const int idx = base + u * 31;
+              const int m = idx / sg.r16, k = idx - m * sg.r16;
+              v[u] = (idx < nt_el && m < p.M && k < sg.r) ? __ldcg(&p.t_acc[m * p.r_total + sg.t_col + k]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int idx = base + u * 31;
+              if (idx < nt_el) {
+                const int m = idx / sg.r16, k = idx - m * sg.r16;
+                const uint16_t h = f32_to_bf16_rn(v[u]);
+                tbh[m * rs16 + k] = h;
+                tbl[m * rs16 + k] = f32_to_bf16_rn(v[u] - bf16_to_f32(h));
+              }
+            }
+          }
+        }
+        __syncwarp(kLanes);
+      }
+      if (lane == 1) {
+        red_release_gpu_add(&p.counters[1], 1);
+        if (early_t) mbar_arrive(tbar);   // also when the wait gave up: the epilogue sees the abort
       }
     }
   } else {
@@ -391,6 +450,34 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         __threadfence();
         ok = cons_sync(cbar, cph, ctl);
         if (ok && ct == 0) atomicAdd(&p.counters[0], 1);
+      }
+      if (ok && cta == 0) {
+        // Every streaming CTA counts itself once it has read t: then the accumulator and
+        // both counters go back to zero for the next call (the sync region's invariant).
+        if (ct == 0) {
+          bool all = true;
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(&p.counters[1]) < grid - p.t_ctas) {
+            if (*reinterpret_cast<volatile int*>(abort_flag) || global_timer_ns() - t0 > p.timeout_ns) {
+              *reinterpret_cast<volatile int*>(abort_flag) = 1;
+              atomicExch(p.status, kStatusTimeout);
+              all = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+          *bcast = all ? 1 : 0;
+        }
+        ok = cons_sync(cbar, cph, ctl);
+        if (ok && *bcast) {
+          for (int idx = ct; idx < p.M * p.r_total; idx += kDecConsumers) p.t_acc[idx] = 0.0f;
+          ok = cons_sync(cbar, cph, ctl);
+          if (ok && ct == 0) {
+            p.counters[0] = 0;
+            p.counters[1] = 0;
+            __threadfence();
+          }
+        }
       }
     } else {
       // s and the U rows of a chunk go to shared memory with cp.async when the chunk
@@ -644,7 +731,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               my[rr * kTok + tok + 1] = acc[nt][2 * h + 1];
             }
         }
-        if (sg.r > 0 && !p.t_local && ch == 0) {   // t stays in shared memory for later chunks
+        if (early_t && ch == 0) {   // t (from warp 0) stays for later chunks
+          if (!(ok = warp_wait_all(tbar, 0u, ctl))) break;
+          if (*reinterpret_cast<volatile int*>(abort_flag)) {
+            ok = false;
+            break;
+          }
+        } else if (sg.r > 0 && !p.t_local && ch == 0) {   // t stays in shared memory for later chunks
           if (ct == 0) {
             bool ready = true;
             const uint64_t t0 = global_timer_ns();
@@ -679,6 +772,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
               if (idx < nt_el) put_t(m, k, v[u]);
             }
           }
+          // all consumers have read t: count this CTA as done with the accumulator
+          if (!(ok = cons_sync(cbar, cph, ctl))) break;
+          if (ct == 0) red_release_gpu_add(&p.counters[1], 1);
         }
         cp_async_wait_all();
         if (!(ok = cons_sync(cbar, cph, ctl))) break;
@@ -750,28 +846,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
     }
 
     if (!t_cta) cp_async_wait_all();   // no copy may still be landing when the CTA exits
-    // The last CTA to finish clears the sync region for the next call (nothing to clear
-    // when no CTA computes t for the others).
-    if (ok && p.t_ctas > 0) ok = cons_sync(cbar, cph, ctl);
-    if (ok && p.t_ctas > 0) {
-      if (ct == 0) {
-        __threadfence();
-        const int old = atomicAdd(&p.counters[1], 1);
-        *bcast = (old == grid - 1) ? 1 : 0;
-      }
-      ok = cons_sync(cbar, cph, ctl);
-      if (ok && *bcast) {
-        __threadfence();
-        for (int idx = ct; idx < p.M * p.r_total; idx += kDecConsumers) p.t_acc[idx] = 0.0f;
-        __threadfence();
-        ok = cons_sync(cbar, cph, ctl);
-        if (ok && ct == 0) {
-          p.counters[0] = 0;
-          p.counters[1] = 0;
-          __threadfence();
-        }
-      }
-    }
   }
   __syncthreads();
 }

@@ -80,6 +80,7 @@ constexpr int kDecMaxTok = 32;          // tokens the decode kernel handles
 constexpr int kDecMaxEpiBytes = 48 * 1024;  // largest epilogue staging (sums + t)
 constexpr int kDecMaxTCtas = 16;        // most CTAs that compute t = V^T x
 constexpr int kDecLocalMaxR8 = 32;      // largest r8 for which streaming CTAs compute t themselves
+constexpr int kEarlyTMax = 512;      // largest t tile (tokens x r16) warp 0 fetches during the W0 loop
 // Two buffers for a chunk's s (up to 128 rows + 8 of alignment) in the kernel's header,
 // after its mbarriers and flags.
 constexpr int kSBufOffset = 384;
