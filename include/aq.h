@@ -35,8 +35,9 @@
  *   wait that expired) are recorded in a per-device status word read by
  *   aq_device_status().
  * - Rounding: products accumulate in fp32; each output element is rounded to bf16
- *   once (nearest-even). t = V^T x is held in bf16 between the two kernels that
- *   produce and consume it.
+ *   once (nearest-even). On the prefill path t = V^T x is held in bf16 between the
+ *   tiles that produce it and those that consume it; on the decode path it stays fp32
+ *   and enters U t as a pair of bf16 values (about 16 significant bits).
  */
 #ifndef AQ_H_
 #define AQ_H_
@@ -87,8 +88,9 @@ typedef struct aq_theta {
   int32_t r;
 } aq_theta;
 
-/* Workspace of aq_linear / aq_linear_qkv. Its first AQ_WORKSPACE_SYNC_BYTES hold the
- * counters and the fp32 accumulator of t = V^T x that the CTAs of the decode kernel share:
+/* Workspace of aq_linear / aq_linear_qkv / aq_linear_multi. Its first
+ * AQ_WORKSPACE_SYNC_BYTES hold the counters and the fp32 accumulator of t = V^T x that the
+ * CTAs of the decode kernel share, and the per-token-tile flags of the prefill kernel:
  * that part must be zero before the workspace is first used (e.g. cudaMemset once after
  * allocating it), and every call that completes leaves it zero again, so one workspace
  * can serve any sequence of calls, shapes and paths on a stream. The rest is scratch

@@ -253,7 +253,8 @@ void theta_spans(const aq_theta* th, Span* out4) {
 //   [0, kSyncBytes)   sync region: zero before first use, left zero by every decode call
 //                     (tile arrival counters, fp32 t accumulator)
 //   [kSyncBytes, ..)  scratch, no initialisation needed (prefill: t [M, ld_t] bf16, then
-//                     V^T [r_j, ldvt] per family); decode uses only the sync region
+//                     V^T of every family stacked as [ld_t, ldvt]: family j at row t_col[j],
+//                     like its columns of t); decode uses only the sync region
 // ---------------------------------------------------------------------------------
 struct WsLayout {
   int64_t ld_t = 0;              // prefill: row stride of t [M, sum round_up(r_j, 8)]
@@ -281,13 +282,10 @@ WsLayout ws_layout(const aq_theta* const* th, int n, int64_t M) {
   }
   if (M <= 0) return w;
   if (w.any_r) {
-    size_t off = static_cast<size_t>(round_up(M * w.ld_t * 2, 256));
+    const size_t off = static_cast<size_t>(round_up(M * w.ld_t * 2, 256));
     w.ldvt = round_up(th[0]->in, 8);
-    for (int j = 0; j < n; ++j) {
-      w.vt_off[j] = kSyncBytes + off;
-      if (th[j]->r > 0) off += static_cast<size_t>(round_up(static_cast<int64_t>(th[j]->r) * w.ldvt * 2, 256));
-    }
-    w.prefill_scratch = off;
+    for (int j = 0; j < n; ++j) w.vt_off[j] = kSyncBytes + off + static_cast<size_t>(w.t_col[j] * w.ldvt * 2);
+    w.prefill_scratch = off + static_cast<size_t>(round_up(w.ld_t * w.ldvt * 2, 256));
   }
   if (M <= kDecodeMaxM || w.any_r) w.total = kSyncBytes + std::max(w.decode_scratch, w.prefill_scratch);
   return w;
@@ -712,23 +710,22 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   if ((st = tmap_2d(&gp.tm_x, x, K, M, ldx, gp.tok_tile, "x")) != AQ_OK) return st;
   int tiles = 0;
   if (fused_t) {
-    // t segments first: t [M, r_j] = x V_j, row operand V_j^T, no scale, no rank-r part
-    for (int j = 0; j < n; ++j) {
-      if (th[j]->r == 0) continue;
-      GemmSeg& s = gp.seg[gp.nseg++];
-      if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[j], K, th[j]->r, wl.ldvt, box_rows, "V^T")) != AQ_OK) return st;
-      s.s = nullptr;
-      s.y = tbuf + wl.t_col[j];
-      s.ldy = wl.ld_t;
-      s.rows = th[j]->r;
-      s.r = 0;
-      s.t_seg = 1;
-      s.n_row_tiles = static_cast<int32_t>(ceil_div(th[j]->r, gp.row_tile));
-      s.n_mma = static_cast<int32_t>(std::min<int64_t>(round_up(th[j]->r, 16), gp.row_tile));
-      s.tile_begin = tiles;
-      tiles += s.n_row_tiles * gp.n_tok_units;
-      gp.t_need += s.n_row_tiles;
-    }
+    // one t segment first: t [M, ld_t] = x [V_0 | V_1 | ...] over the stacked V^T (rows of
+    // padding between families feed only padding columns of t, which nothing reads), no
+    // scale, no rank-r part
+    GemmSeg& s = gp.seg[gp.nseg++];
+    if ((st = tmap_2d(&s.tm_w, wsb + wl.vt_off[0], K, wl.ld_t, wl.ldvt, box_rows, "V^T")) != AQ_OK) return st;
+    s.s = nullptr;
+    s.y = tbuf;
+    s.ldy = wl.ld_t;
+    s.rows = static_cast<int32_t>(wl.ld_t);
+    s.r = 0;
+    s.t_seg = 1;
+    s.n_row_tiles = static_cast<int32_t>(ceil_div(wl.ld_t, gp.row_tile));
+    s.n_mma = static_cast<int32_t>(std::min<int64_t>(round_up(wl.ld_t, 16), gp.row_tile));
+    s.tile_begin = tiles;
+    tiles += s.n_row_tiles * gp.n_tok_units;
+    gp.t_need = s.n_row_tiles;
     gp.t_flags = reinterpret_cast<int32_t*>(wsb);
     gp.n_flags = static_cast<int32_t>(n_flags);
   }

@@ -57,23 +57,23 @@ def _linear(lib, th, x=0x100000, M=4, ldx=32, y=0x200000, ldy=64, ws=0x300000, w
 def test_workspace_bytes(lib):
     """Layout: a zero-initialised sync region of AQ_WORKSPACE_SYNC_BYTES (all the decode
     kernel needs), then prefill scratch: t as bf16 [M, sum round_up(r, 8)] (rounded to
-    256 B) and V^T [r, round_up(in, 8)] per family (each rounded to 256 B). For M <= 32 the
-    workspace covers both paths."""
+    256 B) and V^T of all families stacked as [sum round_up(r, 8), round_up(in, 8)] (rounded
+    to 256 B). For M <= 32 the workspace covers both paths."""
     sync = binding.AQ_WORKSPACE_SYNC_BYTES
     th = _theta(out=64, inp=32, r=4)
-    # M = 4: t 4 x 8 x 2 = 64 -> 256, V^T 4 x 32 x 2 = 256
-    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 4) == sync + 256 + 256
+    # M = 4: t 4 x 8 x 2 = 64 -> 256, V^T 8 x 32 x 2 = 512
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 4) == sync + 256 + 512
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 0) == 0
-    # M = 100: prefill only: t 100 x 8 x 2 = 1600 -> 1792, V^T 256
-    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 100) == sync + 1792 + 256
+    # M = 100: prefill only: t 100 x 8 x 2 = 1600 -> 1792, V^T 512
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 100) == sync + 1792 + 512
     th0 = _theta(r=0)
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th0), 1, 1000) == 0
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th0), 1, 8) == sync
     arr = (binding.c_theta * 3)(_theta(r=4), _theta(r=0), _theta(r=12))
-    # M = 8: t 8 x (8 + 16) x 2 = 384 -> 512, V^T 256 + 768
-    assert lib.aq_linear_workspace_bytes(arr, 3, 8) == sync + 512 + 256 + 768
+    # M = 8: t 8 x (8 + 16) x 2 = 384 -> 512, V^T (8 + 16) x 32 x 2 = 1536
+    assert lib.aq_linear_workspace_bytes(arr, 3, 8) == sync + 512 + 1536
     # M = 40: t 40 x 24 x 2 = 1920 -> 2048
-    assert lib.aq_linear_workspace_bytes(arr, 3, 40) == sync + 2048 + 256 + 768
+    assert lib.aq_linear_workspace_bytes(arr, 3, 40) == sync + 2048 + 1536
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 2, 8) == ctypes.c_size_t(-1).value
 
 
