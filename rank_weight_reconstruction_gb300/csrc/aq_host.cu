@@ -308,7 +308,8 @@ int stages_for(uint32_t stage_bytes, size_t smem_cap, size_t fixed) {
 
 // Prefill N tile: minimise waves x the cost of one tile.
 int prefill_row_tile(const aq_theta* const* th, int n, int64_t n_tok_tiles, int sms) {
-  static const int cand[] = {256, 224, 192, 160, 128, 112, 96, 80, 64, 48, 32, 16};
+  // multiples of 64 only: the epilogue writes y in 64-column bulk stores
+  static const int cand[] = {256, 192, 128, 64};
   int best = 256;
   double best_cost = 1e300;
   for (int bn : cand) {

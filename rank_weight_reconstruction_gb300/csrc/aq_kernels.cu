@@ -555,10 +555,11 @@ __global__ void __launch_bounds__(256) aq_transpose_kernel(const __grid_constant
   const int i0 = blockIdx.x * 32;
   const int k0 = blockIdx.y * 32;
   pdl_launch_dependents();
-  pdl_wait_prior_grid();
   if (k0 >= sg.r) return;
   const int tx = threadIdx.x & 31;
   const int ty = threadIdx.x >> 5;
+  // V is a weight: read it while the previous kernel finishes; the workspace it is written
+  // to may still be in use until then
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = i0 + ty + 8 * j;
@@ -566,6 +567,7 @@ __global__ void __launch_bounds__(256) aq_transpose_kernel(const __grid_constant
     tile[ty + 8 * j][tx] = (i < p.K && k < sg.r) ? sg.V[static_cast<int64_t>(i) * sg.ldv + k] : 0;
   }
   __syncthreads();
+  pdl_wait_prior_grid();
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int k = k0 + ty + 8 * j;
