@@ -237,6 +237,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
         mbar_arrive_expect_tx(vbar, nvb * vb);
         for (int b = 0; b < nvb; ++b) tma_load_2d_plain(vres + b * vb, &sg.tm_v, 0, b * p.vbox, vbar);
       }
+      // x row g of the first M streaming CTAs into L2 while the previous kernel finishes,
+      // so the reads of x after the dependency wait hit L2 (rows are 16-byte aligned and
+      // K * 2 bytes long, a multiple of 16)
+      if (g < p.M) prefetch_l2_bulk(p.x + static_cast<int64_t>(g) * p.ldx, static_cast<uint32_t>(p.K) * 2u);
       pdl_wait_prior_grid();
       for (int q = 0; q < pre; ++q) issue(q, q, false, true);
       int slot = pre == p.stages ? 0 : pre;

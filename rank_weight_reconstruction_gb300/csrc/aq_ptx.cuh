@@ -160,6 +160,12 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int c0, int 
                "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2. A hint
+// only: a line fetched early is kept coherent by L2, which every write goes through.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
