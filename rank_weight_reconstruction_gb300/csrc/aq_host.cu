@@ -23,6 +23,8 @@ thread_local int32_t t_launches = 0;
 std::atomic<int> g_path{AQ_PATH_AUTO};
 
 constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
+constexpr int kGemmMinMBigW0 = 16;                    // ... but from this M the GEMM takes calls
+constexpr int64_t kGemmBigW0Bytes = 128ll << 20;      // whose W0 has at least this many bytes
 constexpr uint64_t kTimeoutNs = 1000ull * 1000 * 1000;  // limit of one in-kernel wait: 1 s
 constexpr size_t kSmemSlack = 1024;                   // room to align the dynamic smem base
 
@@ -387,7 +389,14 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   }
 
   const int path_cfg = g_path.load();
-  const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM);
+  // From 16 tokens on, a call with a large W0 runs faster on the tcgen05 GEMM than on the
+  // mma.sync decode kernel, whose issue rate then bounds it (measured on the 31B-class
+  // 21504 x 5376 projection: 50.9 vs 62.3 us at M = 16, 50.7 vs 84.8 us at M = 32); at
+  // 5376 x 5376 and on the Gemma-3-1B shapes the decode kernel is as fast or faster.
+  int64_t w0_bytes = 0;
+  for (int j = 0; j < n; ++j) w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
+  const bool gemm_pays = M >= kGemmMinMBigW0 && w0_bytes >= kGemmBigW0Bytes;
+  const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM && !gemm_pays);
   if (decode && M > kDecodeMaxM)
     return fail(AQ_ERR_UNSUPPORTED, "%s: the decode kernel handles at most %d tokens (M=%lld)", who, kDecodeMaxM,
                 (long long)M);

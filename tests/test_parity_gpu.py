@@ -330,10 +330,34 @@ def test_31b_projection(M):
     th = synth.make_theta(("31b", "wide", 0), out, inp, 128)
     xb = synth.make_x(("31b-x", M), M, inp)
     y = host_f64(run_linear(th, xb))
+    # a W0 of 231 MB takes the tcgen05 GEMM from 16 tokens on
+    assert aq.aq_last_path() == (aq.AQ_PATH_DECODE if M < 16 else aq.AQ_PATH_PREFILL)
     W0, s, U, V = th.f64()
     xf = x_f64(xb, inp)
     rows = np.arange(M) if M <= 32 else np.unique(np.linspace(0, M - 1, 48).astype(int))
     assert_close(y[rows], oracle.linear(W0, s, U, V, xf[rows]))
+
+
+@pytest.mark.parametrize("M", [16, 32])
+def test_31b_projection_decode_forced(M):
+    """The decode kernel on the 31B-class projection where the automatic choice is the GEMM."""
+    out, inp = synth.CLASS31B_SHAPES["wide"]
+    th = synth.make_theta(("31b", "wide", 0), out, inp, 128)
+    xb = synth.make_x(("31b-x", M), M, inp)
+    y = host_f64(run_linear(th, xb, path=aq.AQ_PATH_DECODE))
+    assert aq.aq_last_path() == aq.AQ_PATH_DECODE
+    assert_close(y, oracle.linear(*th.f64(), x_f64(xb, inp)))
+
+
+def test_path_choice_by_size():
+    """Up to 32 tokens the decode kernel, except from 16 tokens on for a W0 of 128 MB or more."""
+    sq = synth.CLASS31B_SHAPES["square"]
+    th = synth.make_theta(("31b", "square", 0), sq[0], sq[1], 128)
+    for M in (1, 16, 32):
+        run_linear(th, synth.make_x(("path", M), M, sq[1]))
+        assert aq.aq_last_path() == aq.AQ_PATH_DECODE, M
+    run_linear(th, synth.make_x(("path", 33), 33, sq[1]))
+    assert aq.aq_last_path() == aq.AQ_PATH_PREFILL
 
 
 # ----------------------------------------------------------------------------------
