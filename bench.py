@@ -2,12 +2,15 @@
 """Benchmark of the theta-bundle reconstruction linear on GB300.
 
 Headline (one "step"): the Gemma-3-1B-shaped decode stack -- 26 layers x 7 projection
-families (q/k/v batched through aq_linear_qkv; o, gate, up, down through aq_linear),
+families in the pages' production-path form (q/k/v batched through aq_linear_qkv, gate and
+up batched through aq_linear_multi, o and down through aq_linear: 4 calls per layer),
 r = 16, one pass at each of M = 1, 4 and 16 tokens -- captured once into a CUDA graph
 and replayed. Each layer reads its own physical copy of the family W0 (1.40 GB per pass,
-well above the 129 MB L2), so W0 streams from HBM: value = algorithmic bytes / time.
+well above the 129 MB L2), so W0 streams from HBM: value = algorithmic bytes / time (x of
+a batched call counted once).
 
-Also measured in the same run (extra keys): the same stack with one shared W0 per family
+Also measured in the same run (extra keys): the same step with gate and up as separate
+calls; the same stack with one shared W0 per family
 as served at G = 1 (W0 stays in L2; effective GB/s, not an HBM figure); prefill TFLOP/s
 on Gemma-3-1B shapes (r = 64, M = 8192) and on the 31B-class projection (21504 x 5376,
 r = 128, M = 8192); W_eff precompute GB/s over the 60-layer 31B-class stack with G = 4.
@@ -62,13 +65,25 @@ def precompute_bytes(out, inp, r):
     return 2 * (2 * out * inp + r * (out + inp) + out)
 
 
-def step_bytes():
+def gate_up_bytes(r, M):
+    """gate and up over one x in one batched call: x counted once, like Q/K/V."""
+    (og, ig), (ou, iu) = FAMS["gate_proj"], FAMS["up_proj"]
+    return linear_bytes(og, ig, r, M) + linear_bytes(ou, iu, r, M) - 2 * M * ig
+
+
+def step_bytes(fuse_gateup=True):
+    """Algorithmic bytes of one decode step. fuse_gateup: gate and up of a layer are one
+    batched call (the pages' production path), so their shared x is read once."""
     qkv_shapes = [FAMS[f] for f in ("q_proj", "k_proj", "v_proj")]
     total = 0
     for M in DECODE_MS:
         per_layer = qkv_bytes(qkv_shapes, DECODE_RANK, M)
-        for f in ("o_proj", "gate_proj", "up_proj", "down_proj"):
+        for f in ("o_proj", "down_proj"):
             per_layer += linear_bytes(*FAMS[f], DECODE_RANK, M)
+        if fuse_gateup:
+            per_layer += gate_up_bytes(DECODE_RANK, M)
+        else:
+            per_layer += sum(linear_bytes(*FAMS[f], DECODE_RANK, M) for f in ("gate_proj", "up_proj"))
         total += LAYERS * per_layer
     return total
 
@@ -322,7 +337,7 @@ class DecodeStack:
                 if fuse_gateup and f == "up_proj":
                     continue
                 if fuse_gateup and f == "gate_proj":
-                    if only is None:
+                    if only in (None, "gate_up"):
                         out.append(("gate_up", M, lambda th=th, xv=xv, yv=yv: aq.aq_linear_multi(
                             [th["gate_proj"], th["up_proj"]], xv["mlp"], ys=[yv["gate_proj"], yv["up_proj"]],
                             workspace=self.ws)))
@@ -349,6 +364,8 @@ class DecodeStack:
 
 
 def call_bytes(key, M):
+    if key == "gate_up":
+        return gate_up_bytes(DECODE_RANK, M)
     if key == "qkv":
         return qkv_bytes([FAMS[f] for f in ("q_proj", "k_proj", "v_proj")], DECODE_RANK, M)
     return linear_bytes(*FAMS[key], DECODE_RANK, M)
@@ -370,7 +387,7 @@ def run_ours(args, dist: Dist):
     pk = peaks()
 
     stack = DecodeStack(device, copies=True)
-    g, launches, calls = stack.capture()
+    g, launches, calls = stack.capture(fuse_gateup=True)
     B = step_bytes()
     assert B == sum(call_bytes(k, M) for k, M, _ in calls)
     for _ in range(args.warmup):
@@ -412,7 +429,8 @@ def run_ours(args, dist: Dist):
                 "s~U(0.9,1.1), U,V~N(0,0.01^2), x~N(0,1); shapes only, no trained weights",
         "config": {"workload": "gemma3-1b-shaped decode stack: 26 layers x 7 projection families "
                                "(q 1024x1152, k/v 256x1152, o 1152x1024, gate/up 6912x1152, down 1152x6912), "
-                               "r=16, one pass each at M=1,4,16; q/k/v batched via aq_linear_qkv",
+                               "r=16, one pass each at M=1,4,16; q/k/v batched via aq_linear_qkv and gate/up via "
+                               "aq_linear_multi (the pages' production-path fusion, 4 calls per layer)",
                    "layers": LAYERS, "rank": DECODE_RANK, "M": list(DECODE_MS), "calls_per_step": len(calls),
                    "algorithmic_bytes_per_step": B,
                    "w0_storage": "G=1 values, one physical W0 copy per layer (1.40 GB streamed per M pass)",
@@ -426,15 +444,17 @@ def run_ours(args, dist: Dist):
     result["clocks"] = clk.summary()
 
     # ---- per-call timing of the dominant call type (roofline) ----
+    # (the step's own call types, plus gate and up as single calls for comparison)
+    step_types = ("gate_up", "down_proj", "o_proj", "qkv")
     per_type = {}
-    for key in ("gate_proj", "up_proj", "down_proj", "o_proj", "qkv"):
+    for key in step_types + ("gate_proj", "up_proj"):
         for M in DECODE_MS:
-            gk, nl, ck = stack.capture(only=key, M=M)
+            gk, nl, ck = stack.capture(only=key, M=M, fuse_gateup=key == "gate_up")
             t = time_graph(gk, max(3, args.steps))
             per_type[(key, M)] = {"ms_per_call": t / len(ck), "bytes_per_call": call_bytes(key, M),
                                   "launches_per_call": nl / len(ck)}
             del gk
-    total = {k: v["ms_per_call"] * LAYERS for k, v in per_type.items()}
+    total = {k: v["ms_per_call"] * LAYERS for k, v in per_type.items() if k[0] in step_types}
     dom = max(total, key=total.get)
     d = per_type[dom]
     ach = d["bytes_per_call"] / (d["ms_per_call"] * 1e-3) / 1e9
@@ -498,19 +518,19 @@ def extras(result, args, dist, stack, device, pk):
     import rank_weight_reconstruction_gb300 as aq
     from rank_weight_reconstruction_gb300 import Theta
 
-    # ---- the same step with gate and up of each layer in one aq_linear_multi call ----
-    gf, lf, _ = stack.capture(fuse_gateup=True)
+    # ---- the same step with gate and up of each layer as two aq_linear calls ----
+    gf, lf, _ = stack.capture(fuse_gateup=False)
     t = time_graph(gf, max(3, args.steps))
-    result["decode_gateup_fused"] = {"GB_s": round(step_bytes() / (t * 1e-3) / 1e9, 1), "ms_per_step": round(t, 4),
-                                     "launches_per_step": lf,
-                                     "note": "same step and bytes, gate and up of a layer batched (Q/K/V and gate-up "
-                                             "fusion of the pages' production path)"}
+    result["decode_gateup_separate"] = {"GB_s": round(step_bytes(fuse_gateup=False) / (t * 1e-3) / 1e9, 1),
+                                        "ms_per_step": round(t, 4), "launches_per_step": lf,
+                                        "note": "same outputs, gate and up of a layer as separate calls (5 calls per "
+                                                "layer; x of the MLP read twice)"}
     del gf
     torch.cuda.empty_cache()
 
     # ---- as served at G = 1: one shared W0 per family (L2-resident) ----
     shared = DecodeStack(device, copies=False, seed_tag="bench")
-    gs, _, calls = shared.capture()
+    gs, _, calls = shared.capture(fuse_gateup=True)
     t = time_graph(gs, max(3, args.steps))
     result["decode_g1_as_served"] = {"effective_GB_s": round(step_bytes() / (t * 1e-3) / 1e9, 1),
                                      "ms_per_step": round(t, 4),
@@ -690,8 +710,7 @@ def cpu_baseline(args, budget_s=15.0, steps=1):
                 oracle.linear(*th[f], xs[M][FAMS[f][1]])
         spent += time.perf_counter() - t0
         for M in DECODE_MS:
-            done_bytes += call_bytes("qkv", M) + sum(call_bytes(f, M) for f in ("o_proj", "gate_proj", "up_proj",
-                                                                                  "down_proj"))
+            done_bytes += sum(call_bytes(k, M) for k in ("qkv", "o_proj", "gate_up", "down_proj"))
         layers_done += 1
         layer += 1
     return {"value": round(done_bytes / spent / 1e9, 3), "unit": "GB/s", "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
@@ -705,7 +724,8 @@ def run_case(args, dist: Dist):
     one stream (the single-kernel workload that kernel-profiler captures use).
 
     ``linear:out,in,r,M`` times aq_linear on a seeded theta bundle and x [M, in];
-    ``precompute:out,in,r`` times aq_precompute. Prints one JSON line with the average
+    ``gateup:out,in,r,M`` times aq_linear_multi over two such bundles sharing x (the batched
+    gate and up projections); ``precompute:out,in,r`` times aq_precompute. Prints one JSON line with the average
     microseconds per call and its algorithmic bytes or flops."""
     import torch
     import rank_weight_reconstruction_gb300 as aq
@@ -730,12 +750,25 @@ def run_case(args, dist: Dist):
         ws = aq.new_workspace(aq.aq_linear_workspace_bytes(theta, M), device)
         run = lambda: aq.aq_linear(theta, x, y=y, workspace=ws)
         work = {"bytes": linear_bytes(out, inp, r, M), "flops": linear_flops(out, inp, r, M)}
+    elif kind == "gateup":
+        M = vals[3]
+        th2 = synth.make_theta(("case", "up", out, inp, r), out, inp, r)
+        theta2 = aq.Theta(W0=dev_bits(th2.W0, device)[:, :inp], s=dev_bits(th2.s, device),
+                          U=dev_bits(th2.U, device)[:, :r] if r else None,
+                          V=dev_bits(th2.V, device)[:, :r] if r else None)
+        x = dev_bits(synth.make_x(("case", M), M, inp), device)[:, :inp]
+        ys = [torch.empty(M, (out + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :out] for _ in range(2)]
+        ws = aq.new_workspace(aq.aq_linear_workspace_bytes([theta, theta2], M), device)
+        run = lambda: aq.aq_linear_multi([theta, theta2], x, ys=ys, workspace=ws)
+        work = {"bytes": 2 * linear_bytes(out, inp, r, M) - 2 * M * inp,
+                "flops": 2 * linear_flops(out, inp, r, M)}
     elif kind == "precompute":
         W = torch.empty(out, (inp + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :inp]
         run = lambda: aq.aq_precompute(theta, W_eff=W)
         work = {"bytes": precompute_bytes(out, inp, r)}
     else:
-        raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M or precompute:out,in,r)")
+        raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M, gateup:out,in,r,M or "
+                         "precompute:out,in,r)")
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()
@@ -786,7 +819,8 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="run only the captured decode step (for kernel-profiler launch lists)")
     ap.add_argument("--case", default=None,
-                    help="time one call instead: linear:out,in,r,M or precompute:out,in,r (profiler captures)")
+                    help="time one call instead: linear:out,in,r,M, gateup:out,in,r,M or precompute:out,in,r "
+                         "(profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
