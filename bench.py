@@ -16,6 +16,8 @@ on Gemma-3-1B shapes (r = 64, M = 8192) and on the 31B-class projection (21504 x
 r = 128, M = 8192); W_eff precompute GB/s over the 60-layer 31B-class stack with G = 4.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+--sweep times the rank/shape sweep (gate-like and down-like projections, r = 0..256,
+M = 1..4096) against the roofline; --case times one call for profiler captures.
 """
 from __future__ import annotations
 
@@ -555,28 +557,38 @@ def extras(result, args, dist, stack, device, pk):
     ys = {f: torch.empty(M, o, dtype=torch.bfloat16, device=device) for f, (o, _) in FAMS.items()}
     ws = torch.zeros(max(aq.aq_linear_workspace_bytes([layers[0]["q_proj"], layers[0]["k_proj"],
                                                         layers[0]["v_proj"]], M),
+                         aq.aq_linear_workspace_bytes([layers[0]["gate_proj"], layers[0]["up_proj"]], M),
                          aq.aq_linear_workspace_bytes(layers[0]["down_proj"], M)), dtype=torch.uint8, device=device)
 
-    def prefill_layer(ths):
+    def prefill_layer(ths, fuse_gateup):
         aq.aq_linear_qkv([ths["q_proj"], ths["k_proj"], ths["v_proj"]], xs[1152],
                          ys=[ys["q_proj"], ys["k_proj"], ys["v_proj"]], workspace=ws)
         aq.aq_linear(ths["o_proj"], xs[1024], y=ys["o_proj"], workspace=ws)
-        aq.aq_linear(ths["gate_proj"], xs[1152], y=ys["gate_proj"], workspace=ws)
-        aq.aq_linear(ths["up_proj"], xs[1152], y=ys["up_proj"], workspace=ws)
+        if fuse_gateup:
+            aq.aq_linear_multi([ths["gate_proj"], ths["up_proj"]], xs[1152], ys=[ys["gate_proj"], ys["up_proj"]],
+                               workspace=ws)
+        else:
+            aq.aq_linear(ths["gate_proj"], xs[1152], y=ys["gate_proj"], workspace=ws)
+            aq.aq_linear(ths["up_proj"], xs[1152], y=ys["up_proj"], workspace=ws)
         aq.aq_linear(ths["down_proj"], xs[6912], y=ys["down_proj"], workspace=ws)
 
     flops_layer = sum(linear_flops(o, i, r, M) for o, i in FAMS.values())
-    for ths in layers:
-        prefill_layer(ths)
-    torch.cuda.synchronize()
-    gp = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gp):
+    pre = {}
+    # the pages' production-path form (Q/K/V and gate/up batched), then gate and up apart
+    for key, fuse in (("gemma3_1b_M8192_r64", True), ("gemma3_1b_M8192_r64_gateup_separate", False)):
         for ths in layers:
-            prefill_layer(ths)
-    t = time_graph(gp, max(3, args.steps))
-    tf = nl * flops_layer / (t * 1e-3) / 1e12
-    pre = {"gemma3_1b_M8192_r64": {"TFLOP_s": round(tf, 1), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-                                   "ms_per_layer": round(t / nl, 4), "flops_per_layer": flops_layer}}
+            prefill_layer(ths, fuse)
+        torch.cuda.synchronize()
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp):
+            for ths in layers:
+                prefill_layer(ths, fuse)
+        t = time_graph(gp, max(3, args.steps))
+        tf = nl * flops_layer / (t * 1e-3) / 1e12
+        pre[key] = {"TFLOP_s": round(tf, 1), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                    "ms_per_layer": round(t / nl, 4), "flops_per_layer": flops_layer,
+                    "calls_per_layer": 4 if fuse else 5}
+        del gp
     # per family at M = 8192 (gate is the largest)
     fam_t = {}
     for f in ("gate_proj", "down_proj", "o_proj"):
@@ -590,7 +602,7 @@ def extras(result, args, dist, stack, device, pk):
         fam_t[f] = {"TFLOP_s": round(fl / (tt * 1e-3) / 1e12, 1), "us": round(tt * 1e3, 2)}
         del gf
     pre["gemma3_1b_M8192_r64"]["per_family"] = fam_t
-    del gp, layers, xs, ys, ws
+    del layers, xs, ys, ws
     torch.cuda.empty_cache()
 
     # ---- 31B-class projection at M = 8192 (r = 128) ----
@@ -786,6 +798,65 @@ def run_case(args, dist: Dist):
     return res
 
 
+SWEEP_SHAPES = {"gate-like": (6912, 1152), "down-like": (1152, 6912)}
+SWEEP_RANKS = (0, 4, 16, 64, 256)
+SWEEP_MS = (1, 8, 64, 512, 4096)
+SWEEP_COPIES = 16   # W0 copies per point: 255 MB, about twice the L2
+
+
+def run_sweep(args, dist: Dist):
+    """The rank/shape sweep on gate-like and down-like projections (50 points): per point
+    the average time of one aq_linear call in a graph of SWEEP_COPIES back-to-back calls,
+    each on its own copy of W0 (L2-cold), the path the dispatcher took, and the fraction of
+    the roofline time T* = max(B / HBM, F / bf16 peak) on the measured peaks."""
+    import torch
+    import rank_weight_reconstruction_gb300 as aq
+    from rank_weight_reconstruction_gb300 import Theta, build_lib
+
+    if dist.rank != 0:
+        return None
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    aq.load()
+    pk = peaks()
+    names = {aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_PREFILL: "gemm"}
+    points = []
+    for sname, (out, inp) in SWEEP_SHAPES.items():
+        xs = {M: dev_bits(synth.make_x(("sweep", M, inp), M, inp), device)[:, :inp] for M in SWEEP_MS}
+        for r in SWEEP_RANKS:
+            th = synth.make_theta(("sweep", out, inp, r), out, inp, r)
+            w0 = dev_bits(th.W0, device)
+            s_ = dev_bits(th.s, device)
+            U, V = (dev_bits(th.U, device), dev_bits(th.V, device)) if r else (None, None)
+            thetas = [Theta(W0=(w0 if c == 0 else w0.clone())[:, :inp], s=s_, U=U[:, :r] if r else None,
+                            V=V[:, :r] if r else None) for c in range(SWEEP_COPIES)]
+            for M in SWEEP_MS:
+                x = xs[M]
+                y = torch.empty(M, out, dtype=torch.bfloat16, device=device)
+                ws = aq.new_workspace(aq.aq_linear_workspace_bytes(thetas[0], M), device)
+                for T in thetas:
+                    aq.aq_linear(T, x, y=y, workspace=ws)
+                path = names.get(aq.aq_last_path(), str(aq.aq_last_path()))
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for T in thetas:
+                        aq.aq_linear(T, x, y=y, workspace=ws)
+                us = time_graph(g, max(3, min(args.steps, 20))) * 1e3 / SWEEP_COPIES
+                del g
+                B, F = linear_bytes(out, inp, r, M), linear_flops(out, inp, r, M)
+                t_star = max(B / (pk["hbm_gbs"] * 1e9), F / (pk["bf16_tflops"] * 1e12)) * 1e6
+                points.append({"shape": sname, "out": out, "in": inp, "r": r, "M": M, "path": path,
+                               "us": round(us, 3), "GB_s": round(B / us * 1e-3, 1), "TFLOP_s": round(F / us * 1e-6, 1),
+                               "bound": "hbm" if B / (pk["hbm_gbs"] * 1e9) >= F / (pk["bf16_tflops"] * 1e12)
+                               else "tensor", "frac_roofline": round(t_star / us, 4)})
+            del thetas, w0
+            torch.cuda.empty_cache()
+    return {"sweep": "rank/shape sweep, gate-like 6912x1152 and down-like 1152x6912", "peaks": pk,
+            "copies_per_point": SWEEP_COPIES, "status": aq.aq_device_status(), "points": points}
+
+
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
@@ -818,6 +889,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", action="store_true",
                     help="run only the captured decode step (for kernel-profiler launch lists)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the rank/shape sweep (gate-like and down-like, r in 0..256, M in 1..4096)")
     ap.add_argument("--case", default=None,
                     help="time one call instead: linear:out,in,r,M, gateup:out,in,r,M or precompute:out,in,r "
                          "(profiler captures)")
@@ -829,6 +902,8 @@ def main():
         res = run_reference(args, dist)
     elif args.case:
         res = run_case(args, dist)
+    elif args.sweep:
+        res = run_sweep(args, dist)
     else:
         res = run_ours(args, dist)
     if dist.rank == 0 and res is not None:
