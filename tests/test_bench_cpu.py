@@ -1,0 +1,59 @@
+"""The benchmark's work accounting, on the CPU: the algorithmic bytes and flops of a call
+are the survey's formulas, a batched call reads its shared x once, and the decode step is
+the sum of its calls."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_linear_bytes_and_flops_by_hand():
+    out, inp, r, M = 6912, 1152, 16, 4
+    # W0, U, V, s, x, y in bf16
+    by_hand = 2 * (out * inp + out * r + inp * r + out + M * inp + M * out)
+    assert bench.linear_bytes(out, inp, r, M) == by_hand
+    # the shared-block product, the down and up projections, and the scale
+    assert bench.linear_flops(out, inp, r, M) == 2 * M * out * inp + 2 * M * inp * r + 2 * M * r * out + M * out
+
+
+def test_batched_calls_read_x_once():
+    r, M = 16, 16
+    gate, up = bench.FAMS["gate_proj"], bench.FAMS["up_proj"]
+    two_calls = bench.linear_bytes(*gate, r, M) + bench.linear_bytes(*up, r, M)
+    assert bench.gate_up_bytes(r, M) == two_calls - 2 * M * gate[1]
+    q, k, v = (bench.FAMS[f] for f in ("q_proj", "k_proj", "v_proj"))
+    three_calls = sum(bench.linear_bytes(*s, r, M) for s in (q, k, v))
+    assert bench.qkv_bytes([q, k, v], r, M) == three_calls - 2 * 2 * M * q[1]
+
+
+def test_step_is_the_sum_of_its_calls():
+    per_pass = {M: sum(bench.call_bytes(kind, M) for kind in ("qkv", "o_proj", "gate_up", "down_proj"))
+                for M in bench.DECODE_MS}
+    assert bench.step_bytes() == bench.LAYERS * sum(per_pass.values())
+    # the separate-call step reads the MLP input once more per layer and pass
+    extra = bench.LAYERS * sum(2 * M * bench.FAMS["gate_proj"][1] for M in bench.DECODE_MS)
+    assert bench.step_bytes(fuse_gateup=False) - bench.step_bytes() == extra
+
+
+def test_sweep_grid_covers_both_paths():
+    assert len(bench.SWEEP_SHAPES) * len(bench.SWEEP_RANKS) * len(bench.SWEEP_MS) == 50
+    # below and above the decode kernel's token limit, and ranks from none to 256
+    assert min(bench.SWEEP_MS) <= 32 < max(bench.SWEEP_MS)
+    assert 0 in bench.SWEEP_RANKS and max(bench.SWEEP_RANKS) == 256
+    # each point's W0 copies together exceed the 126 MB L2 of the part
+    for out, inp in bench.SWEEP_SHAPES.values():
+        assert bench.SWEEP_COPIES * out * inp * 2 > 126 * 2**20
+
+
+def test_roofline_time_takes_the_larger_bound():
+    hbm, pk = 6801.3e9, 1970.5e12
+    for (out, inp), r, M in (((6912, 1152), 16, 1), ((6912, 1152), 64, 4096)):
+        B, F = bench.linear_bytes(out, inp, r, M), bench.linear_flops(out, inp, r, M)
+        t_star = max(B / hbm, F / pk)
+        assert t_star == (B / hbm if M == 1 else F / pk)
+    assert np.isclose(pk / hbm, 289.7, rtol=1e-3)   # the ridge, in flops per byte
