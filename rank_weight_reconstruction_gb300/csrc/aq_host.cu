@@ -267,9 +267,34 @@ struct WsLayout {
   int64_t ldvt = 0;
   size_t decode_scratch = 0;
   size_t prefill_scratch = 0;
-  size_t total = 0;
+  size_t total = 0;              // what a call needs at least
   bool any_r = false;
+  // split K (prefill with few output tiles over a deep K): fp32 partial sums after the rest,
+  // per slice [M][ld_pz] of W0 x (family j at column pz_col[j]) then [M][ld_t] of x V
+  int64_t ld_pz = 0;
+  int64_t pz_col[kMaxSeg] = {};
+  size_t split_base = 0;
+  size_t split_slice = 0;        // bytes per slice
+  int32_t split_max = 1;         // slices the preferred size holds
+  size_t total_split = 0;        // preferred size: total plus split_max slices of partials
 };
+
+// Most SMs of any sm_103 part, for sizing the split partials without querying a device.
+constexpr int kSplitSmsBound = 192;
+
+// The most K slices any sm_103 part would take for this call (see the planner in
+// linear_impl): only calls whose fewest possible output tiles fill at most half of the SMs.
+int split_bound(const aq_theta* const* th, int n, int64_t M) {
+  for (int j = 0; j < n; ++j)
+    if (th[j]->r > kSplitMaxRank) return 1;
+  const int64_t nkb = ceil_div(th[0]->in, kBK);
+  const int64_t tok_tiles = ceil_div(M, kMmaM);
+  int64_t min_tiles = 0;
+  for (int j = 0; j < n; ++j) min_tiles += tok_tiles * ceil_div(th[j]->out, 256);
+  if (min_tiles * 2 > kSplitSmsBound || nkb < 2 * kSplitMinKb) return 1;
+  const int64_t sp = std::min<int64_t>({kMaxSplit, nkb / kSplitMinKb, kSplitSmsBound / min_tiles});
+  return sp >= 2 ? static_cast<int>(sp) : 1;
+}
 
 WsLayout ws_layout(const aq_theta* const* th, int n, int64_t M) {
   WsLayout w;
@@ -290,6 +315,15 @@ WsLayout ws_layout(const aq_theta* const* th, int n, int64_t M) {
     w.prefill_scratch = off + static_cast<size_t>(round_up(w.ld_t * w.ldvt * 2, 256));
   }
   if (M <= kDecodeMaxM || w.any_r) w.total = kSyncBytes + std::max(w.decode_scratch, w.prefill_scratch);
+  w.total_split = w.total;
+  for (int j = 0; j < n; ++j) {
+    w.pz_col[j] = w.ld_pz;
+    w.ld_pz += round_up(th[j]->out, 4);
+  }
+  w.split_max = split_bound(th, n, M);
+  w.split_base = static_cast<size_t>(round_up(static_cast<int64_t>(w.total), 256));
+  w.split_slice = static_cast<size_t>(M) * static_cast<size_t>(w.ld_pz + (w.any_r ? w.ld_t : 0)) * 4u;
+  if (w.split_max > 1) w.total_split = w.split_base + static_cast<size_t>(w.split_max) * w.split_slice;
   return w;
 }
 
@@ -374,7 +408,9 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
       theta_spans(th[j], ins + ni);
       ni += 4;
     }
-    Span wsp = span(wl.total ? ws : nullptr, 1, static_cast<int64_t>(wl.total / 2), static_cast<int64_t>(wl.total / 2), "workspace");
+    // the bytes this call may touch: what it needs, and the split partials the workspace holds
+    const size_t ws_touch = ws ? std::max(wl.total, std::min(ws_bytes, wl.total_split)) : 0;
+    Span wsp = span(ws_touch ? ws : nullptr, 1, static_cast<int64_t>(ws_touch / 2), static_cast<int64_t>(ws_touch / 2), "workspace");
     for (int j = 0; j < n; ++j) {
       Span yj = span(ys[j], M, th[j]->out, ldys[j], "y");
       for (int i = 0; i < ni; ++i)
@@ -640,12 +676,39 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
   gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
   gp.n_mma = gp.row_tile;
+  // Split K: when the output tiles fill at most half of the SMs and K is deep, the K of every
+  // tile is cut into slices that separate CTAs sum into fp32 partials (no scale, no rank-r
+  // part), and a small kernel finishes y = RN(s * sum z + U * sum t). The slices stop where
+  // the caller's workspace does.
+  const int64_t nkb = ceil_div(K, kBK);
+  int64_t main_tiles = 0;
+  for (int j = 0; j < n; ++j) main_tiles += gp.n_tok_tiles * ceil_div(th[j]->out, gp.row_tile);
+  int split = 1;
+  int max_r = 0;
+  for (int j = 0; j < n; ++j) max_r = std::max(max_r, th[j]->r);
+  if (main_tiles * 2 <= dev->sms && nkb >= 2 * kSplitMinKb && max_r <= kSplitMaxRank && ws &&
+      (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && wl.split_slice > 0) {
+    // as many slices as keep all tiles (the t tiles included) within one wave
+    const size_t room = ws_bytes > wl.split_base ? ws_bytes - wl.split_base : 0;
+    const int64_t tiles = main_tiles + (wl.any_r ? gp.n_tok_tiles * ceil_div(wl.ld_t, gp.row_tile) : 0);
+    const int64_t sp = std::min<int64_t>({dev->sms / tiles, nkb / kSplitMinKb, kMaxSplit, wl.split_max,
+                                          static_cast<int64_t>(room / wl.split_slice)});
+    if (sp >= 2) split = static_cast<int>(sp);
+  }
+  int kb_per = static_cast<int>(nkb);
+  if (split > 1) {
+    kb_per = static_cast<int>(ceil_div(nkb, split));
+    split = static_cast<int>(ceil_div(nkb, kb_per));   // every slice holds at least one k block
+  }
+  float* const pz_base = split > 1 ? reinterpret_cast<float*>(wsb + wl.split_base) : nullptr;
+  float* const pt_base = split > 1 ? pz_base + static_cast<int64_t>(split) * M * wl.ld_pz : nullptr;
   // CTA pairs (2-SM MMAs, M = 256) on adjacent token tiles: each CTA holds half of the N
   // rows of B, so a stage is 32 KB instead of 48 and shared memory moves a third less per
   // MMA, which bounds this GEMM. Pairs need two token tiles and one CTA per SM; each half of
   // B is a whole number of 8-row swizzle atoms.
   size_t smem = 0;
-  for (int cl = (gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1; cl >= 1; --cl) {
+  for (int cl = (split == 1 && gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1; cl >= 1;
+       --cl) {
     gp.cluster = cl;
     gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + (gp.n_mma / cl) * 128, 1024));
     gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack + kYStageTotal);
@@ -657,7 +720,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   // t = x V as the first tiles of the same launch, when the sync region holds a flag per
   // token tile; otherwise as a GEMM launch of its own before it
   const int64_t n_flags = static_cast<int64_t>(gp.n_tok_units) * gp.cluster;
-  const bool fused_t = wl.any_r && 1 + n_flags <= static_cast<int64_t>(kSyncBytes / 4);
+  const bool fused_t = wl.any_r && (split > 1 || 1 + n_flags <= static_cast<int64_t>(kSyncBytes / 4));
 
   if (wl.any_r) {
     // V^T into the workspace: the t tiles read it K-major
@@ -735,9 +798,17 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     s.n_mma = static_cast<int32_t>(std::min<int64_t>(round_up(wl.ld_t, 16), gp.row_tile));
     s.tile_begin = tiles;
     tiles += s.n_row_tiles * gp.n_tok_units;
-    gp.t_need = s.n_row_tiles;
-    gp.t_flags = reinterpret_cast<int32_t*>(wsb);
-    gp.n_flags = static_cast<int32_t>(n_flags);
+    if (split > 1) {
+      // partial sums of t; nothing in this launch waits for them (the families' tiles have no
+      // rank-r part), so no flags. t_seg stays set: V^T comes from the previous kernel.
+      s.y = nullptr;
+      s.part = pt_base;
+      s.ld_part = wl.ld_t;
+    } else {
+      gp.t_need = s.n_row_tiles;
+      gp.t_flags = reinterpret_cast<int32_t*>(wsb);
+      gp.n_flags = static_cast<int32_t>(n_flags);
+    }
   }
   for (int j = 0; j < n; ++j) {
     GemmSeg& s = gp.seg[gp.nseg++];
@@ -756,23 +827,73 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     // bulk tensor stores of y need whole 64-column boxes per tile: a partial box would write
     // into the next tile's columns (the tensor map clips only at the family's last row)
     s.tma_y = gp.row_tile % 64 == 0 ? 1 : 0;
+    if (split > 1) {   // fp32 partials of W0 x; s and U t are the finalize kernel's
+      s.s = nullptr;
+      s.y = nullptr;
+      s.r = 0;
+      s.tma_y = 0;
+      s.part = pz_base + wl.pz_col[j];
+      s.ld_part = wl.ld_pz;
+    }
     if (s.tma_y && (st = tmap_2d(&s.tm_y, ys[j], th[j]->out, M, ldys[j], 32, "y")) != AQ_OK) return st;
     s.tile_begin = tiles;
     tiles += s.n_row_tiles * gp.n_tok_units;
   }
-  gp.total_tiles = tiles;
+  gp.total_tiles = tiles * split;
+  gp.ksplit = split;
+  gp.kb_per = kb_per;
   gp.prefetch_w = 1;
   gp.head_kb = kGemmHeadKb;
   gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);   // two accumulator buffers
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;
-  const int grid = gp.cluster > 1 ? 2 * std::min(tiles, dev->gemm_pairs) : std::min(tiles, dev->sms);
+  const int grid = gp.cluster > 1 ? 2 * std::min(tiles, dev->gemm_pairs) : std::min(gp.total_tiles, dev->sms);
   if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK) return st;
+  if (split > 1) {
+    FinalizeParams fp = {};
+    fp.nseg = n;
+    fp.M = static_cast<int32_t>(M);
+    fp.ksplit = split;
+    fp.ld_pz = wl.ld_pz;
+    fp.ld_pt = wl.ld_t;
+    fp.pz_slice = M * wl.ld_pz;
+    fp.pt_slice = M * wl.ld_t;
+    int blocks = 0;
+    for (int j = 0; j < n; ++j) {
+      FinalizeSeg& f = fp.seg[j];
+      f.pz = pz_base + wl.pz_col[j];
+      f.pt = th[j]->r > 0 ? pt_base + wl.t_col[j] : nullptr;
+      f.s = static_cast<const uint16_t*>(th[j]->s);
+      f.U = static_cast<const uint16_t*>(th[j]->U);
+      f.ldu = th[j]->ld_u;
+      f.y = static_cast<uint16_t*>(ys[j]);
+      f.ldy = ldys[j];
+      f.rows = th[j]->out;
+      f.r = th[j]->r;
+      f.block_begin = blocks;
+      blocks += static_cast<int>(ceil_div(th[j]->out, kFinRows));
+    }
+    if ((st = launch_or_fail(launch_finalize(fp, blocks, cs, true), "launch split-K finalize")) != AQ_OK) return st;
+  }
   t_last_path = AQ_PATH_PREFILL;
   return AQ_OK;
 }
 
 }  // namespace
+
+namespace aq {
+size_t linear_workspace_min_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
+}  // namespace aq
+
+size_t aq::linear_workspace_min_bytes(const aq_theta* th, int32_t n_theta, int64_t M) {
+  if (!th || n_theta < 1 || n_theta > AQ_MAX_FAMILIES || M < 0) return static_cast<size_t>(-1);
+  const aq_theta* ptrs[kMaxSeg];
+  for (int j = 0; j < n_theta; ++j) {
+    if (th[j].r < 0 || th[j].r > AQ_MAX_RANK || th[j].in < 1) return static_cast<size_t>(-1);
+    ptrs[j] = &th[j];
+  }
+  return ws_layout(ptrs, n_theta, M).total;
+}
 
 int aq::set_last_error(int status, const char* message) {
   t_err = message ? message : "";
@@ -791,7 +912,7 @@ size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M)
     if (th[j].r < 0 || th[j].r > AQ_MAX_RANK || th[j].in < 1) return static_cast<size_t>(-1);
     ptrs[j] = &th[j];
   }
-  return ws_layout(ptrs, n_theta, M).total;
+  return ws_layout(ptrs, n_theta, M).total_split;
 }
 
 aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y, int64_t ldy,

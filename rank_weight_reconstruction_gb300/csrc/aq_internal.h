@@ -36,6 +36,8 @@ struct GemmSeg {
   int32_t tma_y;     // 1: y leaves through shared memory and bulk tensor stores
   int32_t t_seg;     // 1: computes t = x V (row operand V^T from the workspace, written by the
                      //    previous kernel); its tiles publish per-token-tile flags
+  float* part;       // split K: fp32 partial sums [ksplit][M][ld_part] instead of y (no s, r = 0)
+  int64_t ld_part;
 };
 
 // Segments of one prefill GEMM launch: the families, and before them their t = x V parts.
@@ -69,8 +71,45 @@ struct GemmParams {
   int32_t head_kb;      // k blocks of tile i+1 issued before the rank-r blocks of tile i
   int32_t* status;      // device status word
   uint64_t timeout_ns;
+  int32_t ksplit;       // K slices per tile (1: none); work item = unit * ksplit + slice
+  int32_t kb_per;       // k blocks per slice (the last slice may have fewer)
 };
 static_assert(sizeof(GemmParams) <= 4096, "kernel parameters are limited to 4 KB");
+
+// Split-K finalize: y = RN(s * sum_k z_k + U * sum_k t_k) from the fp32 partials of a split
+// GEMM, the slices summed in order.
+struct FinalizeSeg {
+  const float* pz;       // [ksplit][M][ld_pz] partial sums of W0 x for this family's rows
+  const float* pt;       // [ksplit][M][ld_pt] partial sums of x V, at this family's columns
+  const uint16_t* s;     // [rows] bf16
+  const uint16_t* U;     // [rows, ldu] bf16, r columns
+  int64_t ldu;
+  uint16_t* y;
+  int64_t ldy;
+  int32_t rows;
+  int32_t r;
+  int32_t block_begin;   // first blockIdx.x of this family
+};
+struct FinalizeParams {
+  FinalizeSeg seg[kMaxSeg];
+  int32_t nseg;
+  int32_t M;
+  int32_t ksplit;
+  int64_t ld_pz;
+  int64_t ld_pt;
+  int64_t pz_slice;      // elements between slices of pz (M * ld_pz)
+  int64_t pt_slice;
+};
+constexpr int kFinRows = 64;       // outputs per finalize block (one per thread)
+constexpr int kFinTok = 8;         // tokens per finalize block
+constexpr int kFinMaxR = 256;      // largest rank the finalize stages in shared memory
+constexpr int kSplitMinKb = 4;     // k blocks per slice at least
+constexpr int kMaxSplit = 16;
+// Largest rank for which K is split: the finalize sums the slices' partials of t and of W0 x
+// with dependent global loads and runs U t on the FP32 pipes, which pays for itself only at
+// small r (measured on 1152 x 6912 at M = 64 and 512: 1.2-2.5x faster for r <= 16, slower
+// than the unsplit GEMM for r = 64 and 256).
+constexpr int kSplitMaxRank = 16;
 
 // Decode (M <= kDecMaxTok tokens): each W0-streaming CTA owns a contiguous range of
 // output rows of one family over the full K; a few extra CTAs compute t = V^T x.
@@ -207,6 +246,7 @@ constexpr int kGemmHeadKb = 6;
 // columns of bf16 (128-byte swizzled rows), after the ring
 constexpr int kYStageBytes = 32 * 128;
 constexpr int kYStageTotal = 4 * 2 * kYStageBytes;
+cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl);
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);

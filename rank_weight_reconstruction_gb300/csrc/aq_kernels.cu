@@ -174,6 +174,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   const int ncl = static_cast<int>(gridDim.x) / cl;
   const int n_it = cid < p.total_tiles ? (p.total_tiles - 1 - cid) / ncl + 1 : 0;
   auto tile_of = [&](int it) { return cid + it * ncl; };
+  // Work item it of this CTA: a unit's tile and one slice of its K (split K), or all of K.
+  // Zero-initialised parameters mean no split.
+  const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
+  const int kb_per = p.ksplit > 1 ? p.kb_per : nkb_main;
+  struct Item {
+    TileCoord tc;
+    int ks, kb_lo, nkb;
+  };
+  auto item_of = [&](int it) {
+    const int w = tile_of(it);
+    Item m;
+    m.ks = w % ksplit;
+    m.tc = tile_coord(p, w / ksplit, crank);
+    m.kb_lo = m.ks * kb_per;
+    m.nkb = min(kb_per, nkb_main - m.kb_lo);
+    return m;
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -213,27 +230,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       };
       // the row operand of the first tile may be loaded before the previous grid completes
       // only when it is a weight (V^T of a t tile is written by the previous kernel)
-      const bool pre_w = p.prefetch_w && n_it > 0 && !p.seg[tile_coord(p, tile_of(0), crank).seg].t_seg;
+      const bool pre_w = p.prefetch_w && n_it > 0 && !p.seg[item_of(0).tc.seg].t_seg;
       if (!pre_w) pdl_wait_prior_grid();
       for (int it = 0; ok && it <= n_it; ++it) {
-        const int h = it == 0 ? nkb_main : min(p.head_kb, nkb_main);   // head k blocks of tile it
+        const Item cur = it < n_it ? item_of(it) : Item{};
+        const int h = it == 0 ? cur.nkb : min(p.head_kb, cur.nkb);   // head k blocks of item it
         if (it < n_it) {
-          const TileCoord tc = tile_coord(p, tile_of(it), crank);
+          const TileCoord tc = cur.tc;
           const GemmSeg& sg = p.seg[tc.seg];
           int kb = 0;
           if (it == 0 && pre_w) {
             // Weight tiles of the first stages go out before waiting on the previous grid.
-            const int pre = nkb_main < p.stages ? nkb_main : p.stages;
+            const int pre = cur.nkb < p.stages ? cur.nkb : p.stages;
             for (; kb < pre; ++kb) {
               uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
               if (leader) mbar_arrive_expect_tx(&full[kb], tx_bytes);
-              load_rows(st, &sg.tm_w, kb, tc.row0, sg.n_mma, &full[kb]);
+              load_rows(st, &sg.tm_w, cur.kb_lo + kb, tc.row0, sg.n_mma, &full[kb]);
               filled |= 1u << kb;
             }
             pdl_wait_prior_grid();
             for (int j = 0; j < pre; ++j) {
               uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-              load(st, &p.tm_x, j * kBK, tc.tok0, &full[j]);
+              load(st, &p.tm_x, (cur.kb_lo + j) * kBK, tc.tok0, &full[j]);
             }
             stage = pre;
             if (stage == p.stages) {
@@ -241,10 +259,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
               phase ^= 1;
             }
           }
-          for (; ok && kb < h; ++kb) ok = push(tc, sg, false, kb);
+          for (; ok && kb < h; ++kb) ok = push(tc, sg, false, cur.kb_lo + kb);
         }
         if (ok && it >= 1) {
-          const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
+          const TileCoord tc = item_of(it - 1).tc;
           const GemmSeg& sg = p.seg[tc.seg];
           const int nkb_low = sg.r > 0 ? ceil_div_i(sg.r, kBK) : 0;
           if (nkb_low > 0 && p.t_flags) {
@@ -265,9 +283,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           for (int kb = 0; ok && kb < nkb_low; ++kb) ok = push(tc, sg, true, kb);
         }
         if (ok && it >= 1 && it < n_it) {
-          const TileCoord tc = tile_coord(p, tile_of(it), crank);
-          const GemmSeg& sg = p.seg[tc.seg];
-          for (int kb = h; ok && kb < nkb_main; ++kb) ok = push(tc, sg, false, kb);
+          const GemmSeg& sg = p.seg[cur.tc.seg];
+          for (int kb = h; ok && kb < cur.nkb; ++kb) ok = push(cur.tc, sg, false, cur.kb_lo + kb);
         }
       }
       if (!ok && leader) {
@@ -327,16 +344,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     // per use (bit b for buffer b), not per tile
     uint32_t lr_phase = 0;
     for (int it = 0; ok && it <= n_it; ++it) {   // (the odd CTA of a pair issues nothing)
-      const int h = it == 0 ? nkb_main : min(p.head_kb, nkb_main);
+      const Item cur = it < n_it ? item_of(it) : Item{};
+      const int h = it == 0 ? cur.nkb : min(p.head_kb, cur.nkb);
       if (it < n_it) {
         const uint32_t b = it & 1;
         if (!warp_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, ctl)) break;
         tc_fence_after();
-        const TileCoord tc = tile_coord(p, tile_of(it), crank);
-        ok = run(0, h, 0, b, 0u, idesc_bf16_f32(mma_m, p.seg[tc.seg].n_mma));
+        ok = run(0, h, 0, b, 0u, idesc_bf16_f32(mma_m, p.seg[cur.tc.seg].n_mma));
       }
       if (ok && it >= 1) {
-        const TileCoord tc = tile_coord(p, tile_of(it - 1), crank);
+        const TileCoord tc = item_of(it - 1).tc;
         const GemmSeg& sg = p.seg[tc.seg];
         if (sg.r > 0) {
           const uint32_t b = (it - 1) & 1;
@@ -350,8 +367,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       }
       if (ok && it < n_it) {
         const uint32_t b = it & 1;
-        const TileCoord tc = tile_coord(p, tile_of(it), crank);
-        ok = run(h, nkb_main, 0, b, 1u, idesc_bf16_f32(mma_m, p.seg[tc.seg].n_mma));
+        ok = run(h, cur.nkb, 0, b, 1u, idesc_bf16_f32(mma_m, p.seg[cur.tc.seg].n_mma));
         if (ok && lane == 0) commit_all(&acc_full[b]);
         __syncwarp();
       }
@@ -388,7 +404,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     pdl_wait_prior_grid();
     uint32_t lr_phase = 0;   // phases of acc_done[b] (bit b), advanced per rank-r use
     for (int it = 0; it < n_it; ++it) {
-      const TileCoord tc = tile_coord(p, tile_of(it), crank);
+      const Item itm = item_of(it);
+      const TileCoord tc = itm.tc;
       const GemmSeg& sg = p.seg[tc.seg];
       const bool has_lr = sg.r > 0;
       const uint32_t b = it & 1;
@@ -471,6 +488,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       }
       const int tok = tc.tok0 + et;
       const bool tok_ok = tok < p.M;
+      if (sg.part) {
+        // split K: this slice's raw fp32 sums (no scale, no rank-r part), summed in order
+        // and finished by the finalize kernel; ld_part and the columns are multiples of 4
+        float* prow = sg.part + (static_cast<int64_t>(itm.ks) * p.M + (tok_ok ? tok : 0)) * sg.ld_part;
+        for (int c = 0; c < sg.n_mma; c += 16) {
+          float v[16];
+          tmem_ld_16(acc + c, v);
+          tmem_ld_wait();
+          const int o0 = tc.row0 + c;
+          if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
+          if ((c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows)) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(prow + o0 + 4 * q4) =
+                  make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < p.row_tile && o0 + j < sg.rows) prow[o0 + j] = v[j];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_lead(&acc_empty[b]);
+        continue;
+      }
       uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
       for (int c = 0; c < sg.n_mma; c += 16) {
         float v[16];
@@ -546,6 +589,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   }
   if constexpr (kPair) cluster_sync_all();
 }
+// ------------------------------------------------------------------------------------
+// Split-K finalize: y[m, o] = RN(s[o] * sum_k z_k[m, o] + sum_j U[o, j] * t[m, j]) with
+// t[m, j] = sum_k t_k[m, j], every sum over the slices in slice order (deterministic).
+// One thread per output row, kFinTok tokens per block; U t on the FP32 pipes (at most
+// r FMAs per output, a small fraction of the GEMM's work at the shapes that split).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFinRows) aq_finalize_kernel(const __grid_constant__ FinalizeParams p) {
+  __shared__ float ts[kFinTok][kFinMaxR];
+  int si = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxSeg; ++j)
+    if (j < p.nseg && static_cast<int>(blockIdx.x) >= p.seg[j].block_begin) si = j;
+  const FinalizeSeg& sg = p.seg[si];
+  const int o = (static_cast<int>(blockIdx.x) - sg.block_begin) * kFinRows + static_cast<int>(threadIdx.x);
+  const int m0 = static_cast<int>(blockIdx.y) * kFinTok;
+  pdl_wait_prior_grid();   // the partial sums are the previous grid's output
+  for (int idx = threadIdx.x; idx < kFinTok * sg.r; idx += kFinRows) {
+    const int mm = idx / sg.r, k = idx - mm * sg.r;
+    float v = 0.0f;
+    if (m0 + mm < p.M)
+      for (int ks = 0; ks < p.ksplit; ++ks) v += sg.pt[ks * p.pt_slice + static_cast<int64_t>(m0 + mm) * p.ld_pt + k];
+    ts[mm][k] = v;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (o >= sg.rows) return;
+  float acc[kFinTok];
+#pragma unroll
+  for (int mm = 0; mm < kFinTok; ++mm) acc[mm] = 0.0f;
+  if (sg.r > 0) {
+    // U row o in 16-byte pieces (U is 16-byte aligned with ld_u a multiple of 8); the piece
+    // that would pass r is read element by element, so no read leaves the row's r values
+    const uint16_t* urow = sg.U + static_cast<int64_t>(o) * sg.ldu;
+    const int r8 = sg.r & ~7;
+#pragma unroll 2
+    for (int k0 = 0; k0 < r8; k0 += 8) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(urow + k0));
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float u0 = __uint_as_float(ww[e] << 16), u1 = __uint_as_float(ww[e] & 0xFFFF0000u);
+#pragma unroll
+        for (int mm = 0; mm < kFinTok; ++mm) {
+          acc[mm] = fmaf(u0, ts[mm][k0 + 2 * e], acc[mm]);
+          acc[mm] = fmaf(u1, ts[mm][k0 + 2 * e + 1], acc[mm]);
+        }
+      }
+    }
+    for (int k = r8; k < sg.r; ++k) {
+      const float u = bf16_to_f32(urow[k]);
+#pragma unroll
+      for (int mm = 0; mm < kFinTok; ++mm) acc[mm] = fmaf(u, ts[mm][k], acc[mm]);
+    }
+  }
+  const float sc = sg.s ? bf16_to_f32(sg.s[o]) : 1.0f;
+#pragma unroll
+  for (int mm = 0; mm < kFinTok; ++mm) {
+    const int m = m0 + mm;
+    if (m < p.M) {
+      float z = 0.0f;
+      for (int ks = 0; ks < p.ksplit; ++ks) z += sg.pz[ks * p.pz_slice + static_cast<int64_t>(m) * p.ld_pz + o];
+      sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, z, acc[mm]));
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // V [in, r] -> V^T [r, in]
 // ------------------------------------------------------------------------------------
@@ -904,6 +1013,12 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel<true>), &cfg);
+}
+
+cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl) {
+  void* args[] = {const_cast<FinalizeParams*>(&p)};
+  const dim3 grid(blocks, (p.M + kFinTok - 1) / kFinTok);
+  return launch_ex(reinterpret_cast<const void*>(&aq_finalize_kernel), grid, dim3(kFinRows), 0, st, pdl, args);
 }
 
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl) {

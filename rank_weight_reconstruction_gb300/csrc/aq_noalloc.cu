@@ -22,6 +22,12 @@
 // (its first AQ_WORKSPACE_SYNC_BYTES) needs; every completed call leaves that part zero.
 static __device__ __align__(256) unsigned char aq_noalloc_scratch[AQ_NOALLOC_WORKSPACE_BYTES];
 
+namespace aq {
+// The workspace a call cannot run without (aq_linear_workspace_bytes adds room for optional
+// split-K partial sums, which the scratch holds as far as it goes).
+size_t linear_workspace_min_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
+}  // namespace aq
+
 namespace {
 
 std::mutex g_scratch_mu;
@@ -60,7 +66,7 @@ aq_status scratch_address(void** out) {
 extern "C" aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y,
                                        int64_t ldy, void* stream) {
   if (!th) return static_cast<aq_status>(aq::set_last_error(AQ_ERR_INVALID_ARG, "aq_linear_noalloc: theta is NULL"));
-  const size_t need = aq_linear_workspace_bytes(th, 1, M);
+  const size_t need = aq::linear_workspace_min_bytes(th, 1, M);
   if (need == static_cast<size_t>(-1))  // invalid sizes: let aq_linear's validation name them
     return aq_linear(th, x, M, ldx, y, ldy, nullptr, 0, stream);
   if (need > static_cast<size_t>(AQ_NOALLOC_WORKSPACE_BYTES)) {

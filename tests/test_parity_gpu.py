@@ -324,6 +324,23 @@ def test_rank_sweep(shape, r, M):
 # ----------------------------------------------------------------------------------
 # 31B-class projection: out 21504, in 5376, r 128, M in {1, 32, 8192}
 # ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("r", [0, 5, 64])
+def test_split_k_dispatch(r):
+    """A down-like projection at 64 tokens has 18 output tiles of 64 rows over a K of 6912:
+    up to rank 16 its K is split across CTAs and a finalize kernel sums the slices (one
+    more launch); at rank 64 it stays one GEMM. Both within tolerance of the oracle."""
+    out, inp, M = 1152, 6912, 64
+    th = synth.make_theta(("split", r), out, inp, r)
+    xb = synth.make_x(("split", r), M, inp)
+    y = run_linear(th, xb)
+    assert aq.aq_last_path() == aq.AQ_PATH_PREFILL
+    gemm_launches = 1 if r == 0 else 2             # (V^T transpose,) GEMM
+    split = r <= 16
+    assert aq.aq_last_launch_count() == gemm_launches + (1 if split else 0)
+    assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, inp)), f"r={r}")
+    assert aq.aq_device_status() == aq.AQ_OK
+
+
 @pytest.mark.parametrize("M", [1, 32, 8192])
 def test_31b_projection(M):
     out, inp = synth.CLASS31B_SHAPES["wide"]
