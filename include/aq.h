@@ -95,14 +95,18 @@ typedef struct aq_theta {
  * allocating it), and every call that completes leaves it zero again, so one workspace
  * can serve any sequence of calls, shapes and paths on a stream. The rest is scratch
  * that needs no initialisation (per-CTA partial sums at decode; t in bf16 and a
- * transposed copy of V at prefill). After a call whose bounded wait expired
+ * transposed copy of V at prefill; and, when a prefill call splits K, the fp32 partial
+ * sums of every K slice). After a call whose bounded wait expired
  * (aq_device_status() == AQ_ERR_TIMEOUT) the sync part must be zeroed again. */
 #define AQ_WORKSPACE_SYNC_BYTES (128u * 1024u)
 
-/* Bytes of device workspace aq_linear (n_theta == 1), aq_linear_qkv (n_theta == 3, pass
- * the three bundles) or aq_linear_multi (n_theta == n) needs for M tokens, on either path. Returns 0 if none is
- * needed (M == 0, or M above the decode limit with r == 0) and (size_t)-1 for invalid
- * arguments. */
+/* Bytes of device workspace for aq_linear (n_theta == 1), aq_linear_qkv (n_theta == 3,
+ * pass the three bundles) or aq_linear_multi (n_theta == n) over M tokens, on either path,
+ * including room for the fp32 partial sums of a prefill call that splits K (see aq_linear).
+ * A smaller workspace that still holds the call's minimum is accepted: the call then splits
+ * K into fewer slices, or not at all. Returns 0 if the call needs none and splits nothing
+ * (M == 0, or M above the decode limit with r == 0 and too many output tiles to split), and
+ * (size_t)-1 for invalid arguments. */
 size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M);
 
 /* y[m, o] = RN_bf16( s[o] * sum_i W0[o,i] x[m,i] + sum_k U[o,k] * t[m,k] ),
@@ -112,13 +116,18 @@ size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M)
  *   th        the bundle (host pointer to the struct; the struct's pointers are device)
  *   x         [M, in] device, row stride ldx >= in
  *   y         [M, out] device, row stride ldy >= out; must not overlap x, W0, s, U, V
- *   workspace device, >= aq_linear_workspace_bytes(th, 1, M) bytes, 256-byte aligned,
- *             first AQ_WORKSPACE_SYNC_BYTES zero (see above); NULL when that size is 0
+ *   workspace device, aq_linear_workspace_bytes(th, 1, M) bytes (a smaller one that holds
+ *             the call's minimum also works; the error names that minimum), 256-byte
+ *             aligned, first AQ_WORKSPACE_SYNC_BYTES zero (see above); NULL when no
+ *             workspace is needed
  *   stream    cudaStream_t
  * M == 0 is a no-op returning AQ_OK. Decode (M <= aq_decode_max_m() = 32) is one
- * launch that streams W0 once, split evenly over the SMs; prefill (larger M) runs a
- * tcgen05 GEMM after a small t = x V GEMM. Both fuse s and the rank-r term into the
- * epilogue. Concurrent calls sharing one workspace must be ordered on the GPU. */
+ * launch that streams W0 once, split evenly over the SMs. Prefill (larger M) transposes V
+ * and runs one tcgen05 GEMM whose first tiles compute t = x V. Both fuse s and the rank-r
+ * term into the epilogue. A prefill call whose output tiles fill at most half of the SMs
+ * over a deep K, with r <= 16, instead splits K over more CTAs that write fp32 partial
+ * sums, and a third launch computes y from them in a fixed order. Concurrent calls
+ * sharing one workspace must be ordered on the GPU. */
 aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
                     void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
                     void* stream);
@@ -148,12 +157,13 @@ aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t 
 /* aq_linear for callers that may not allocate device memory. The paper has no
  * counterpart: this entry point exists for callers such as plugins inside a runtime that
  * owns all device memory, or serving loops that forbid allocation after start-up.
- * Same arguments and results as aq_linear, minus the workspace: the scratch it needs
- * (aq_linear_workspace_bytes(th, 1, M) bytes) comes from one array of
- * AQ_NOALLOC_WORKSPACE_BYTES compiled into the library, which every GPU that uses the
- * library keeps allocated until the process exits. The caller still passes x and y.
- *   - A call whose scratch need exceeds AQ_NOALLOC_WORKSPACE_BYTES is rejected with
- *     AQ_ERR_WORKSPACE (message in aq_last_error) before anything is enqueued.
+ * Same arguments and results as aq_linear, minus the workspace: its scratch comes from one
+ * array of AQ_NOALLOC_WORKSPACE_BYTES compiled into the library, which every GPU that uses
+ * the library keeps allocated until the process exits. The caller still passes x and y.
+ *   - A call whose minimum scratch need exceeds AQ_NOALLOC_WORKSPACE_BYTES is rejected
+ *     with AQ_ERR_WORKSPACE (message in aq_last_error) before anything is enqueued. Split-K
+ *     partial sums use what the array has beyond that minimum, so such a call may split K
+ *     into fewer slices than with a full workspace.
  *   - The first call on a device looks up the array's device address on that device;
  *     make that first call before capturing a stream into a CUDA graph.
  *   - All calls on a device share the one array and it keeps the previous call's

@@ -77,6 +77,24 @@ def test_workspace_bytes(lib):
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 2, 8) == ctypes.c_size_t(-1).value
 
 
+def test_workspace_bytes_split_k(lib):
+    """A down-like projection (1152 x 6912) at 64 tokens may split its K (at most 16
+    slices: 108 k blocks, 5 output tiles of 256 rows at the fewest). The workspace then
+    also holds, after the rest, fp32 partial sums per slice: [M][round_up(out, 4)] of W0 x
+    and [M][sum round_up(r, 8)] of x V. Ranks above 16 never split."""
+    sync = binding.AQ_WORKSPACE_SYNC_BYTES
+    M, slices = 64, 16
+    th = _theta(out=1152, inp=6912, r=16, ld_u=16, ld_v=16)
+    base = sync + 64 * 16 * 2 + 16 * 6912 * 2            # t bf16, V^T (both whole 256-B units)
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, M) == base + slices * M * (1152 + 16) * 4
+    th0 = _theta(out=1152, inp=6912, r=0)
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th0), 1, M) == slices * M * 1152 * 4
+    th64 = _theta(out=1152, inp=6912, r=64, ld_u=64, ld_v=64)
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th64), 1, M) == sync + 64 * 64 * 2 + 64 * 6912 * 2
+    # many output tiles (8192 tokens): nothing to split
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th0), 1, 8192) == 0
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(r=257), binding.AQ_ERR_UNSUPPORTED),
     (dict(r=-1), binding.AQ_ERR_SHAPE),
