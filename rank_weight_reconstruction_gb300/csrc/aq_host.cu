@@ -463,9 +463,9 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     dp.xs_ld = static_cast<int32_t>(kp + 8);
     dp.x_res = M * (kp + 8) * 2 <= 64 * 1024 ? 1 : 0;
     {
-      int64_t w0_bytes = 0;
-      for (int j = 0; j < n; ++j) w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
-      dp.l2_prefetch = w0_bytes <= 48ll * 1024 * 1024 ? 1 : 0;   // L2 is 126 MB
+      int64_t call_w0_bytes = 0;
+      for (int j = 0; j < n; ++j) call_w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
+      dp.l2_prefetch = call_w0_bytes <= 48ll * 1024 * 1024 ? 1 : 0;   // L2 is 126 MB
     }
     dp.xres_bytes = dp.x_res ? static_cast<uint32_t>(round_up(M * (kp + 8) * 2, 1024)) : 0u;
     // t = V^T x: computed by every streaming CTA for its own family when that family's V
@@ -684,9 +684,9 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   int64_t main_tiles = 0;
   for (int j = 0; j < n; ++j) main_tiles += gp.n_tok_tiles * ceil_div(th[j]->out, gp.row_tile);
   int split = 1;
-  int max_r = 0;
-  for (int j = 0; j < n; ++j) max_r = std::max(max_r, th[j]->r);
-  if (main_tiles * 2 <= dev->sms && nkb >= 2 * kSplitMinKb && max_r <= kSplitMaxRank && ws &&
+  int call_max_r = 0;
+  for (int j = 0; j < n; ++j) call_max_r = std::max(call_max_r, th[j]->r);
+  if (main_tiles * 2 <= dev->sms && nkb >= 2 * kSplitMinKb && call_max_r <= kSplitMaxRank && ws &&
       (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && wl.split_slice > 0) {
     // as many slices as keep all tiles (the t tiles included) within one wave
     const size_t room = ws_bytes > wl.split_base ? ws_bytes - wl.split_base : 0;
