@@ -18,3 +18,4 @@ from .reconstruction import (  # noqa: F401
     weight_acceptance,
     within_tolerance,
 )
+from .decomposition import band_mean, decompose, decompose_stack, truncated_svd  # noqa: F401
