@@ -1,6 +1,6 @@
-"""The benchmark's work accounting, on the CPU: the algorithmic bytes and flops of a call
-are the survey's formulas, a batched call reads its shared x once, and the decode step is
-the sum of its calls."""
+"""The benchmark's work accounting, on the CPU: a call's algorithmic bytes and flops match
+the formulas written out by hand, a batched call reads its shared x once, and the decode
+step is the sum of its calls."""
 import os
 import sys
 
