@@ -73,6 +73,16 @@ def gate_up_bytes(r, M):
     return linear_bytes(og, ig, r, M) + linear_bytes(ou, iu, r, M) - 2 * M * ig
 
 
+def decode_config():
+    """The headline workload, shared by both arms of the benchmark."""
+    return {"workload": "gemma3-1b-shaped decode stack: 26 layers x 7 projection families "
+                        "(q 1024x1152, k/v 256x1152, o 1152x1024, gate/up 6912x1152, down 1152x6912), "
+                        "r=16, one pass each at M=1,4,16; q/k/v batched via aq_linear_qkv and gate/up via "
+                        "aq_linear_multi (the pages' production-path fusion, 4 calls per layer)",
+            "layers": LAYERS, "rank": DECODE_RANK, "M": list(DECODE_MS),
+            "algorithmic_bytes_per_step": step_bytes()}
+
+
 def step_bytes(fuse_gateup=True):
     """Algorithmic bytes of one decode step. fuse_gateup: gate and up of a layer are one
     batched call (the pages' production path), so their shared x is read once."""
@@ -429,16 +439,11 @@ def run_ours(args, dist: Dist):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded splitmix64 + Box-Muller draws rounded to bf16; W0~N(0,0.02^2), "
                 "s~U(0.9,1.1), U,V~N(0,0.01^2), x~N(0,1); shapes only, no trained weights",
-        "config": {"workload": "gemma3-1b-shaped decode stack: 26 layers x 7 projection families "
-                               "(q 1024x1152, k/v 256x1152, o 1152x1024, gate/up 6912x1152, down 1152x6912), "
-                               "r=16, one pass each at M=1,4,16; q/k/v batched via aq_linear_qkv and gate/up via "
-                               "aq_linear_multi (the pages' production-path fusion, 4 calls per layer)",
-                   "layers": LAYERS, "rank": DECODE_RANK, "M": list(DECODE_MS), "calls_per_step": len(calls),
-                   "algorithmic_bytes_per_step": B,
-                   "w0_storage": "G=1 values, one physical W0 copy per layer (1.40 GB streamed per M pass)",
-                   "l2": "inputs larger than L2 (each pass streams 1.40 GB of W0 against a 129 MB L2)",
-                   "timing": "CUDA graph of the whole step, CUDA events on the replay stream, max over ranks",
-                   "parallelism": f"replicas x{dist.world}"},
+        "config": dict(decode_config(), calls_per_step=len(calls),
+                       w0_storage="G=1 values, one physical W0 copy per layer (1.40 GB streamed per M pass)",
+                       l2="inputs larger than L2 (each pass streams 1.40 GB of W0 against a 129 MB L2)",
+                       timing="CUDA graph of the whole step, CUDA events on the replay stream, max over ranks",
+                       parallelism=f"replicas x{dist.world}"),
         "gpu_launches": launches * args.steps,
         "wall_s_timed": round(wall, 4),
         "peaks": pk,
@@ -871,9 +876,10 @@ def run_reference(args, dist: Dist):
     return {"metric": METRIC, "impl": "reference", "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(B / (v * 1e9) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
-            "config": {"workload": "gemma3-1b-shaped decode stack (26 layers x 7 families, r=16, M=1,4,16): "
-                                   "each step times a bounded sample of whole layers on the host cores",
-                       "parallelism": "host cores"},
+            "config": dict(decode_config(),
+                           timing="each step: the fp64 oracle over a bounded sample of whole layers of the "
+                                  "step on the host cores, host wall clock",
+                           parallelism="host cores"),
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
