@@ -196,10 +196,12 @@ aq_status aq_device_status(void* stream);
  * exits; aq_device_status() then reports it. No fault, trap or hang is involved. */
 aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
 
-/* Path selection for aq_linear / aq_linear_qkv. AQ_PATH_AUTO picks by M (decode
- * kernel for M <= aq_decode_max_m(), prefill kernel above). The other values force a
- * path for tests: prefill works for every M, decode for M <= aq_decode_max_m() (larger M
- * returns AQ_ERR_UNSUPPORTED). Process-wide setting. */
+/* Path selection for aq_linear / aq_linear_qkv / aq_linear_multi. AQ_PATH_AUTO picks by M
+ * and size: the decode kernel for M <= aq_decode_max_m(), except that from 16 tokens a
+ * call whose W0 (summed over its families) holds 128 MB or more takes the prefill GEMM;
+ * the prefill GEMM above. The other values force a path for tests: prefill works for
+ * every M, decode for M <= aq_decode_max_m() (larger M returns AQ_ERR_UNSUPPORTED).
+ * Process-wide setting. */
 typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2 } aq_path;
 aq_status aq_set_path(aq_path path);
 int32_t aq_decode_max_m(void);
