@@ -77,6 +77,18 @@ def test_workspace_bytes(lib):
     assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 2, 8) == ctypes.c_size_t(-1).value
 
 
+def test_workspace_error_names_the_minimum(lib):
+    """The preferred size includes split-K partials. A call is refused only below its
+    minimum, and the message names that minimum. The call is refused before any device
+    access, so the placeholder pointers are never dereferenced."""
+    th = _theta(out=1152, inp=6912, r=16, ld_u=16, ld_v=16)
+    minimum = binding.AQ_WORKSPACE_SYNC_BYTES + 64 * 16 * 2 + 16 * 6912 * 2
+    assert lib.aq_linear_workspace_bytes(ctypes.byref(th), 1, 64) > minimum
+    st = lib.aq_linear(ctypes.byref(th), 0x10000000, 64, 6912, 0x20000000, 1152, 0x30000000, minimum - 256, None)
+    assert st == binding.AQ_ERR_WORKSPACE
+    assert str(minimum) in binding.aq_last_error()
+
+
 def test_workspace_bytes_split_k(lib):
     """A down-like projection (1152 x 6912) at 64 tokens may split its K (at most 16
     slices: 108 k blocks, 5 output tiles of 256 rows at the fewest). The workspace then
