@@ -18,4 +18,4 @@ from .reconstruction import (  # noqa: F401
     weight_acceptance,
     within_tolerance,
 )
-from .decomposition import band_mean, decompose, decompose_stack, truncated_svd  # noqa: F401
+from .decomposition import band_mean, decompose, decompose_stack, randomized_svd, truncated_svd  # noqa: F401

@@ -53,6 +53,34 @@ def truncated_svd(resid, r: int):
     return u[:, :r] * sv[None, :r], vt[:r, :].T
 
 
+def randomized_svd(A, r: int, omega, power_iters: int = 0):
+    """Rank-r factors of A [m, n] by the randomized SVD the pages name (Halko, Martinsson and
+    Tropp, 2009: the randomized range finder, with q power iterations, then the SVD of the
+    small projected matrix):
+        Y = A·Ω,  Q = orth(Y),  [q times: Q = orth(A·orth(Aᵀ·Q))],  B = Qᵀ·A = Ũ·S·Vᵀ,
+        U = Q·Ũ[:, :r]·diag(S[:r]),  V = V[:, :r].
+    Ω [n, k] is the random test matrix, k = r + oversampling. It is an input, so that two
+    implementations can be compared on the same draws. The pages' fallback applies: when
+    min(m, n) <= 256, or when the probe would capture the whole matrix (k >= min(m, n)),
+    the factors are the exact truncation (truncated_svd)."""
+    A = np.asarray(A, dtype=np.float64)
+    omega = np.asarray(omega, dtype=np.float64)
+    m, n = A.shape
+    k = omega.shape[1]
+    if omega.shape[0] != n or k < r:
+        raise ValueError(f"the test matrix must be [{n}, >= {r}], got {omega.shape}")
+    if min(m, n) <= 256 or k >= min(m, n):
+        return truncated_svd(A, r)
+    if r == 0:
+        return np.zeros((m, 0)), np.zeros((n, 0))
+    Q = np.linalg.qr(A @ omega)[0]
+    for _ in range(power_iters):
+        Z = np.linalg.qr(A.T @ Q)[0]
+        Q = np.linalg.qr(A @ Z)[0]
+    ub, sv, vt = np.linalg.svd(Q.T @ A, full_matrices=False)
+    return (Q @ ub[:, :r]) * sv[None, :r], vt[:r].T
+
+
 def decompose(weight, W0, r: int):
     """One projection weight [out, in] against its band's W0: (s, U, V) with
     weight ≈ diag(s)·W0 + U·Vᵀ."""

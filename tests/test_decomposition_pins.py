@@ -3,7 +3,8 @@ the mathematics fix, and planted mistakes that at least one pin must catch.
 
 Each pin reaches its expected value by another route than the oracle's: eigenvalues of
 residᵀ·resid for the Eckart-Young error, a planted decomposition whose parts are known,
-closed forms for bands of scalar multiples, and the passthrough case the pages describe.
+closed forms for bands of scalar multiples, the passthrough case the pages describe, and,
+for the randomized SVD, exact recovery of low-rank matrices and the published error bound.
 """
 import numpy as np
 import pytest
@@ -110,6 +111,98 @@ def pin_passthrough(decompose_stack):
         if not np.allclose(s, 1.0, rtol=1e-14) or not np.allclose(U @ V.T, 0.0, atol=1e-12):
             return False
     return True
+
+
+def _orthonormal(rng, n, k):
+    return np.linalg.qr(rng.standard_normal((n, k)))[0]
+
+
+def pin_rsvd_fallback(rsvd):
+    """The pages' fallback: min(m, n) <= 256, or a probe of k >= min(m, n) columns, gives
+    the exact truncation."""
+    rng = _rng(21)
+    small = rng.standard_normal((40, 60))
+    U, V = rsvd(small, 5, rng.standard_normal((60, 15)))
+    U0, V0 = oracle.truncated_svd(small, 5)
+    wide = rng.standard_normal((300, 280))
+    U1, V1 = rsvd(wide, 4, rng.standard_normal((280, 280)))
+    U2, V2 = oracle.truncated_svd(wide, 4)
+    return np.allclose(U @ V.T, U0 @ V0.T, atol=1e-12) and np.allclose(U1 @ V1.T, U2 @ V2.T, atol=1e-10)
+
+
+def pin_rsvd_exact_low_rank(rsvd):
+    """A matrix of rank r is recovered exactly: a Gaussian probe of r + p columns spans its
+    range with probability one."""
+    rng = _rng(22)
+    A = rng.standard_normal((300, 6)) @ rng.standard_normal((6, 400))
+    U, V = rsvd(A, 6, rng.standard_normal((400, 16)))
+    return np.allclose(U @ V.T, A, rtol=0, atol=1e-9 * np.abs(A).max())
+
+
+def pin_rsvd_spectral_gap(rsvd):
+    """Four singular values far above the rest, oversampling p = 10. Without power
+    iterations the squared error stays within Halko, Martinsson and Tropp's expected-error
+    factor 1 + r/(p - 1) of the optimum, the energy of the tail. With power iterations,
+    which sharpen a gap of 10^4 to the rounding level, it is the optimum."""
+    rng = _rng(23)
+    m, n, r, p = 300, 320, 4, 10
+    sig = np.concatenate([[100.0, 60.0, 30.0, 10.0], 1e-3 * rng.uniform(0.5, 1.0, size=m - 4)])
+    A = (_orthonormal(rng, m, m) * sig[None, :]) @ _orthonormal(rng, n, m).T
+    tail = np.sum(sig[r:] ** 2)
+    for q, bound in ((0, 1 + r / (p - 1)), (1, 1 + 1e-6), (2, 1 + 1e-6)):
+        U, V = rsvd(A, r, rng.standard_normal((n, r + p)), q)
+        if np.sum((A - U @ V.T) ** 2) > bound * tail:
+            return False
+    return True
+
+
+def pin_rsvd_structure(rsvd):
+    """As for the exact truncation: V orthonormal, UᵀU diagonal and non-increasing."""
+    rng = _rng(24)
+    A = rng.standard_normal((270, 300))
+    U, V = rsvd(A, 5, rng.standard_normal((300, 15)), 1)
+    d = np.diag(U.T @ U)
+    return np.allclose(V.T @ V, np.eye(5), atol=1e-10) and np.allclose(U.T @ U, np.diag(d), atol=1e-8 * d.max()) \
+        and np.all(np.diff(d) <= 1e-9 * d.max())
+
+
+RSVD_PINS = (pin_rsvd_fallback, pin_rsvd_exact_low_rank, pin_rsvd_spectral_gap, pin_rsvd_structure)
+
+
+@pytest.mark.parametrize("pin", RSVD_PINS, ids=lambda p: p.__name__)
+def test_randomized_svd_pins(pin):
+    assert pin(oracle.randomized_svd)
+
+
+def rsvd_unorthonormalised(A, r, omega, power_iters=0):   # Y used as the basis, never orthonormalised
+    A = np.asarray(A, float)
+    if min(A.shape) <= 256 or omega.shape[1] >= min(A.shape):
+        return oracle.truncated_svd(A, r)
+    Y = A @ omega
+    ub, sv, vt = np.linalg.svd(Y.T @ A, full_matrices=False)
+    return (Y @ ub[:, :r]) * sv[None, :r], vt[:r].T
+
+
+def rsvd_without_singular_values(A, r, omega, power_iters=0):   # U = Q·Ũ, S dropped
+    A = np.asarray(A, float)
+    if min(A.shape) <= 256 or omega.shape[1] >= min(A.shape):
+        return oracle.truncated_svd(A, r)
+    Q = np.linalg.qr(A @ omega)[0]
+    ub, sv, vt = np.linalg.svd(Q.T @ A, full_matrices=False)
+    return Q @ ub[:, :r], vt[:r].T
+
+
+def rsvd_never_falls_back(A, r, omega, power_iters=0):   # the randomized path on small matrices too
+    A = np.asarray(A, float)
+    Q = np.linalg.qr(A @ omega[:, : min(omega.shape[1], min(A.shape) - 1)])[0]
+    ub, sv, vt = np.linalg.svd(Q.T @ A, full_matrices=False)
+    return (Q @ ub[:, :r]) * sv[None, :r], vt[:r].T
+
+
+@pytest.mark.parametrize("mutant", [rsvd_unorthonormalised, rsvd_without_singular_values, rsvd_never_falls_back],
+                         ids=lambda m: m.__name__)
+def test_pins_catch_randomized_svd_mutants(mutant):
+    assert not all(pin(mutant) for pin in RSVD_PINS)
 
 
 SVD_PINS = (pin_eckart_young, pin_factor_structure)
