@@ -11,11 +11,13 @@ from .reconstruction import (  # noqa: F401
     effective_weight_bf16,
     error_stats,
     linear,
+    linear_error_bound,
     linear_qkv,
     ls_residual,
     ls_scale,
     round_to_bf16,
     weight_acceptance,
+    within_error_bound,
     within_tolerance,
 )
 from .decomposition import band_mean, decompose, decompose_stack, randomized_svd, truncated_svd  # noqa: F401

@@ -163,6 +163,39 @@ def within_tolerance(y, y_ref, elem_tol: float = 1e-2, l2_tol: float = 2e-3) -> 
     return st["max_abs_err"] <= elem_tol * st["max_abs_ref"] and st["rel_l2"] <= l2_tol
 
 
+def linear_error_bound(W0, s, U, V, x, unit_roundoff: float = 2.0 ** -23) -> np.ndarray:
+    """Element-wise bound on |y − y_ref| for a bf16 result of the identity computed with fp32
+    accumulation, t held in bf16 between the down- and the up-projection, and one final
+    rounding to bf16 (the rounding points read from "Execution paths", "The GEMM
+    formulation" and "The custom op": bf16 storage, fp32 accumulation).
+
+    Three terms, each from the classical analysis of floating-point sums (Higham, "Accuracy
+    and Stability of Numerical Algorithms", sec. 3.1, |fl(Σ a_i) − Σ a_i| <= γ_n Σ |a_i| with
+    γ_n = n·u / (1 − n·u), taken with u = 2^-23 so that truncating accumulation is covered):
+      acc   = γ_n·( |s|·(|W0|·|x|) + |U|·(|V|·|x|) ),  n = in + r + 2 (the longest chain of
+              roundings: a dot product over `in`, one over r, the scale and the sum);
+      t_rd  = 2^-8·|U|·|t|: t rounded to bf16 (relative error at most 2^-8) before U·t;
+      out   = 2^-8·(|y_ref| + acc + t_rd): the final rounding of the fp32 value to bf16.
+    Returns acc + t_rd + out (+ 2^-133 for bf16's subnormal spacing). Where an output has so
+    few elements that the relative-L2 bar of ``within_tolerance`` is out of reach even for
+    the exactly rounded RN_bf16(y_ref), this bound is the bar each element is held to.
+    """
+    W0, s, U, V, x = map(_f64, (W0, s, U, V, x))
+    ax = np.abs(x)
+    n = W0.shape[1] + U.shape[1] + 2
+    gamma = n * unit_roundoff / (1.0 - n * unit_roundoff)
+    acc = gamma * (np.abs(s)[None, :] * (ax @ np.abs(W0).T) + (ax @ np.abs(V)) @ np.abs(U).T)
+    t_rd = 2.0 ** -8 * (np.abs(x @ V) @ np.abs(U).T)
+    y = linear(W0, s, U, V, x)
+    return acc + t_rd + 2.0 ** -8 * (np.abs(y) + acc + t_rd) + 2.0 ** -133
+
+
+def within_error_bound(y, W0, s, U, V, x) -> bool:
+    """Every element of y within ``linear_error_bound`` of the fp64 identity."""
+    y_ref = linear(W0, s, U, V, x)
+    return bool(np.all(np.abs(_f64(y) - y_ref) <= linear_error_bound(W0, s, U, V, x)))
+
+
 def bf16_ordinal(bits) -> np.ndarray:
     """Monotone integer image of bf16 bit patterns (+0 and −0 both map to 0), so that
     adjacent representable values differ by exactly 1."""

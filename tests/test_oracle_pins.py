@@ -403,3 +403,78 @@ def test_weight_acceptance_rejects_a_missing_chunk():
     bad = _fp32_weight(W0, s, U, V, drop_chunk=(64, 128))
     acc = oracle.weight_acceptance(bad, W0, s, U, V)
     assert not acc["all_ok"] and acc["outside_bound"] > 1000
+
+
+# ----------------------------------------------------------------------------------
+# the element-wise error bound of the linear (the bar for outputs too small for the
+# relative-L2 bar)
+# ----------------------------------------------------------------------------------
+def _fp32_linear(W0, s, U, V, x, t_bf16=True):
+    """A plain fp32 evaluation: W0 x and t = V^T x summed one index at a time in fp32, t
+    rounded to bf16 when t_bf16, the combine in fp32, one final rounding to bf16."""
+    f = np.float32
+    z = np.zeros((x.shape[0], W0.shape[0]), f)
+    for i in range(W0.shape[1]):
+        z = (z + np.outer(x[:, i], W0[:, i]).astype(f)).astype(f)
+    t = np.zeros((x.shape[0], V.shape[1]), f)
+    for i in range(V.shape[0]):
+        t = (t + np.outer(x[:, i], V[i, :]).astype(f)).astype(f)
+    if t_bf16:
+        t = oracle.round_to_bf16(t.astype(np.float64)).astype(f)
+    lr = np.zeros_like(z)
+    for k in range(U.shape[1]):
+        lr = (lr + np.outer(t[:, k], U[:, k]).astype(f)).astype(f)
+    y32 = (s[None, :].astype(f) * z + lr).astype(f)
+    return oracle.round_to_bf16(y32.astype(np.float64))
+
+
+def _tiny_cases():
+    for out, inp, r, M in ((8, 8, 0, 1), (8, 16, 1, 3), (24, 64, 16, 2), (64, 40, 3, 5), (16, 1152, 16, 4)):
+        th = synth.make_theta(("bound", out, inp, r), out, inp, r)
+        x = synth.bf16_bits_to_f64(synth.make_x(("bound", M, inp), M, inp))[:, :inp]
+        yield th.f64(), x
+
+
+def test_error_bound_admits_exact_rounding_and_fp32_evaluations():
+    for (W0, s, U, V), x in _tiny_cases():
+        y_ref = oracle.linear(W0, s, U, V, x)
+        assert oracle.within_error_bound(oracle.round_to_bf16(y_ref), W0, s, U, V, x)
+        assert oracle.within_error_bound(_fp32_linear(W0, s, U, V, x), W0, s, U, V, x)
+        assert oracle.within_error_bound(_fp32_linear(W0, s, U, V, x, t_bf16=False), W0, s, U, V, x)
+
+
+def test_error_bound_admits_fp32_near_cancellation():
+    """s·W0 x and U t of opposite sign and almost equal size: the fp32 result is far from
+    the exact one in relative terms, and the bound (absolute, from the terms' magnitudes)
+    still admits it."""
+    rng = np.random.default_rng(7)
+    W0 = oracle.round_to_bf16(rng.normal(0, 0.02, (32, 64)))
+    x = oracle.round_to_bf16(rng.normal(0, 1, (3, 64)))
+    U = oracle.round_to_bf16(rng.normal(0, 0.5, (32, 1)))
+    V = oracle.round_to_bf16(rng.normal(0, 0.02, (64, 1)))
+    # choose s so that s·(W0 x) nearly cancels U t for token 0
+    z, lr = x @ W0.T, (x @ V) @ U.T
+    s = oracle.round_to_bf16(-lr[0] / z[0])
+    y_ref = oracle.linear(W0, s, U, V, x)
+    assert np.min(np.abs(y_ref[0]) / (np.abs(s * z[0]) + np.abs(lr[0]))) < 1e-2
+    assert oracle.within_error_bound(_fp32_linear(W0, s, U, V, x), W0, s, U, V, x)
+
+
+@pytest.mark.parametrize("mutant", [_m_drop_delta, _m_no_scale, _m_reversed_rank, _m_squared_t],
+                         ids=lambda f: f.__name__)
+def test_error_bound_rejects_mutants_on_tiny_outputs(mutant):
+    """The same planted mistakes, made by a kernel, fail the bound on tiny outputs: on every
+    tiny case where the mistake changes the result (a rank-r part; two ranks or more for the
+    reversed rank order), at least one element leaves its bound. (Scaling the delta by s as
+    well moves y by about (s - 1)·U t, below the output's own rounding at s ~ U(0.9, 1.1); the
+    integer-valued GPU cases, compared bit for bit, catch that one.)"""
+    caught = 0
+    cases = 0
+    for (W0, s, U, V), x in _tiny_cases():
+        r = U.shape[1]
+        if (r == 0 and mutant is not _m_no_scale) or (r < 2 and mutant is _m_reversed_rank):
+            continue
+        cases += 1
+        got = oracle.round_to_bf16(mutant(W0, s, U, V, x))
+        caught += not oracle.within_error_bound(got, W0, s, U, V, x)
+    assert cases > 0 and caught == cases, (caught, cases)
