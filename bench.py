@@ -439,11 +439,12 @@ def run_ours(args, dist: Dist):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded splitmix64 + Box-Muller draws rounded to bf16; W0~N(0,0.02^2), "
                 "s~U(0.9,1.1), U,V~N(0,0.01^2), x~N(0,1); shapes only, no trained weights",
-        "config": dict(decode_config(), calls_per_step=len(calls),
-                       w0_storage="G=1 values, one physical W0 copy per layer (1.40 GB streamed per M pass)",
-                       l2="inputs larger than L2 (each pass streams 1.40 GB of W0 against a 129 MB L2)",
-                       timing="CUDA graph of the whole step, CUDA events on the replay stream, max over ranks",
-                       parallelism=f"replicas x{dist.world}"),
+        "config": decode_config(),
+        "setup": {"calls_per_step": len(calls),
+                  "w0_storage": "G=1 values, one physical W0 copy per layer (1.40 GB streamed per M pass)",
+                  "l2": "inputs larger than L2 (each pass streams 1.40 GB of W0 against a 129 MB L2)",
+                  "timing": "CUDA graph of the whole step, CUDA events on the replay stream, max over ranks",
+                  "parallelism": f"replicas x{dist.world}"},
         "gpu_launches": launches * args.steps,
         "wall_s_timed": round(wall, 4),
         "peaks": pk,
@@ -876,10 +877,10 @@ def run_reference(args, dist: Dist):
     return {"metric": METRIC, "impl": "reference", "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(B / (v * 1e9) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
-            "config": dict(decode_config(),
-                           timing="each step: the fp64 oracle over a bounded sample of whole layers of the "
-                                  "step on the host cores, host wall clock",
-                           parallelism="host cores"),
+            "config": decode_config(),
+            "setup": {"timing": "each step: the fp64 oracle over a bounded sample of whole layers of the "
+                                "step on the host cores, host wall clock",
+                      "parallelism": "host cores"},
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -16,7 +16,8 @@
  *   elements). Orientation follows "Execution paths", "The GEMM formulation":
  *   x [M, in], y [M, out], W0 [out, in], V [in, r], U [out, r]; s scales y's columns.
  * - Every tensor pointer is a DEVICE pointer owned by the caller; the library keeps
- *   no reference after a call returns and allocates no device memory.
+ *   no reference after a call returns and allocates no device memory. (The one array
+ *   it owns is the fixed scratch of aq_linear_noalloc, compiled into the library.)
  * - Alignment: pointers 16-byte aligned, every leading dimension a multiple of 8
  *   elements (rows start on 16-byte boundaries: the kernels move operands with TMA).
  * - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL is
@@ -94,7 +95,7 @@ typedef struct aq_theta {
  * that part must be zero before the workspace is first used (e.g. cudaMemset once after
  * allocating it), and every call that completes leaves it zero again, so one workspace
  * can serve any sequence of calls, shapes and paths on a stream. The rest is scratch
- * that needs no initialisation (per-CTA partial sums at decode; t in bf16 and a
+ * that needs no initialisation (the decode kernel uses none of it; t in bf16 and a
  * transposed copy of V at prefill; and, when a prefill call splits K, the fp32 partial
  * sums of every K slice). After a call whose bounded wait expired
  * (aq_device_status() == AQ_ERR_TIMEOUT) the sync part must be zeroed again. */
@@ -122,12 +123,12 @@ size_t aq_linear_workspace_bytes(const aq_theta* th, int32_t n_theta, int64_t M)
  *             workspace is needed
  *   stream    cudaStream_t
  * M == 0 is a no-op returning AQ_OK. Decode (M <= aq_decode_max_m() = 32) is one
- * launch that streams W0 once, split evenly over the SMs. Prefill (larger M) transposes V
- * and runs one tcgen05 GEMM whose first tiles compute t = x V. Both fuse s and the rank-r
- * term into the epilogue. A prefill call whose output tiles fill at most half of the SMs
- * over a deep K, with r <= 16, instead splits K over more CTAs that write fp32 partial
- * sums, and a third launch computes y from them in a fixed order. Concurrent calls
- * sharing one workspace must be ordered on the GPU. */
+ * launch that streams W0 once, split evenly over the SMs. The mid-M and prefill GEMMs (see
+ * aq_set_path) transpose V and run one tcgen05 GEMM whose first tiles compute t = x V. All
+ * fuse s and the rank-r term into the epilogue. A GEMM call whose output tiles fill at most
+ * half of the SMs over a deep K, with r <= 16, instead splits K over more CTAs that write
+ * fp32 partial sums, and a third launch computes y from them in a fixed order. Concurrent
+ * calls sharing one workspace must be ordered on the GPU. */
 aq_status aq_linear(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
                     void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
                     void* stream);
@@ -162,10 +163,13 @@ aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t 
  * the library keeps allocated until the process exits. The caller still passes x and y.
  *   - A call whose minimum scratch need exceeds AQ_NOALLOC_WORKSPACE_BYTES is rejected
  *     with AQ_ERR_WORKSPACE (message in aq_last_error) before anything is enqueued. Split-K
- *     partial sums use what the array has beyond that minimum, so such a call may split K
- *     into fewer slices than with a full workspace.
+ *     partial sums use what the array has beyond that minimum (for r = 0 too, whose
+ *     minimum is zero), so such a call may split K into fewer slices than with a full
+ *     workspace.
  *   - The first call on a device looks up the array's device address on that device;
- *     make that first call before capturing a stream into a CUDA graph.
+ *     make that first call before capturing a stream into a CUDA graph. The address is
+ *     looked up again when the device's current context has changed since (after
+ *     cudaDeviceReset, for example); a call that does so must not be captured either.
  *   - All calls on a device share the one array and it keeps the previous call's
  *     contents. Its sync part (see AQ_WORKSPACE_SYNC_BYTES) starts at zero when the
  *     library is loaded and every completed call leaves it zero; after an expired wait
@@ -177,6 +181,13 @@ aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t 
 aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_t ldx,
                             void* y, int64_t ldy, void* stream);
 
+/* Test hook for aq_linear_noalloc (no counterpart in the paper): copies `bytes` of the
+ * built-in scratch array of the current device, starting at `offset`, to `dst` (host or
+ * device memory), ordered on `stream`, and returns once the copy is done. Lets a test check
+ * that the array's sync part reads back zero after a series of calls. A range outside the
+ * array returns AQ_ERR_INVALID_ARG. Allocates nothing. */
+aq_status aq_noalloc_scratch_read(void* dst, size_t offset, size_t bytes, void* stream);
+
 /* W_eff[o, i] = RN_bf16( s[o] * W0[o,i] + sum_k U[o,k] * V[i,k] )
  * ("Execution paths", "Precompute-outside: the production path": built once per
  * layer at load). W_eff is [out, in] device, row stride ld_weff >= in, and must not
@@ -187,7 +198,18 @@ aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* 
 /* Synchronises `stream`, then returns the device status word of the current device
  * (AQ_OK, or AQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last clear)
  * and clears it. A kernel whose wait expires stops its work (its outputs are then
- * undefined), releases its tensor memory and exits; the CUDA context stays usable. */
+ * undefined), releases its tensor memory and exits; the CUDA context stays usable.
+ *
+ * Residency contract. The CTAs of one decode launch hand t = V^T x to each other through
+ * the workspace (t CTAs publish it, the W0-streaming CTAs wait for it, one CTA waits for
+ * all of them before it clears the sync region), and the prefill GEMM's tiles wait for the
+ * t tiles of the same launch. These launches are sized to fit on the GPU at once, so every
+ * wait ends when the launch has the device to itself or shares it with other work of this
+ * process that completes. If SMs are held for longer by another context, an MPS client or a
+ * green context, some CTAs may not run until the waits of others expire: such a call ends
+ * with AQ_ERR_TIMEOUT in the status word and undefined outputs, and reports nothing else.
+ * Callers that share the GPU that way should poll aq_device_status() after a batch of
+ * calls (it synchronises the stream) and recompute the batch when it reports a timeout. */
 aq_status aq_device_status(void* stream);
 
 /* Test hook for the bounded-wait path: launches one block that waits on a barrier no
@@ -196,16 +218,25 @@ aq_status aq_device_status(void* stream);
  * exits; aq_device_status() then reports it. No fault, trap or hang is involved. */
 aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
 
-/* Path selection for aq_linear / aq_linear_qkv / aq_linear_multi. AQ_PATH_AUTO picks by M
- * and size: the decode kernel for M <= aq_decode_max_m(), except that from 16 tokens a
- * call whose W0 (summed over its families) holds 128 MB or more takes the prefill GEMM;
- * the prefill GEMM above. The other values force a path for tests: prefill works for
- * every M, decode for M <= aq_decode_max_m() (larger M returns AQ_ERR_UNSUPPORTED).
+/* Path selection for aq_linear / aq_linear_qkv / aq_linear_multi. Three kernels serve the
+ * three token buckets of one call:
+ *   AQ_PATH_DECODE   the mma.sync streaming kernel, M <= aq_decode_max_m() = 32: W0 split by
+ *                    output rows over the SMs, x resident, t = V^T x within the launch;
+ *   AQ_PATH_MIDM     the tcgen05 GEMM with 128 output rows per tile as the accumulator lanes
+ *                    and the tokens (up to 256 per tile) as the MMA N, so that each W0 tile is
+ *                    read once for all tokens; a transpose of V and t = x V inside the launch;
+ *   AQ_PATH_PREFILL  the tcgen05 GEMM with 128 tokens per tile as the accumulator lanes and
+ *                    output rows as N (CTA pairs, 2-SM MMAs), for large M.
+ * AQ_PATH_AUTO picks by M and size: decode up to 32 tokens, except that from 16 tokens a call
+ * whose W0 (summed over its families) holds 128 MB or more takes the mid-M GEMM; mid-M up to
+ * 512 tokens; prefill above. The other values force a path for tests: mid-M and prefill work
+ * for every M, decode for M <= aq_decode_max_m() (larger M returns AQ_ERR_UNSUPPORTED).
  * Process-wide setting. */
-typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2 } aq_path;
+typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2, AQ_PATH_MIDM = 3 } aq_path;
 aq_status aq_set_path(aq_path path);
 int32_t aq_decode_max_m(void);
-/* Path the last aq_linear / aq_linear_qkv call on this thread took (1 or 2; 0 if none). */
+/* Path the last aq_linear / aq_linear_qkv / aq_linear_multi call on this thread took (an
+ * aq_path value other than AQ_PATH_AUTO; 0 if none). */
 int32_t aq_last_path(void);
 
 /* Number of kernel launches the last successful aq_* call on this thread enqueued. */

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     AQ_OK,
     AQ_PATH_AUTO,
     AQ_PATH_DECODE,
+    AQ_PATH_MIDM,
     AQ_PATH_PREFILL,
     AqError,
     Theta,

@@ -27,12 +27,13 @@ AQ_MAX_RANK = 256
 AQ_PATH_AUTO = 0
 AQ_PATH_DECODE = 1
 AQ_PATH_PREFILL = 2
+AQ_PATH_MIDM = 3
 
 EXPORTED_SYMBOLS = [
     "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
     "aq_device_status", "aq_selftest_bounded_wait", "aq_set_path", "aq_decode_max_m",
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
-    "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi",
+    "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -85,6 +86,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_linear_multi.restype = ctypes.c_int
     lib.aq_linear_noalloc.argtypes = [th_p, vp, i64, i64, vp, i64, vp]
     lib.aq_linear_noalloc.restype = ctypes.c_int
+    lib.aq_noalloc_scratch_read.argtypes = [vp, sz, sz, vp]
+    lib.aq_noalloc_scratch_read.restype = ctypes.c_int
     lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
     lib.aq_precompute.restype = ctypes.c_int
     lib.aq_device_status.argtypes = [vp]

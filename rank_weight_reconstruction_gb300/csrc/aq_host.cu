@@ -23,6 +23,7 @@ thread_local int32_t t_launches = 0;
 std::atomic<int> g_path{AQ_PATH_AUTO};
 
 constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
+constexpr int kMidMaxM = 512;                         // swapped-operand GEMM up to this M
 constexpr int kGemmMinMBigW0 = 16;                    // ... but from this M the GEMM takes calls
 constexpr int64_t kGemmBigW0Bytes = 128ll << 20;      // whose W0 has at least this many bytes
 constexpr uint64_t kTimeoutNs = 1000ull * 1000 * 1000;  // limit of one in-kernel wait: 1 s
@@ -433,6 +434,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   for (int j = 0; j < n; ++j) w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
   const bool gemm_pays = M >= kGemmMinMBigW0 && w0_bytes >= kGemmBigW0Bytes;
   const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM && !gemm_pays);
+  // Mid-M: the tcgen05 GEMM with output rows as accumulator lanes and the tokens as N
+  const bool midm = !decode && (path_cfg == AQ_PATH_MIDM || (path_cfg == AQ_PATH_AUTO && M <= kMidMaxM));
   if (decode && M > kDecodeMaxM)
     return fail(AQ_ERR_UNSUPPORTED, "%s: the decode kernel handles at most %d tokens (M=%lld)", who, kDecodeMaxM,
                 (long long)M);
@@ -672,10 +675,20 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   GemmParams gp = {};
   gp.M = static_cast<int32_t>(M);
   gp.K = K;
-  gp.tok_tile = kMmaM;
-  gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
-  gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
-  gp.n_mma = gp.row_tile;
+  if (midm) {
+    // 128 output rows per tile as the accumulator lanes; all tokens (in tiles of at most 256,
+    // balanced, multiples of 16) as the MMA N
+    gp.swap = 1;
+    gp.row_tile = kMmaM;
+    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, 256));
+    gp.tok_tile = static_cast<int32_t>(round_up(ceil_div(M, gp.n_tok_tiles), 16));
+    gp.n_mma = gp.tok_tile;
+  } else {
+    gp.tok_tile = kMmaM;
+    gp.n_tok_tiles = static_cast<int32_t>(ceil_div(M, kMmaM));
+    gp.row_tile = prefill_row_tile(th, n, gp.n_tok_tiles, dev->sms);
+    gp.n_mma = gp.row_tile;
+  }
   // Split K: when the output tiles fill at most half of the SMs and K is deep, the K of every
   // tile is cut into slices that separate CTAs sum into fp32 partials (no scale, no rank-r
   // part), and a small kernel finishes y = RN(s * sum z + U * sum t). The slices stop where
@@ -707,12 +720,15 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   // MMA, which bounds this GEMM. Pairs need two token tiles and one CTA per SM; each half of
   // B is a whole number of 8-row swizzle atoms.
   size_t smem = 0;
-  for (int cl = (split == 1 && gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1; cl >= 1;
-       --cl) {
+  // (the swapped layout writes y straight from registers: no output staging)
+  const size_t ystage = midm ? 0 : kYStageTotal;
+  for (int cl = (!midm && split == 1 && gp.n_tok_tiles >= 2 && dev->gemm_pairs > 0 && gp.row_tile % 16 == 0) ? 2 : 1;
+       cl >= 1; --cl) {
     gp.cluster = cl;
+    // a stage: the 128-lane operand (A) and the N-row operand (B, or this CTA's half of it)
     gp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + (gp.n_mma / cl) * 128, 1024));
-    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack + kYStageTotal);
-    smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + kYStageTotal + static_cast<size_t>(gp.stages) * gp.stage_bytes;
+    gp.stages = stages_for(gp.stage_bytes, dev->smem_optin, kHeaderBytes + kGemmSBufBytes + kSmemSlack + ystage);
+    smem = kSmemSlack + kHeaderBytes + kGemmSBufBytes + ystage + static_cast<size_t>(gp.stages) * gp.stage_bytes;
     if (cl == 1 || smem >= kGemmPairMinSmem) break;
   }
   gp.n_tok_units = static_cast<int32_t>(ceil_div(gp.n_tok_tiles, gp.cluster));
@@ -721,6 +737,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   // token tile; otherwise as a GEMM launch of its own before it
   const int64_t n_flags = static_cast<int64_t>(gp.n_tok_units) * gp.cluster;
   const bool fused_t = wl.any_r && (split > 1 || 1 + n_flags <= static_cast<int64_t>(kSyncBytes / 4));
+  if (midm && wl.any_r && !fused_t)
+    return fail(AQ_ERR_UNSUPPORTED, "%s: M=%lld has too many token tiles for the mid-M path", who, (long long)M);
 
   if (wl.any_r) {
     // V^T into the workspace: the t tiles read it K-major
@@ -795,7 +813,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     s.r = 0;
     s.t_seg = 1;
     s.n_row_tiles = static_cast<int32_t>(ceil_div(wl.ld_t, gp.row_tile));
-    s.n_mma = static_cast<int32_t>(std::min<int64_t>(round_up(wl.ld_t, 16), gp.row_tile));
+    s.n_mma = midm ? gp.n_mma : static_cast<int32_t>(std::min<int64_t>(round_up(wl.ld_t, 16), gp.row_tile));
     s.tile_begin = tiles;
     tiles += s.n_row_tiles * gp.n_tok_units;
     if (split > 1) {
@@ -826,7 +844,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     s.n_mma = gp.n_mma;
     // bulk tensor stores of y need whole 64-column boxes per tile: a partial box would write
     // into the next tile's columns (the tensor map clips only at the family's last row)
-    s.tma_y = gp.row_tile % 64 == 0 ? 1 : 0;
+    s.tma_y = (!midm && gp.row_tile % 64 == 0) ? 1 : 0;
     if (split > 1) {   // fp32 partials of W0 x; s and U t are the finalize kernel's
       s.s = nullptr;
       s.y = nullptr;
@@ -875,7 +893,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     }
     if ((st = launch_or_fail(launch_finalize(fp, blocks, cs, true), "launch split-K finalize")) != AQ_OK) return st;
   }
-  t_last_path = AQ_PATH_PREFILL;
+  t_last_path = midm ? AQ_PATH_MIDM : AQ_PATH_PREFILL;
   return AQ_OK;
 }
 
@@ -1020,7 +1038,7 @@ aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
 }
 
 aq_status aq_set_path(aq_path path) {
-  if (path != AQ_PATH_AUTO && path != AQ_PATH_DECODE && path != AQ_PATH_PREFILL)
+  if (path != AQ_PATH_AUTO && path != AQ_PATH_DECODE && path != AQ_PATH_PREFILL && path != AQ_PATH_MIDM)
     return fail(AQ_ERR_INVALID_ARG, "aq_set_path: unknown path %d", (int)path);
   g_path.store(path);
   return AQ_OK;

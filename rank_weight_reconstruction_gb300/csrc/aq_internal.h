@@ -54,8 +54,9 @@ struct GemmParams {
   int32_t row_tile;     // rows of the row operand per tile (box rows of tm_w / tm_u)
   int32_t tok_tile;     // tokens per tile (box rows of tm_x / tm_t)
   int32_t n_tok_tiles;
-  int32_t cluster;      // 1, or 2: CTA pairs take adjacent token tiles of one row tile and
-                        //    each loads half of the row operand for both (TMA multicast)
+  int32_t cluster;      // 1, or 2: CTA pairs take adjacent token tiles of one row tile; each
+                        //    CTA loads half of the row operand (its own TMA loads, no
+                        //    multicast) and the pair's 2-SM MMAs read both halves
   int32_t n_tok_units;  // ceil(n_tok_tiles / cluster): token tiles per row tile, in pairs
   int32_t total_tiles;  // work units: row tiles x n_tok_units, summed over the segments
   int32_t n_mma;        // MMA N: round_up(row_tile, 16)
@@ -73,6 +74,9 @@ struct GemmParams {
   uint64_t timeout_ns;
   int32_t ksplit;       // K slices per tile (1: none); work item = unit * ksplit + slice
   int32_t kb_per;       // k blocks per slice (the last slice may have fewer)
+  int32_t swap;         // 1: the row operand's 128-row tiles are the accumulator lanes and the
+                        //    tokens (tok_tile <= 256 of them) the MMA N; row_tile = 128,
+                        //    n_mma = tok_tile (the mid-M bucket)
 };
 static_assert(sizeof(GemmParams) <= 4096, "kernel parameters are limited to 4 KB");
 

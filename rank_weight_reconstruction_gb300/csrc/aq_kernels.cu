@@ -9,8 +9,9 @@
 //                        s in TMEM, the rank-r up-projection is then added as extra K blocks
 //                        into the same accumulator, and y is rounded once. t = x V runs as
 //                        the first tiles of the same launch (or, for very large M, as a
-//                        launch of its own). CTA pairs share the W0 / U tiles by TMA
-//                        multicast.
+//                        launch of its own). A CTA pair runs 2-SM MMAs (cta_group::2):
+//                        each CTA of the pair loads its own half of the W0 / U rows with
+//                        plain TMA loads (no multicast) and the even CTA's MMA reads both.
 // aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
 // aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
 //                        epilogue, W_eff written back with TMA stores.
@@ -97,8 +98,17 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, i
 // barrier; its MMA commits arrive on both CTAs' `empty`, `acc_full` and `acc_done`; both
 // CTAs' epilogue warps arrive on its `acc_scaled` and `acc_empty`.
 // kPair: the CTA-pair (cluster = 2) variant; a function may not mix cta_group::1 and ::2.
-template <bool kPair>
+//
+// kSwap: the roles of the two operands are exchanged (the mid-M bucket, a few dozen to a few
+// hundred tokens). The accumulator lanes are then 128 rows of the row operand (W0, V^T or U)
+// and its N columns are the tokens (tok_tile = N <= 256): D[row, token]. One W0 tile feeds an
+// MMA with all of a call's tokens, so W0 is streamed once even when the tokens are far fewer
+// than 128, where the token-lane layout would pad most of every MMA. The epilogue owns one
+// output row per thread: s is a per-thread scalar, and y is written down a column (32
+// consecutive rows per warp-wide store). Not combined with CTA pairs.
+template <bool kPair, bool kSwap>
 __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!(kPair && kSwap), "the swapped-operand GEMM runs without CTA pairs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -217,9 +227,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) return false;
         uint8_t* st = ring + static_cast<size_t>(stage) * p.stage_bytes;
         if (leader) mbar_arrive_expect_tx(&full[stage], tx_bytes);
-        // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
-        load(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
-        load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, sg.n_mma, &full[stage]);
+        if constexpr (kSwap) {
+          // A = 128 rows (W0, or U), B = the tokens (x, or t for the rank-r blocks)
+          load(st, low ? &sg.tm_u : &sg.tm_w, kb * kBK, tc.row0, &full[stage]);
+          load(st + kStageA, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
+        } else {
+          // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
+          load(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
+          load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, sg.n_mma, &full[stage]);
+        }
         filled |= 1u << stage;
         fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
         if (++stage == p.stages) {
@@ -245,13 +261,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
             for (; kb < pre; ++kb) {
               uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
               if (leader) mbar_arrive_expect_tx(&full[kb], tx_bytes);
-              load_rows(st, &sg.tm_w, cur.kb_lo + kb, tc.row0, sg.n_mma, &full[kb]);
+              if constexpr (kSwap) {
+                load(st, &sg.tm_w, (cur.kb_lo + kb) * kBK, tc.row0, &full[kb]);
+              } else {
+                load_rows(st, &sg.tm_w, cur.kb_lo + kb, tc.row0, sg.n_mma, &full[kb]);
+              }
               filled |= 1u << kb;
             }
             pdl_wait_prior_grid();
             for (int j = 0; j < pre; ++j) {
               uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-              load(st, &p.tm_x, (cur.kb_lo + j) * kBK, tc.tok0, &full[j]);
+              load(kSwap ? st + kStageA : st, &p.tm_x, (cur.kb_lo + j) * kBK, tc.tok0, &full[j]);
             }
             stage = pre;
             if (stage == p.stages) {
@@ -411,6 +431,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       const uint32_t b = it & 1;
       const uint32_t par = (it >> 1) & 1;
       const uint32_t acc = t_lane + b * static_cast<uint32_t>(p.n_mma);
+      if constexpr (kSwap) {
+        // ---- lane = output row, columns = tokens ----
+        const int row = tc.row0 + et;
+        const bool row_ok = et < p.row_tile && row < sg.rows;
+        // this row's scale, requested before the wait so that it lands while the MMAs run
+        const float sc = (row_ok && sg.s) ? bf16_to_f32(sg.s[row]) : 1.0f;
+        if (!warp_wait(&acc_full[b], par, ctl)) break;
+        tc_fence_after();
+        if (has_lr) {
+          // scale the W0 x accumulator by s in place; the MMA warp then adds U t
+          for (int c = 0; c < sg.n_mma; c += 16) {
+            float v[16];
+            tmem_ld_16(acc + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= sc;
+            tmem_st_16(acc + c, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_lead(&acc_scaled[b]);
+          if (!warp_wait(&acc_done[b], (lr_phase >> b) & 1u, ctl)) break;
+          lr_phase ^= 1u << b;
+          tc_fence_after();
+        }
+        if (sg.part) {
+          // split K: this slice's raw fp32 sums [slice][token][row], 32 consecutive rows per
+          // warp-wide store
+          float* pcol = sg.part + static_cast<int64_t>(itm.ks) * p.M * sg.ld_part + (row_ok ? row : 0);
+          for (int c = 0; c < sg.n_mma; c += 16) {
+            float v[16];
+            tmem_ld_16(acc + c, v);
+            tmem_ld_wait();
+            if (!row_ok) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = tc.tok0 + c + j;
+              if (tok < p.M) pcol[static_cast<int64_t>(tok) * sg.ld_part] = v[j];
+            }
+          }
+        } else {
+          uint16_t* ycol = sg.y + (row_ok ? row : 0);
+          for (int c = 0; c < sg.n_mma; c += 16) {
+            float v[16];
+            tmem_ld_16(acc + c, v);
+            tmem_ld_wait();
+            if (!row_ok) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = tc.tok0 + c + j;
+              if (tok < p.M) ycol[static_cast<int64_t>(tok) * sg.ldy] = f32_to_bf16_rn(has_lr ? v[j] : v[j] * sc);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_lead(&acc_empty[b]);
+        if (sg.t_seg && !sg.part) {
+          // publish this token tile's t: every thread's stores, then one release
+          __threadfence();
+          fence_proxy_async_global();
+          if (!epi_sync()) break;
+          if (et == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
+        }
+        continue;
+      }
       // s of this tile's rows into shared memory (fp32, zero past the tile) while the
       // tensor core works on it
       if (!epi_sync()) break;   // every epilogue warp is done with the previous tile's s
@@ -994,10 +1081,13 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
 cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<GemmParams*>(&p)};
   if (p.cluster > 1)
-    return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<true>), dim3(grid), dim3(kGemmThreads), smem, st,
-                     pdl, args, dim3(2, 1, 1));
-  return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<false>), dim3(grid), dim3(kGemmThreads), smem, st,
-                   pdl, args);
+    return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<true, false>), dim3(grid), dim3(kGemmThreads), smem,
+                     st, pdl, args, dim3(2, 1, 1));
+  if (p.swap)
+    return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<false, true>), dim3(grid), dim3(kGemmThreads), smem,
+                     st, pdl, args);
+  return launch_ex(reinterpret_cast<const void*>(&aq_gemm_kernel<false, false>), dim3(grid), dim3(kGemmThreads), smem,
+                   st, pdl, args);
 }
 
 cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
@@ -1012,7 +1102,7 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel<true>), &cfg);
+  return cudaOccupancyMaxActiveClusters(n, reinterpret_cast<const void*>(&aq_gemm_kernel<true, false>), &cfg);
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl) {
@@ -1045,8 +1135,9 @@ cudaError_t configure_kernels(int device, size_t max_smem) {
   (void)device;
   cudaError_t e;
   const int s = static_cast<int>(max_smem);
-  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
-  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = configure_decode(max_smem))) return e;
   if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
     return e;

@@ -8,6 +8,7 @@
 // start-up (cudaMalloc can synchronise the device and fragments a fixed memory budget),
 // or code running where no allocator is reachable at all. For them the scratch lives in
 // one fixed array compiled into this library.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -30,11 +31,34 @@ size_t linear_workspace_min_bytes(const aq_theta* th, int32_t n_theta, int64_t M
 
 namespace {
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The current context, through the driver entry point (the runtime exposes no handle of
+// its own). A context torn down and created again -- cudaDeviceReset, for one -- reloads
+// this library's device code, and the array's address may then differ.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};  // device address of aq_noalloc_scratch, per device index
+// device address of aq_noalloc_scratch per device index, and the context it was looked up in
+void* g_scratch_ptr[64] = {};
+CUcontext g_scratch_ctx[64] = {};
 
 // In host code the array's name is only a host-side stand-in; the kernels need its
-// device address, which is looked up once per device with that device current.
+// device address, which is looked up with the device current: once per device, and again
+// whenever the device's current context is no longer the one of the last lookup.
 aq_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -45,8 +69,9 @@ aq_status scratch_address(void** out) {
   }
   if (dev < 0 || dev >= 64)
     return static_cast<aq_status>(aq::set_last_error(AQ_ERR_UNSUPPORTED, "aq_linear_noalloc: device index out of range"));
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, aq_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -56,6 +81,7 @@ aq_status scratch_address(void** out) {
       return static_cast<aq_status>(aq::set_last_error(AQ_ERR_CUDA, msg));
     }
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_ptr[dev];
   return AQ_OK;
@@ -77,9 +103,27 @@ extern "C" aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_
              (long long)M, th->r, th->in, need, (unsigned)AQ_NOALLOC_WORKSPACE_BYTES);
     return static_cast<aq_status>(aq::set_last_error(AQ_ERR_WORKSPACE, msg));
   }
-  if (need == 0) return aq_linear(th, x, M, ldx, y, ldy, nullptr, 0, stream);
+  // A call that needs no scratch may still split K into slices whose partial sums live in
+  // it (r = 0 prefill calls with few output tiles): hand it the array whenever a full-size
+  // workspace would be nonzero.
+  if (need == 0 && aq_linear_workspace_bytes(th, 1, M) == 0) return aq_linear(th, x, M, ldx, y, ldy, nullptr, 0, stream);
   void* scratch = nullptr;
   aq_status st = scratch_address(&scratch);
   if (st != AQ_OK) return st;
   return aq_linear(th, x, M, ldx, y, ldy, scratch, AQ_NOALLOC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" aq_status aq_noalloc_scratch_read(void* dst, size_t offset, size_t bytes, void* stream) {
+  if (!dst || offset > AQ_NOALLOC_WORKSPACE_BYTES || bytes > AQ_NOALLOC_WORKSPACE_BYTES - offset)
+    return static_cast<aq_status>(
+        aq::set_last_error(AQ_ERR_INVALID_ARG, "aq_noalloc_scratch_read: range outside the scratch array"));
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyFromSymbolAsync(dst, aq_noalloc_scratch, bytes, offset, cudaMemcpyDefault, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "aq_noalloc_scratch_read: %s", cudaGetErrorString(e));
+    return static_cast<aq_status>(aq::set_last_error(AQ_ERR_CUDA, msg));
+  }
+  return AQ_OK;
 }

@@ -2,7 +2,7 @@
 
 Bars (fixed before any kernel was written):
 * reconstruction linear: max |y - y_ref| <= 1e-2 * max |y_ref| and relative L2 <= 2e-3
-  over the whole output (or over the sampled rows at full 31B-class sizes);
+  over the whole output, at every size (large outputs are compared in row chunks);
 * integer-valued inputs: every intermediate is exact in fp32 and bf16, so the result
   must equal the oracle bit for bit on every path;
 * W_eff: every element within 1 bf16 ulp of RN_bf16(oracle); passthrough and r = 0 with
@@ -16,12 +16,13 @@ import oracle
 import rank_weight_reconstruction_gb300 as aq
 from rank_weight_reconstruction_gb300 import synth
 
-from helpers import bits, dev, dev_theta, host_f64, x_f64
+from helpers import bits, close_over_rows, dev, dev_theta, host_f64, x_f64
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [aq.AQ_PATH_DECODE, aq.AQ_PATH_PREFILL]
-PATH_IDS = {aq.AQ_PATH_AUTO: "auto", aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_PREFILL: "prefill"}
+PATHS = [aq.AQ_PATH_DECODE, aq.AQ_PATH_MIDM, aq.AQ_PATH_PREFILL]
+PATH_IDS = {aq.AQ_PATH_AUTO: "auto", aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_MIDM: "midm",
+            aq.AQ_PATH_PREFILL: "prefill"}
 
 
 @pytest.fixture(autouse=True)
@@ -315,25 +316,25 @@ def test_rank_sweep(shape, r, M):
     th = synth.make_theta(("sweep", out, inp, r), out, inp, r)
     xb = synth.make_x(("sweep", out, inp, M), M, inp)
     y = host_f64(run_linear(th, xb))
-    W0, s, U, V = th.f64()
-    xf = x_f64(xb, inp)
-    rows = np.arange(M) if M <= 512 else np.unique(np.linspace(0, M - 1, 64).astype(int))
-    assert_close(y[rows], oracle.linear(W0, s, U, V, xf[rows]))
+    st, ok = close_over_rows(y, *th.f64(), x_f64(xb, inp))
+    assert ok, st
 
 
 # ----------------------------------------------------------------------------------
 # 31B-class projection: out 21504, in 5376, r 128, M in {1, 32, 8192}
 # ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("path", [aq.AQ_PATH_MIDM, aq.AQ_PATH_PREFILL], ids=lambda p: PATH_IDS[p])
 @pytest.mark.parametrize("r", [0, 5, 64])
-def test_split_k_dispatch(r):
-    """A down-like projection at 64 tokens has 18 output tiles of 64 rows over a K of 6912:
-    up to rank 16 its K is split across CTAs and a finalize kernel sums the slices (one
-    more launch); at rank 64 it stays one GEMM. Both within tolerance of the oracle."""
+def test_split_k_dispatch(r, path):
+    """A down-like projection at 64 tokens has few output tiles over a K of 6912 (9 tiles of
+    128 rows on the mid-M GEMM, 18 tiles of 64 rows on the prefill GEMM): up to rank 16 its
+    K is split across CTAs and a finalize kernel sums the slices (one more launch); at rank 64
+    it stays one GEMM. All within tolerance of the oracle."""
     out, inp, M = 1152, 6912, 64
     th = synth.make_theta(("split", r), out, inp, r)
     xb = synth.make_x(("split", r), M, inp)
-    y = run_linear(th, xb)
-    assert aq.aq_last_path() == aq.AQ_PATH_PREFILL
+    y = run_linear(th, xb, path)
+    assert aq.aq_last_path() == path
     gemm_launches = 1 if r == 0 else 2             # (V^T transpose,) GEMM
     split = r <= 16
     assert aq.aq_last_launch_count() == gemm_launches + (1 if split else 0)
@@ -347,12 +348,12 @@ def test_31b_projection(M):
     th = synth.make_theta(("31b", "wide", 0), out, inp, 128)
     xb = synth.make_x(("31b-x", M), M, inp)
     y = host_f64(run_linear(th, xb))
-    # a W0 of 231 MB takes the tcgen05 GEMM from 16 tokens on
-    assert aq.aq_last_path() == (aq.AQ_PATH_DECODE if M < 16 else aq.AQ_PATH_PREFILL)
-    W0, s, U, V = th.f64()
-    xf = x_f64(xb, inp)
-    rows = np.arange(M) if M <= 32 else np.unique(np.linspace(0, M - 1, 48).astype(int))
-    assert_close(y[rows], oracle.linear(W0, s, U, V, xf[rows]))
+    # a W0 of 231 MB takes the mid-M tcgen05 GEMM from 16 tokens on, the prefill GEMM above 512
+    assert aq.aq_last_path() == (aq.AQ_PATH_DECODE if M < 16 else aq.AQ_PATH_MIDM if M <= 512
+                                 else aq.AQ_PATH_PREFILL)
+    # the whole output, every token tile of the persistent multi-wave schedule included
+    st, ok = close_over_rows(y, *th.f64(), x_f64(xb, inp), chunk=512)
+    assert ok, st
 
 
 @pytest.mark.parametrize("M", [16, 32])
@@ -367,14 +368,18 @@ def test_31b_projection_decode_forced(M):
 
 
 def test_path_choice_by_size():
-    """Up to 32 tokens the decode kernel, except from 16 tokens on for a W0 of 128 MB or more."""
+    """Up to 32 tokens the decode kernel, except from 16 tokens on for a W0 of 128 MB or more;
+    the mid-M GEMM up to 512 tokens; the prefill GEMM above."""
     sq = synth.CLASS31B_SHAPES["square"]
     th = synth.make_theta(("31b", "square", 0), sq[0], sq[1], 128)
-    for M in (1, 16, 32):
-        run_linear(th, synth.make_x(("path", M), M, sq[1]))
-        assert aq.aq_last_path() == aq.AQ_PATH_DECODE, M
-    run_linear(th, synth.make_x(("path", 33), 33, sq[1]))
-    assert aq.aq_last_path() == aq.AQ_PATH_PREFILL
+    for M, path in ((1, aq.AQ_PATH_DECODE), (16, aq.AQ_PATH_DECODE), (32, aq.AQ_PATH_DECODE),
+                    (33, aq.AQ_PATH_MIDM), (512, aq.AQ_PATH_MIDM), (513, aq.AQ_PATH_PREFILL)):
+        y = host_f64(run_linear(th, synth.make_x(("path", M), M, sq[1])))
+        assert aq.aq_last_path() == path, M
+        if M in (33, 513):
+            xb = synth.make_x(("path", M), M, sq[1])
+            st, ok = close_over_rows(y, *th.f64(), x_f64(xb, sq[1]))
+            assert ok, (M, st)
 
 
 # ----------------------------------------------------------------------------------
@@ -385,11 +390,16 @@ def _ulp_diff(got_bits, ref_value):
     return np.abs(oracle.bf16_ordinal(got_bits) - oracle.bf16_ordinal(ref_bits))
 
 
-def assert_weight_ok(W, th):
+def assert_weight_ok(W, th, what=""):
     acc = oracle.weight_acceptance(bits(W), *th.f64())
+    # what the acceptance actually used: elements beyond 1 ulp and the largest distance
+    print(f"W_eff {what or (th.out, th.inp, th.r)}: {acc['elements'] - acc['within_1ulp']} of "
+          f"{acc['elements']} elements beyond 1 ulp, max {acc['max_ulp']} ulp")
     assert acc["all_ok"], acc
-    # the 1-ulp bar holds everywhere except on near-cancelling elements
-    assert acc["within_1ulp"] >= acc["elements"] - max(4, acc["elements"] // 100000), acc
+    # the 1-ulp bar holds everywhere except on near-cancelling elements: measured on GB300,
+    # at most 72 of 115.6 M elements of a 21504 x 5376 layer (0.6 per million), 3 of 8 M at
+    # 6912 x 1152, r = 130, and 1 of 0.2 M at 520 x 384, r = 256
+    assert acc["within_1ulp"] >= acc["elements"] - max(4, acc["elements"] // 1000000), acc
     return acc
 
 
@@ -488,6 +498,6 @@ def test_31b_band_precompute(shape):
         th = synth.make_theta(("31b-layer", shape, layer), out, inp, 128, W0=W0b[band])
         W = aq.aq_precompute(dev_theta(th))
         torch.cuda.synchronize()
-        assert_weight_ok(W, th)
+        assert_weight_ok(W, th, f"31B {shape} layer {layer}")
         del W
     assert aq.aq_device_status() == aq.AQ_OK

@@ -3,10 +3,10 @@
 Some callers cannot hand the library a workspace -- a plugin inside a runtime that owns
 all device memory and passes plugins only their inputs and outputs, or a serving loop
 that forbids allocation once it runs. aq_linear_noalloc serves them from a scratch array
-built into the library. These tests call it through the C ABI and compare it with
-aq_linear (which gets a caller-allocated workspace) on two calls in a row, the second
-with different shapes so that stale scratch from the first would show. This file is
-named so that pytest collects it last.
+built into the library. These tests call it through the C ABI, several times in a row over
+different shapes, paths and ranks so that stale scratch from one call would show in the
+next, and check every result against the fp64 oracle and against aq_linear (which gets a
+caller-allocated workspace). This file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -17,7 +17,7 @@ import torch
 import oracle
 from rank_weight_reconstruction_gb300 import binding, build_lib, synth
 
-from helpers import dev, dev_theta, host_f64
+from helpers import dev, dev_theta, host_f64, x_f64
 
 
 @pytest.fixture(scope="module")
@@ -33,24 +33,42 @@ def _noalloc(lib, theta, x, y):
     return st
 
 
+def _sync_part_of_scratch(lib):
+    """The first AQ_WORKSPACE_SYNC_BYTES of the built-in scratch array, copied out."""
+    out = torch.full((binding.AQ_WORKSPACE_SYNC_BYTES,), 0x5A, dtype=torch.uint8, device="cuda")
+    st = lib.aq_noalloc_scratch_read(out.data_ptr(), 0, out.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == binding.AQ_OK, binding.aq_last_error()
+    return out
+
+
+# (out, in, r), M. The decode calls at in = 1152, r = 32 have a V of 72 KB, too large for
+# every W0-streaming CTA to stage, so a few CTAs compute t = V^T x and publish it through
+# the array's sync part (its counters and fp32 accumulator); the call at 200 tokens takes
+# the tcgen05 GEMM, whose scratch holds t and a transposed V past the sync part.
+CASES = [((300, 264, 24), 5), ((2048, 1152, 32), 1), ((1000, 520, 40), 200), ((2048, 1152, 32), 16),
+         ((2048, 1152, 32), 1)]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_aq_linear_on_two_calls_in_a_row(lib):
+def test_noalloc_matches_oracle_and_aq_linear_on_calls_in_a_row(lib):
     binding.aq_set_path(binding.AQ_PATH_AUTO)
-    # first a decode-sized call (scratch holds t), then a prefill-sized one (scratch holds
-    # t and a transposed V) over different shapes and values
-    cases = [((300, 264, 24), 5), ((1000, 520, 40), 200)]
-    for (out, inp, r), M in cases:
+    assert int(_sync_part_of_scratch(lib).count_nonzero()) == 0
+    for (out, inp, r), M in CASES:
         th = synth.make_theta(("noalloc", out, inp, r), out, inp, r)
         xb = synth.make_x(("noalloc", M, inp), M, inp)
         theta = dev_theta(th)
         x = dev(xb)[:, :inp]
-        y_ref = binding.aq_linear(theta, x)                 # caller-provided workspace
         y = torch.full((M, (out + 7) // 8 * 8), float("nan"), dtype=torch.bfloat16, device="cuda")[:, :out]
         assert _noalloc(lib, theta, x, y) == binding.AQ_OK, binding.aq_last_error()
         torch.cuda.synchronize()
-        got, ref = host_f64(y), host_f64(y_ref)
+        got = host_f64(y)
         assert np.all(np.isfinite(got))
-        assert oracle.within_tolerance(got, ref), oracle.error_stats(got, ref)
+        ref = oracle.linear(*th.f64(), x_f64(xb, inp))
+        assert oracle.within_tolerance(got, ref), ((out, inp, r, M), oracle.error_stats(got, ref))
+        y_ws = host_f64(binding.aq_linear(theta, x))          # caller-provided workspace
+        assert oracle.within_tolerance(got, y_ws), ((out, inp, r, M), oracle.error_stats(got, y_ws))
+        # every completed call leaves the shared array's sync part zero for the next one
+        assert int(_sync_part_of_scratch(lib).count_nonzero()) == 0, (out, inp, r, M)
     assert binding.aq_device_status() == binding.AQ_OK
 
 
@@ -66,3 +84,8 @@ def test_noalloc_rejects_calls_beyond_its_scratch(lib):
     assert st == binding.AQ_ERR_WORKSPACE
     assert "scratch" in binding.aq_last_error()
     assert lib.aq_linear_noalloc(None, 0, 1, 8, 0, 8, None) == binding.AQ_ERR_INVALID_ARG
+    # the read-out hook refuses ranges outside the array without touching the GPU
+    buf = ctypes.create_string_buffer(16)
+    assert lib.aq_noalloc_scratch_read(buf, binding.AQ_NOALLOC_WORKSPACE_BYTES - 8, 16, None) == \
+        binding.AQ_ERR_INVALID_ARG
+    assert lib.aq_noalloc_scratch_read(None, 0, 16, None) == binding.AQ_ERR_INVALID_ARG
