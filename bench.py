@@ -230,7 +230,7 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = ("aq_decode.cu", "aq_kernels.cu", "aq_host.cu", "aq_internal.h", "aq_ptx.cuh")
+KERNEL_SOURCES = ("aq_decode.cu", "aq_decode2.cu", "aq_kernels.cu", "aq_host.cu", "aq_internal.h", "aq_ptx.cuh")
 
 
 def kernel_source_hash():
@@ -469,8 +469,9 @@ def run_ours(args, dist: Dist):
     traffic, traffic_src = captured_traffic(f"decode:{dom[0]}:M{dom[1]}")
     result["roofline"] = {
         "bound": "hbm",
-        "kernel": f"aq_decode_kernel ({dom[0]}, M={dom[1]}): row-owning CTAs, TMA W0 ring, mma.sync, "
-                  "fused s scale and U t epilogue",
+        "kernel": f"aq_decode2_kernel ({dom[0]}, M={dom[1]}): clusters split over K, TMA W0 ring, mma.sync with "
+                  "t = V^T x in the same loop, partial sums pushed through distributed shared memory, fused s "
+                  "scale and U t",
         "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
         "peak_source": f"{pk['source']} copy bandwidth (burst)", "traffic": traffic, "traffic_source": traffic_src,
         "note": "algorithmic bytes of one call / average time per call over 26 back-to-back calls, each on its "
@@ -757,6 +758,8 @@ def run_case(args, dist: Dist):
     torch.cuda.set_device(device)
     build_lib.build()
     aq.load()
+    aq.aq_set_path({"auto": aq.AQ_PATH_AUTO, "decode": aq.AQ_PATH_DECODE, "midm": aq.AQ_PATH_MIDM,
+                    "prefill": aq.AQ_PATH_PREFILL}[args.path])
     out, inp, r = vals[:3]
     th = synth.make_theta(("case", out, inp, r), out, inp, r)
     theta = aq.Theta(W0=dev_bits(th.W0, device)[:, :inp], s=dev_bits(th.s, device),
@@ -826,7 +829,10 @@ def run_sweep(args, dist: Dist):
     build_lib.build()
     aq.load()
     pk = peaks()
-    names = {aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_PREFILL: "gemm"}
+    names = {aq.AQ_PATH_DECODE: "decode", aq.AQ_PATH_MIDM: "midm", aq.AQ_PATH_PREFILL: "prefill"}
+    forced = {"auto": aq.AQ_PATH_AUTO, "decode": aq.AQ_PATH_DECODE, "midm": aq.AQ_PATH_MIDM,
+              "prefill": aq.AQ_PATH_PREFILL}[args.path]
+    aq.aq_set_path(forced)
     points = []
     for sname, (out, inp) in SWEEP_SHAPES.items():
         xs = {M: dev_bits(synth.make_x(("sweep", M, inp), M, inp), device)[:, :inp] for M in SWEEP_MS}
@@ -838,6 +844,8 @@ def run_sweep(args, dist: Dist):
             thetas = [Theta(W0=(w0 if c == 0 else w0.clone())[:, :inp], s=s_, U=U[:, :r] if r else None,
                             V=V[:, :r] if r else None) for c in range(SWEEP_COPIES)]
             for M in SWEEP_MS:
+                if forced == aq.AQ_PATH_DECODE and M > aq.aq_decode_max_m():
+                    continue
                 x = xs[M]
                 y = torch.empty(M, out, dtype=torch.bfloat16, device=device)
                 ws = aq.new_workspace(aq.aq_linear_workspace_bytes(thetas[0], M), device)
@@ -859,7 +867,8 @@ def run_sweep(args, dist: Dist):
                                else "tensor", "frac_roofline": round(t_star / us, 4)})
             del thetas, w0
             torch.cuda.empty_cache()
-    return {"sweep": "rank/shape sweep, gate-like 6912x1152 and down-like 1152x6912", "peaks": pk,
+    aq.aq_set_path(aq.AQ_PATH_AUTO)
+    return {"sweep": "rank/shape sweep, gate-like 6912x1152 and down-like 1152x6912", "path": args.path, "peaks": pk,
             "copies_per_point": SWEEP_COPIES, "status": aq.aq_device_status(), "points": points}
 
 
@@ -898,6 +907,8 @@ def main():
                     help="run only the captured decode step (for kernel-profiler launch lists)")
     ap.add_argument("--sweep", action="store_true",
                     help="the rank/shape sweep (gate-like and down-like, r in 0..256, M in 1..4096)")
+    ap.add_argument("--path", choices=["auto", "decode", "midm", "prefill"], default="auto",
+                    help="--sweep / --case: force one path (aq_set_path) to map where the paths cross")
     ap.add_argument("--case", default=None,
                     help="time one call instead: linear:out,in,r,M, gateup:out,in,r,M or precompute:out,in,r "
                          "(profiler captures)")

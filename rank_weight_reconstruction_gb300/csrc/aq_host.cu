@@ -370,6 +370,140 @@ aq_status launch_or_fail(cudaError_t e, const char* what) {
   return AQ_OK;
 }
 
+// Cluster decode plan (M <= 16). Returns false when the call does not fit it (the caller then
+// plans the row-owning decode kernel); otherwise launches and reports the launch's status.
+//   * C = cluster size = K slices of about nine 64-wide k blocks each;
+//   * one CTA per SM: SMs / C clusters, shared among the families in proportion to their rows,
+//     rc <= 256 rows per cluster;
+//   * every region in half of an SM's shared memory, so that consecutive calls' CTAs co-reside.
+bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, int64_t ldx, void* const* ys,
+                  const int64_t* ldys, const DevInfo* dev, cudaStream_t cs, aq_status* st) {
+  const int K = th[0]->in;
+  if (M < 1 || M > 16 || K % kBK != 0) return false;
+  int max_r16 = 0;
+  int64_t rows_total = 0;
+  for (int j = 0; j < n; ++j) {
+    if (th[j]->r > 32) return false;
+    max_r16 = std::max(max_r16, static_cast<int>(round_up(th[j]->r, 16)));
+    rows_total += th[j]->out;
+  }
+  const int nkb = K / kBK;
+  const size_t half = std::min<size_t>(dev->smem_optin, 227 * 1024) / 2 - 1024;
+  Dec2Params dp = {};
+  size_t smem = 0;
+  int clusters = 0;
+  bool fits = false;
+  // Slices of about nine 64-wide k blocks (measured on the Gemma-3-1B decode step: one slice per
+  // CTA, i.e. no cluster, was twice as slow for the q/k/v and o projections), more when the plan
+  // does not fit half of an SM. After the loop the CTAs push their partial sums into each
+  // other's receive areas (distributed shared-memory stores), so the exchange costs one cluster
+  // barrier and no remote read.
+  for (int want = std::max(1, std::min(kDec2MaxC, (nkb + 4) / 9)); want <= kDec2MaxC && !fits; ++want) {
+    dp = Dec2Params{};
+    dp.M = static_cast<int32_t>(M);
+    dp.K = K;
+    dp.nkb = nkb;
+    dp.kb_per = static_cast<int32_t>(ceil_div(nkb, want));
+    const int C = static_cast<int>(ceil_div(nkb, dp.kb_per));   // no empty slice
+    if (C != want) continue;
+    dp.C = C;
+    // clusters: one CTA per SM, at least 8 rows per cluster, every family at least one
+    const int64_t n_cl = std::max<int64_t>(n, std::min<int64_t>(dev->sms / C, ceil_div(rows_total, 8)));
+    int64_t cnt[kMaxSeg] = {};
+    int64_t used = 0;
+    for (int j = 0; j < n; ++j) {
+      cnt[j] = std::max<int64_t>(1, n_cl * th[j]->out / rows_total);
+      used += cnt[j];
+    }
+    while (used < n_cl) {
+      int best = 0;
+      for (int j = 1; j < n; ++j)
+        if (static_cast<int64_t>(th[j]->out) * cnt[best] > static_cast<int64_t>(th[best]->out) * cnt[j]) best = j;
+      ++cnt[best];
+      ++used;
+    }
+    int rc_max = 0, kg_max = 1;
+    bool rc_ok = true;
+    clusters = 0;
+    for (int j = 0; j < n; ++j) {
+      Dec2Seg& sg = dp.seg[dp.nseg++];
+      sg.rc = static_cast<int32_t>(ceil_div(th[j]->out, cnt[j]));
+      if (sg.rc > 256) rc_ok = false;
+      cnt[j] = ceil_div(th[j]->out, sg.rc);
+      sg.cl_begin = clusters;
+      clusters += static_cast<int>(cnt[j]);
+      sg.s = static_cast<const uint16_t*>(th[j]->s);
+      sg.U = static_cast<const uint16_t*>(th[j]->U);
+      sg.ldu = th[j]->ld_u;
+      sg.y = static_cast<uint16_t*>(ys[j]);
+      sg.ldy = ldys[j];
+      sg.rows = th[j]->out;
+      sg.r = th[j]->r;
+      sg.r16 = static_cast<int32_t>(round_up(th[j]->r, 16));
+      rc_max = std::max(rc_max, static_cast<int>(sg.rc));
+      const int nslab = static_cast<int>(ceil_div(sg.rc, 16));
+      kg_max = std::max(kg_max, nslab >= 8 ? 1 : 8 / nslab);
+    }
+    if (!rc_ok) continue;
+    // shared memory: header, x slice, V slice, U rows and s of the finished rows, t, W0 ring
+    // (x box odd where the tensor has the block: its eight token rows of an ldmatrix then land
+    // in distinct banks)
+    dp.xkb = (dp.kb_per | 1) <= nkb ? (dp.kb_per | 1) : dp.kb_per;
+    dp.x_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.xkb) * M * 128, 1024));
+    dp.vrow = max_r16;
+    const int64_t kslice = static_cast<int64_t>(dp.kb_per) * kBK;
+    const int64_t nvb = ceil_div(kslice, 256);
+    dp.vbox = static_cast<int32_t>(round_up(ceil_div(kslice, nvb), 16));
+    dp.v_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(nvb * dp.vbox * dp.vrow * 2, 1024)) : 0u;
+    const int64_t rf_max = ceil_div(rc_max, C);
+    dp.u_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(rf_max * max_r16 * 2, 1024)) : 0u;
+    dp.s_bytes = static_cast<uint32_t>(round_up((rf_max + 15) / 8 * 16, 1024));
+    dp.tf_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(static_cast<int64_t>(max_r16) * M * 4, 1024)) : 0u;
+    dp.rx_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(C) * (rf_max + max_r16) * M * 4, 1024));
+    const size_t fixed =
+        kHeaderBytes + kSmemSlack + dp.x_bytes + dp.v_bytes + dp.u_bytes + dp.s_bytes + dp.tf_bytes + dp.rx_bytes;
+    if (fixed >= half) continue;
+    const size_t ring = half - fixed;
+    dp.kbox = 0;
+    int kb_start = std::min(9, static_cast<int>(dp.kb_per));
+    if (kb_start % 2 == 0) --kb_start;   // odd, and never past the slice
+    for (int kb = kb_start; kb >= 1; kb -= 2) {
+      const size_t sb = static_cast<size_t>(round_up(static_cast<int64_t>(kb) * rc_max * 128, 1024));
+      if (ring / sb >= 2 || kb == 1) {
+        dp.kbox = kb;
+        dp.stage_bytes = static_cast<uint32_t>(sb);
+        dp.stages = static_cast<int32_t>(std::min<size_t>(kMaxStages, ring / sb));
+        break;
+      }
+    }
+    if (dp.kbox < 1 || dp.kbox > dp.kb_per || dp.stages < 2) continue;
+    // the partial sums of W0 x and t reuse the ring once the loop is done
+    const size_t exch = (static_cast<size_t>(kg_max) * rc_max * M + static_cast<size_t>(9) * max_r16 * M) * 4;
+    const size_t ring_used = static_cast<size_t>(dp.stages) * dp.stage_bytes;
+    if (exch > ring_used) continue;
+    smem = fixed + ring_used;
+    fits = true;
+  }
+  if (!fits) return false;
+  const int C = dp.C;
+  // tensor maps
+  if ((*st = tmap_3d(&dp.tm_x, x, K, M, ldx, dp.xkb, static_cast<int>(M), "x")) != AQ_OK) return true;
+  for (int j = 0; j < n; ++j) {
+    Dec2Seg& sg = dp.seg[j];
+    if ((*st = tmap_3d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, dp.kbox, sg.rc, "W0")) != AQ_OK) return true;
+    if (th[j]->r > 0 &&
+        (*st = tmap_2d_plain(&sg.tm_v, th[j]->V, th[j]->r, K, th[j]->ld_v, dp.vrow, dp.vbox, "V")) != AQ_OK)
+      return true;
+  }
+  dp.x = static_cast<const uint16_t*>(x);
+  dp.ldx = ldx;
+  dp.status = dev->status;
+  dp.timeout_ns = kTimeoutNs;
+  *st = launch_or_fail(launch_decode2(dp, clusters * C, smem, cs, true), "launch cluster decode kernel");
+  if (*st == AQ_OK) t_last_path = AQ_PATH_DECODE;
+  return true;
+}
+
 aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M, int64_t ldx,
                       void* const* ys, const int64_t* ldys, void* ws, size_t ws_bytes, void* stream) {
   const char* who = n == 1 ? "aq_linear" : "aq_linear_qkv";
@@ -449,6 +583,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
   if (decode) {
+    if (plan_decode2(th, n, x, M, ldx, ys, ldys, dev, cs, &st)) return st;
     // ---- one launch: W0 streamed by row-owning CTAs, t = V^T x by a few extra CTAs ----
     DecodeParams dp = {};
     dp.x = static_cast<const uint16_t*>(x);
@@ -699,7 +834,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   int split = 1;
   int call_max_r = 0;
   for (int j = 0; j < n; ++j) call_max_r = std::max(call_max_r, th[j]->r);
-  if (main_tiles * 2 <= dev->sms && nkb >= 2 * kSplitMinKb && call_max_r <= kSplitMaxRank && ws &&
+  if (main_tiles * 2 <= dev->sms && nkb >= 2 * kSplitMinKb && call_max_r <= kSplitMaxRank && M <= 65535 && ws &&
       (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && wl.split_slice > 0) {
     // as many slices as keep all tiles (the t tiles included) within one wave
     const size_t room = ws_bytes > wl.split_base ? ws_bytes - wl.split_base : 0;

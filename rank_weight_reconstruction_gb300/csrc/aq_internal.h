@@ -104,8 +104,7 @@ struct FinalizeParams {
   int64_t pz_slice;      // elements between slices of pz (M * ld_pz)
   int64_t pt_slice;
 };
-constexpr int kFinRows = 64;       // outputs per finalize block (one per thread)
-constexpr int kFinTok = 8;         // tokens per finalize block
+constexpr int kFinRows = 256;      // outputs per finalize block: consecutive rows of one token
 constexpr int kFinMaxR = 256;      // largest rank the finalize stages in shared memory
 constexpr int kSplitMinKb = 4;     // k blocks per slice at least
 constexpr int kMaxSplit = 16;
@@ -198,6 +197,51 @@ struct DecodeParams {
   uint64_t timeout_ns;
 };
 
+// Cluster decode kernel (M <= 16): a cluster of C CTAs owns `rc` rows of one family, CTA q of
+// the cluster covers K slice q (k blocks [q * kb_per, (q + 1) * kb_per)); t = V^T x is formed in
+// the same mma loop; partial sums are added across the cluster through distributed shared
+// memory.
+constexpr int kDec2MaxC = 8;   // largest cluster (K slices) of the cluster decode kernel
+constexpr int kDec2Batch = 4;  // outputs per thread whose remote partial sums are loaded together
+struct Dec2Seg {
+  CUtensorMap tm_w;    // W0 as {64, K/64, rows}, box {64, kbox, rc}, 128-byte swizzle
+  CUtensorMap tm_v;    // V [in, r]: 2-D, no swizzle, box {vrow, vbox} (zero past r)
+  const uint16_t* s;
+  const uint16_t* U;
+  int64_t ldu;
+  uint16_t* y;
+  int64_t ldy;
+  int32_t rows;
+  int32_t r;
+  int32_t r16;         // round_up(r, 16): rows of V^T in the mma tiles, width of staged U rows
+  int32_t rc;          // rows per cluster (<= 256)
+  int32_t cl_begin;    // first cluster of this family
+};
+
+struct Dec2Params {
+  CUtensorMap tm_x;    // x as {64, K/64, M}, box {64, xkb, M}, 128-byte swizzle
+  Dec2Seg seg[kMaxSeg];
+  const uint16_t* x;   // for L2 prefetch hints
+  int64_t ldx;
+  int32_t nseg;
+  int32_t M;
+  int32_t K;           // a multiple of 64
+  int32_t nkb;
+  int32_t C;           // cluster size = K slices
+  int32_t kb_per;      // k blocks per slice
+  int32_t kbox;        // k blocks per W0 stage (odd: conflict-free ldmatrix rows)
+  int32_t xkb;         // k blocks of the x box (>= kb_per, odd)
+  int32_t vrow;        // elements per staged V row (>= every family's r16)
+  int32_t vbox;        // V rows per TMA box (multiple of 16, <= 256)
+  int32_t stages;
+  uint32_t stage_bytes;  // kbox * max rc * 128, 1 KB aligned
+  uint32_t x_bytes, v_bytes, u_bytes, s_bytes, tf_bytes;  // shared-memory regions, 1 KB aligned
+  uint32_t rx_bytes;     // receive area of the cluster exchange: [C][rf][M] + [C][r16][M] fp32
+  int32_t* status;
+  uint64_t timeout_ns;
+};
+static_assert(sizeof(Dec2Params) <= 4096, "kernel parameters are limited to 4 KB");
+
 // V [in, r] -> Vt [r, in] (bf16) for the prefill t GEMM.
 struct TransposeSeg {
   const uint16_t* V;
@@ -253,6 +297,8 @@ constexpr int kYStageTotal = 4 * 2 * kYStageBytes;
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl);
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
+cudaError_t launch_decode2(const Dec2Params& p, int grid, size_t smem, cudaStream_t st, bool pdl);
+cudaError_t configure_decode2(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
                               bool pdl);

@@ -679,67 +679,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
 // ------------------------------------------------------------------------------------
 // Split-K finalize: y[m, o] = RN(s[o] * sum_k z_k[m, o] + sum_j U[o, j] * t[m, j]) with
 // t[m, j] = sum_k t_k[m, j], every sum over the slices in slice order (deterministic).
-// One thread per output row, kFinTok tokens per block; U t on the FP32 pipes (at most
-// r FMAs per output, a small fraction of the GEMM's work at the shapes that split).
+// One thread per output (kFinRows consecutive rows of one token per block: the partial sums
+// and y are read and written in 128-byte lines), the U row in registers, t of the block's
+// token summed once into shared memory. The work per output is ksplit loads and r FMAs, so
+// the kernel is a few round trips deep; enough threads keep those round trips overlapped.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kFinRows) aq_finalize_kernel(const __grid_constant__ FinalizeParams p) {
-  __shared__ float ts[kFinTok][kFinMaxR];
+  __shared__ float ts[kFinMaxR];
   int si = 0;
 #pragma unroll
   for (int j = 1; j < kMaxSeg; ++j)
     if (j < p.nseg && static_cast<int>(blockIdx.x) >= p.seg[j].block_begin) si = j;
   const FinalizeSeg& sg = p.seg[si];
   const int o = (static_cast<int>(blockIdx.x) - sg.block_begin) * kFinRows + static_cast<int>(threadIdx.x);
-  const int m0 = static_cast<int>(blockIdx.y) * kFinTok;
+  const int m = static_cast<int>(blockIdx.y);
+  const bool live = o < sg.rows;
+  // weights before the dependency wait: this row's U and s
+  float u[kSplitMaxRank];
+#pragma unroll
+  for (int j = 0; j < kSplitMaxRank; ++j) u[j] = 0.0f;
+  if (live && sg.r > 0) {
+    const uint16_t* urow = sg.U + static_cast<int64_t>(o) * sg.ldu;
+#pragma unroll
+    for (int j = 0; j < kSplitMaxRank; ++j)
+      if (j < sg.r) u[j] = bf16_to_f32(urow[j]);
+  }
+  const float sc = (live && sg.s) ? bf16_to_f32(sg.s[o]) : 1.0f;
   pdl_wait_prior_grid();   // the partial sums are the previous grid's output
-  for (int idx = threadIdx.x; idx < kFinTok * sg.r; idx += kFinRows) {
-    const int mm = idx / sg.r, k = idx - mm * sg.r;
+  if (static_cast<int>(threadIdx.x) < sg.r) {
     float v = 0.0f;
-    if (m0 + mm < p.M)
-      for (int ks = 0; ks < p.ksplit; ++ks) v += sg.pt[ks * p.pt_slice + static_cast<int64_t>(m0 + mm) * p.ld_pt + k];
-    ts[mm][k] = v;
+    for (int ks = 0; ks < p.ksplit; ++ks)
+      v += sg.pt[ks * p.pt_slice + static_cast<int64_t>(m) * p.ld_pt + threadIdx.x];
+    ts[threadIdx.x] = v;
+  }
+  float z = 0.0f;
+  if (live) {
+    const float* pz = sg.pz + static_cast<int64_t>(m) * p.ld_pz + o;
+#pragma unroll 4
+    for (int ks = 0; ks < p.ksplit; ++ks) z += pz[ks * p.pz_slice];
   }
   __syncthreads();
   pdl_launch_dependents();
-  if (o >= sg.rows) return;
-  float acc[kFinTok];
+  if (!live) return;
+  float lr = 0.0f;
 #pragma unroll
-  for (int mm = 0; mm < kFinTok; ++mm) acc[mm] = 0.0f;
-  if (sg.r > 0) {
-    // U row o in 16-byte pieces (U is 16-byte aligned with ld_u a multiple of 8); the piece
-    // that would pass r is read element by element, so no read leaves the row's r values
-    const uint16_t* urow = sg.U + static_cast<int64_t>(o) * sg.ldu;
-    const int r8 = sg.r & ~7;
-#pragma unroll 2
-    for (int k0 = 0; k0 < r8; k0 += 8) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(urow + k0));
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float u0 = __uint_as_float(ww[e] << 16), u1 = __uint_as_float(ww[e] & 0xFFFF0000u);
-#pragma unroll
-        for (int mm = 0; mm < kFinTok; ++mm) {
-          acc[mm] = fmaf(u0, ts[mm][k0 + 2 * e], acc[mm]);
-          acc[mm] = fmaf(u1, ts[mm][k0 + 2 * e + 1], acc[mm]);
-        }
-      }
-    }
-    for (int k = r8; k < sg.r; ++k) {
-      const float u = bf16_to_f32(urow[k]);
-#pragma unroll
-      for (int mm = 0; mm < kFinTok; ++mm) acc[mm] = fmaf(u, ts[mm][k], acc[mm]);
-    }
-  }
-  const float sc = sg.s ? bf16_to_f32(sg.s[o]) : 1.0f;
-#pragma unroll
-  for (int mm = 0; mm < kFinTok; ++mm) {
-    const int m = m0 + mm;
-    if (m < p.M) {
-      float z = 0.0f;
-      for (int ks = 0; ks < p.ksplit; ++ks) z += sg.pz[ks * p.pz_slice + static_cast<int64_t>(m) * p.ld_pz + o];
-      sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, z, acc[mm]));
-    }
-  }
+  for (int j = 0; j < kSplitMaxRank; ++j)
+    if (j < sg.r) lr = fmaf(u[j], ts[j], lr);
+  sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, z, lr));
 }
 
 // ------------------------------------------------------------------------------------
@@ -1107,7 +1093,7 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n) {
 
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<FinalizeParams*>(&p)};
-  const dim3 grid(blocks, (p.M + kFinTok - 1) / kFinTok);
+  const dim3 grid(blocks, p.M);
   return launch_ex(reinterpret_cast<const void*>(&aq_finalize_kernel), grid, dim3(kFinRows), 0, st, pdl, args);
 }
 
@@ -1139,6 +1125,7 @@ cudaError_t configure_kernels(int device, size_t max_smem) {
   if ((e = cudaFuncSetAttribute(aq_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = configure_decode(max_smem))) return e;
+  if ((e = configure_decode2(max_smem))) return e;
   if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
     return e;
   return cudaSuccess;
