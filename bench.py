@@ -760,7 +760,7 @@ def run_case(args, dist: Dist):
     aq.load()
     aq.aq_set_path({"auto": aq.AQ_PATH_AUTO, "decode": aq.AQ_PATH_DECODE, "midm": aq.AQ_PATH_MIDM,
                     "prefill": aq.AQ_PATH_PREFILL}[args.path])
-    out, inp, r = vals[:3]
+    out, inp, r = vals[:3] if kind != "qkv" else (vals[0], vals[2], vals[3])
     th = synth.make_theta(("case", out, inp, r), out, inp, r)
     theta = aq.Theta(W0=dev_bits(th.W0, device)[:, :inp], s=dev_bits(th.s, device),
                      U=dev_bits(th.U, device)[:, :r] if r else None, V=dev_bits(th.V, device)[:, :r] if r else None)
@@ -783,13 +783,28 @@ def run_case(args, dist: Dist):
         run = lambda: aq.aq_linear_multi([theta, theta2], x, ys=ys, workspace=ws)
         work = {"bytes": 2 * linear_bytes(out, inp, r, M) - 2 * M * inp,
                 "flops": 2 * linear_flops(out, inp, r, M)}
+    elif kind == "qkv":
+        # q/k/v of one layer over one x: qkv:out_q,out_kv,in,r,M (the k and v families have out_kv rows)
+        out_q, out_kv, inp, r, M = vals
+        ths = [synth.make_theta(("case", "qkv", j, o, inp, r), o, inp, r) for j, o in enumerate((out_q, out_kv, out_kv))]
+        thetas = [aq.Theta(W0=dev_bits(t.W0, device)[:, :inp], s=dev_bits(t.s, device),
+                           U=dev_bits(t.U, device)[:, :r] if r else None, V=dev_bits(t.V, device)[:, :r] if r else None)
+                  for t in ths]
+        x = dev_bits(synth.make_x(("case", M), M, inp), device)[:, :inp]
+        Y = torch.empty(M, out_q + 2 * out_kv, dtype=torch.bfloat16, device=device)
+        ys = [Y[:, :out_q], Y[:, out_q:out_q + out_kv], Y[:, out_q + out_kv:]]
+        ws = aq.new_workspace(aq.aq_linear_workspace_bytes(thetas, M), device)
+        run = lambda: aq.aq_linear_qkv(thetas, x, ys=ys, workspace=ws)
+        work = {"bytes": qkv_bytes([(out_q, inp), (out_kv, inp), (out_kv, inp)], r, M),
+                "flops": sum(linear_flops(o, inp, r, M) for o in (out_q, out_kv, out_kv))}
+        vals = [out_q, inp, r, M]
     elif kind == "precompute":
         W = torch.empty(out, (inp + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :inp]
         run = lambda: aq.aq_precompute(theta, W_eff=W)
         work = {"bytes": precompute_bytes(out, inp, r)}
     else:
-        raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M, gateup:out,in,r,M or "
-                         "precompute:out,in,r)")
+        raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M, gateup:out,in,r,M, "
+                         "qkv:out_q,out_kv,in,r,M or precompute:out,in,r)")
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()
@@ -910,8 +925,8 @@ def main():
     ap.add_argument("--path", choices=["auto", "decode", "midm", "prefill"], default="auto",
                     help="--sweep / --case: force one path (aq_set_path) to map where the paths cross")
     ap.add_argument("--case", default=None,
-                    help="time one call instead: linear:out,in,r,M, gateup:out,in,r,M or precompute:out,in,r "
-                         "(profiler captures)")
+                    help="time one call instead: linear:out,in,r,M, gateup:out,in,r,M, qkv:out_q,out_kv,in,r,M "
+                         "or precompute:out,in,r (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -76,6 +76,12 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
+// 16-byte store into a peer's shared memory (16-byte aligned shared::cluster address).
+__device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // Barrier of the 256 mma warps (named barrier 1). Every consumer thread reaches each call site
 // on every path, a failed wait included, so it always completes.
 __device__ __forceinline__ void cons_bar() { named_bar_sync(1, kDecConsumers); }
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   uint8_t* us = vs + p.v_bytes;                      // U rows this CTA finishes: [rf][r16] bf16
   uint8_t* ss = us + p.u_bytes;                      // s of those rows, bf16
   float* tf = reinterpret_cast<float*>(ss + p.s_bytes);  // t over the whole K: [r16][M] fp32
-  // what the peers push: per sender rank, W0 x of the rows this CTA finishes [C][rf][M], then
+  // what the peers push: per sender rank, W0 x of the rows this CTA finishes [C][M][rf4], then
   // t [C][r16][M]; never aliased, so a peer may push while this CTA is still in its loop
   float* zrx = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tf) + p.tf_bytes);
   uint8_t* ring = reinterpret_cast<uint8_t*>(zrx) + p.rx_bytes;
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   const int M = p.M;
   // rows this CTA finishes
   const int rf = (Rc + C - 1) / C;
+  const int rf4 = (rf + 3) & ~3;   // rows per token in the receive area: 16-byte pushes
   const int f0 = rank * rf;
   const int f_n = max(0, min(rf, rows_here - f0));
 
@@ -340,7 +347,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
     cons_bar();
     float* zex = reinterpret_cast<float*>(ring);               // [kg][M][Rc]: rows fastest
     float* tex = zex + static_cast<size_t>(kg) * Rc * M;       // [8][r16][M]
-    float* tloc = tex + static_cast<size_t>(8) * r16 * M;      // [r16][M]
     if (active) {
 #pragma unroll
       for (int a = 0; a < 2; ++a)
@@ -370,40 +376,38 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
               }
     }
     cons_bar();
-    // This CTA's sums over its slice: W0 x over the k-block groups (in place, into group 0) and t
-    // over the eight warps, in a fixed order.
-    if (kg > 1 && rows_here > 0) {
-      const size_t grp = static_cast<size_t>(Rc) * M;
-      for (int idx = ct; idx < Rc * M; idx += kDecConsumers) {
-        float v = zex[idx];
-        for (int k = 1; k < kg; ++k) v += zex[k * grp + idx];
-        zex[idx] = v;
-      }
-    }
-    for (int idx = ct; idx < r16 * M; idx += kDecConsumers) {
-      float v = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v += tex[static_cast<size_t>(w) * r16 * M + idx];
-      tloc[idx] = v;
-    }
-    cons_bar();
     // push: the rows peer q finishes go to its receive area at this CTA's rank, and t to every
-    // peer (this CTA included); stores only, no remote read
+    // peer (this CTA included); each pushed value is this CTA's sum over its k-block groups (W0 x)
+    // or its eight warps (t), in a fixed order. Stores only, no remote read.
     {
-      // receive areas: z [C][M][rf] (rows fastest), then t [C][r16][M]
-      const int zn = rf * M, tn = r16 * M;
+      // receive areas: z [C][M][rf4] (rows fastest), then t [C][r16][M]; 16-byte pushes
+      const int zn = rf4 * M, tn = r16 * M;
+      const size_t grp = static_cast<size_t>(Rc) * M;
       const uint32_t zr_me = smem_u32(zrx) + static_cast<uint32_t>(rank * zn) * 4u;
       const uint32_t tr_me = smem_u32(zrx) + static_cast<uint32_t>(C * zn + rank * tn) * 4u;
-      for (int idx = ct; idx < C * zn; idx += kDecConsumers) {
-        const int q = idx / zn, e = idx - q * zn;   // e = tok * rf + rr
-        const int tok = e / rf, rr = e - tok * rf;
-        const int row = q * rf + rr;
-        const float v = row < rows_here ? zex[tok * Rc + row] : 0.0f;
-        st_dsmem_f32(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v);
+      const int zq = zn / 4;
+      for (int idx = ct; idx < C * zq; idx += kDecConsumers) {
+        const int q = idx / zq, e = (idx - q * zq) * 4;   // e = tok * rf4 + rr, rr a multiple of 4
+        const int tok = e / rf4, rr = e - tok * rf4;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = q * rf + rr + i;
+          v[i] = 0.0f;
+          if (rr + i < rf && row < rows_here)
+            for (int k = 0; k < kg; ++k) v[i] += zex[k * grp + tok * Rc + row];
+        }
+        st_dsmem_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
-      for (int idx = ct; idx < C * tn; idx += kDecConsumers) {
-        const int q = idx / tn, e = idx - q * tn;
-        st_dsmem_f32(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), tloc[e]);
+      const int tq = tn / 4;
+      for (int idx = ct; idx < C * tq; idx += kDecConsumers) {
+        const int q = idx / tq, e = (idx - q * tq) * 4;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] += tex[static_cast<size_t>(w) * tn + e + i];
+        st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
     }
   }
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   ok = ok && !*reinterpret_cast<volatile int*>(abort_flag);
   if (warp > 0) {
     const int ct = threadIdx.x - 32;
-    const int zn = rf * M, tn = r16 * M;
+    const int zn = rf4 * M, tn = r16 * M;
     const float* zr = zrx;
     const float* tr = zrx + static_cast<size_t>(C) * zn;
     // t = sum over the cluster's slices, in rank order
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       for (int idx = ct; idx < f_n * M; idx += kDecConsumers) {
         const int tok = idx / f_n, rr = idx - tok * f_n;   // rows fastest: coalesced stores of y
         float z = 0.0f;
-        for (int q = 0; q < C; ++q) z += zr[q * zn + tok * rf + rr];
+        for (int q = 0; q < C; ++q) z += zr[q * zn + tok * rf4 + rr];
         // U row in 16-byte pieces (the row stride r16 * 2 is a multiple of 32 bytes)
         float lr = 0.0f;
         const uint4* ur = reinterpret_cast<const uint4*>(urow_base + rr * r16);

@@ -459,7 +459,7 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
     dp.u_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(rf_max * max_r16 * 2, 1024)) : 0u;
     dp.s_bytes = static_cast<uint32_t>(round_up((rf_max + 15) / 8 * 16, 1024));
     dp.tf_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(static_cast<int64_t>(max_r16) * M * 4, 1024)) : 0u;
-    dp.rx_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(C) * (rf_max + max_r16) * M * 4, 1024));
+    dp.rx_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(C) * (round_up(rf_max, 4) + max_r16) * M * 4, 1024));
     const size_t fixed =
         kHeaderBytes + kSmemSlack + dp.x_bytes + dp.v_bytes + dp.u_bytes + dp.s_bytes + dp.tf_bytes + dp.rx_bytes;
     if (fixed >= half) continue;
@@ -478,7 +478,7 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
     }
     if (dp.kbox < 1 || dp.kbox > dp.kb_per || dp.stages < 2) continue;
     // the partial sums of W0 x and t reuse the ring once the loop is done
-    const size_t exch = (static_cast<size_t>(kg_max) * rc_max * M + static_cast<size_t>(9) * max_r16 * M) * 4;
+    const size_t exch = (static_cast<size_t>(kg_max) * rc_max * M + static_cast<size_t>(8) * max_r16 * M) * 4;
     const size_t ring_used = static_cast<size_t>(dp.stages) * dp.stage_bytes;
     if (exch > ring_used) continue;
     smem = fixed + ring_used;

@@ -236,7 +236,7 @@ struct Dec2Params {
   int32_t stages;
   uint32_t stage_bytes;  // kbox * max rc * 128, 1 KB aligned
   uint32_t x_bytes, v_bytes, u_bytes, s_bytes, tf_bytes;  // shared-memory regions, 1 KB aligned
-  uint32_t rx_bytes;     // receive area of the cluster exchange: [C][rf][M] + [C][r16][M] fp32
+  uint32_t rx_bytes;     // receive area of the cluster exchange: [C][M][round_up(rf, 4)] + [C][r16][M] fp32
   int32_t* status;
   uint64_t timeout_ns;
 };
