@@ -65,7 +65,8 @@ typedef enum aq_status {
   AQ_ERR_WORKSPACE = 5,    /* workspace missing, misaligned or smaller than required */
   AQ_ERR_OVERLAP = 6,      /* an output buffer overlaps an input buffer */
   AQ_ERR_CUDA = 7,         /* a CUDA runtime or driver call failed (message in aq_last_error) */
-  AQ_ERR_TIMEOUT = 8       /* device side: a bounded wait inside a kernel expired */
+  AQ_ERR_TIMEOUT = 8,      /* device side: a bounded wait inside a kernel expired */
+  AQ_ERR_NUMERIC = 9       /* aq_randomized_svd: a factorisation met a non-positive pivot */
 } aq_status;
 
 /* One projection's theta bundle. All pointers are device pointers to bf16 data.
@@ -227,11 +228,12 @@ aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
  *                    read once for all tokens; a transpose of V and t = x V inside the launch;
  *   AQ_PATH_PREFILL  the tcgen05 GEMM with 128 tokens per tile as the accumulator lanes and
  *                    output rows as N (CTA pairs, 2-SM MMAs), for large M.
- * AQ_PATH_AUTO picks by M and size: decode up to 32 tokens, except that from 16 tokens a call
- * whose W0 (summed over its families) holds 128 MB or more takes the mid-M GEMM; mid-M up to
- * 512 tokens; prefill above. The other values force a path for tests: mid-M and prefill work
- * for every M, decode for M <= aq_decode_max_m() (larger M returns AQ_ERR_UNSUPPORTED).
- * Process-wide setting. */
+ * AQ_PATH_AUTO picks by M and size, as measured on GB300: decode up to 32 tokens, except that
+ * from 16 tokens a call whose W0 (summed over its families) holds 128 MB or more takes the
+ * prefill GEMM; above 32 tokens the prefill GEMM, except that calls of 1024 to 4096 tokens
+ * whose families have at most 16 tiles of 128 rows over K >= 4096 take the AQ_PATH_MIDM GEMM.
+ * The other values force a path for tests: mid-M and prefill work for every M, decode for
+ * M <= aq_decode_max_m() (larger M returns AQ_ERR_UNSUPPORTED). Process-wide setting. */
 typedef enum aq_path { AQ_PATH_AUTO = 0, AQ_PATH_DECODE = 1, AQ_PATH_PREFILL = 2, AQ_PATH_MIDM = 3 } aq_path;
 aq_status aq_set_path(aq_path path);
 int32_t aq_decode_max_m(void);
@@ -241,6 +243,45 @@ int32_t aq_last_path(void);
 
 /* Number of kernel launches the last successful aq_* call on this thread enqueued. */
 int32_t aq_last_launch_count(void);
+
+/* ---------------------------------------------------------------------------------
+ * The decomposition that produces a bundle ("How attnquant works", "How the decomposition
+ * produces s, U, and V"), run on the GPU in double precision. It is a load-time step: every
+ * call is stream-ordered like the others, and aq_randomized_svd synchronises its stream at
+ * the end to report a numerical breakdown.
+ * --------------------------------------------------------------------------------- */
+
+/* W0 of one band: W0[o, i] = RN_bf16( (sum over l of weights[l][o, i]) / L ), the sum in fp64
+ * in layer order ("W0 is the mean of the projection weights across the layers that share it").
+ *   weights  host array of L device pointers to bf16 [out, in] matrices, row stride ld
+ *   W0       device bf16 [out, in], row stride ld_w0
+ * 1 <= L <= 256. */
+aq_status aq_band_mean(const void* const* weights, int32_t L, int32_t out, int32_t in, int64_t ld, void* W0,
+                       int64_t ld_w0, void* stream);
+
+/* Per-row least-squares scale of W0 toward one layer's weight and the residual it leaves:
+ *   s[o]       = RN_bf16( (w[o] . W0[o]) / (W0[o] . W0[o]) ), 1 for a W0 row of zeros
+ *   resid[o,i] = w[o,i] - s[o] * W0[o,i]   (fp64, against the stored bf16 s)
+ * The dot products accumulate in fp64 in a fixed order. weight and W0 are device bf16 [out, in]
+ * with row strides ldw and ld_w0, s device bf16 [out], resid device fp64 [out, ld_r]. */
+aq_status aq_ls_residual(const void* weight, int64_t ldw, const void* W0, int64_t ld_w0, int32_t out, int32_t in,
+                         void* s, double* resid, int64_t ld_r, void* stream);
+
+/* Rank-r factors of A [m, n] (device fp64, row stride lda) by the randomized SVD the pages name
+ * (Halko, Martinsson and Tropp, 2009): Y = A Omega, Q = orth(Y), power_iters times
+ * Q = orth(A orth(A^T Q)), B = Q^T A = W S Vb^T; U = Q W[:, :r] S[:r] (bf16 [m, ld_u]) and
+ * V = Vb[:, :r] (bf16 [n, ld_v]), so U V^T approximates A. Omega [n, k] (device fp64, row stride
+ * ld_omega) is the caller's random test matrix, k = r + oversampling, r <= k <= min(m, n) and
+ * k <= 256; k = min(m, n) captures the whole range, which makes the factors the exact rank-r
+ * truncation (the pages' fallback for min(m, n) <= 256). orth() is CholeskyQR2, the small SVD
+ * comes from a Jacobi eigen-decomposition of B B^T, all in fp64. Factors are unique only up to
+ * the sign of each pair of columns (and the order of equal singular values): compare U V^T.
+ * workspace: device, aq_randomized_svd_workspace_bytes(m, n, k, r) bytes, 16-byte aligned.
+ * Returns AQ_ERR_NUMERIC if a Cholesky pivot is not positive (A Omega rank deficient). */
+size_t aq_randomized_svd_workspace_bytes(int32_t m, int32_t n, int32_t k, int32_t r);
+aq_status aq_randomized_svd(const double* A, int64_t lda, int32_t m, int32_t n, int32_t r, const double* omega,
+                            int64_t ld_omega, int32_t k, int32_t power_iters, void* U, int64_t ld_u, void* V,
+                            int64_t ld_v, void* workspace, size_t workspace_bytes, void* stream);
 
 const char* aq_status_string(aq_status status);
 /* Thread-local description of the last error returned on this thread ("" if none). */

@@ -20,4 +20,11 @@ from .reconstruction import (  # noqa: F401
     within_error_bound,
     within_tolerance,
 )
-from .decomposition import band_mean, decompose, decompose_stack, randomized_svd, truncated_svd  # noqa: F401
+from .decomposition import (  # noqa: F401
+    band_mean,
+    decompose,
+    decompose_stack,
+    ls_residual_stored,
+    randomized_svd,
+    truncated_svd,
+)

@@ -81,6 +81,18 @@ def randomized_svd(A, r: int, omega, power_iters: int = 0):
     return (Q @ ub[:, :r]) * sv[None, :r], vt[:r].T
 
 
+def ls_residual_stored(weight, W0):
+    """The scale as the bundle stores it and the residual left for U·Vᵀ: s_b = RN_bf16(s) with s
+    the least-squares scale of ``ls_scale``, and resid = weight − diag(s_b)·W0. The bundle holds
+    s in bfloat16 ("The theta bundle": every piece stored like the weights), so the rank-r factors
+    must represent the residual of the stored scale, not of the exact one."""
+    from .reconstruction import round_to_bf16
+    weight = np.asarray(weight, dtype=np.float64)
+    W0 = np.asarray(W0, dtype=np.float64)
+    s_b = round_to_bf16(ls_scale(weight, W0))
+    return s_b, weight - s_b[:, None] * W0
+
+
 def decompose(weight, W0, r: int):
     """One projection weight [out, in] against its band's W0: (s, U, V) with
     weight ≈ diag(s)·W0 + U·Vᵀ."""

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     AQ_PATH_PREFILL,
     AqError,
     Theta,
+    aq_band_mean,
     aq_decode_max_m,
     aq_device_status,
     aq_last_launch_count,
@@ -23,7 +24,9 @@ from .binding import (  # noqa: F401
     aq_linear_multi,
     aq_linear_qkv,
     aq_linear_workspace_bytes,
+    aq_ls_residual,
     aq_precompute,
+    aq_randomized_svd,
     aq_selftest_bounded_wait,
     aq_set_path,
     load,

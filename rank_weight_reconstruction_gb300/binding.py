@@ -22,6 +22,7 @@ AQ_ERR_WORKSPACE = 5
 AQ_ERR_OVERLAP = 6
 AQ_ERR_CUDA = 7
 AQ_ERR_TIMEOUT = 8
+AQ_ERR_NUMERIC = 9
 AQ_MAX_RANK = 256
 
 AQ_PATH_AUTO = 0
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = [
     "aq_device_status", "aq_selftest_bounded_wait", "aq_set_path", "aq_decode_max_m",
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
     "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
+    "aq_band_mean", "aq_ls_residual", "aq_randomized_svd_workspace_bytes", "aq_randomized_svd",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -88,6 +90,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_linear_noalloc.restype = ctypes.c_int
     lib.aq_noalloc_scratch_read.argtypes = [vp, sz, sz, vp]
     lib.aq_noalloc_scratch_read.restype = ctypes.c_int
+    lib.aq_band_mean.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i64, vp, i64, vp]
+    lib.aq_band_mean.restype = ctypes.c_int
+    lib.aq_ls_residual.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp, i64, vp]
+    lib.aq_ls_residual.restype = ctypes.c_int
+    lib.aq_randomized_svd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.aq_randomized_svd_workspace_bytes.restype = sz
+    lib.aq_randomized_svd.argtypes = [vp, i64, i32, i32, i32, vp, i64, i32, i32, vp, i64, vp, i64, vp, sz, vp]
+    lib.aq_randomized_svd.restype = ctypes.c_int
     lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
     lib.aq_precompute.restype = ctypes.c_int
     lib.aq_device_status.argtypes = [vp]
@@ -132,6 +142,13 @@ def _ld(t) -> int:
     import torch
     if t.dtype != torch.bfloat16:
         raise TypeError(f"expected a bfloat16 tensor, got {t.dtype}")
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError("expected a 2-D row-major tensor (unit column stride)")
+    return int(t.stride(0)) if t.size(0) > 1 else int(max(t.stride(0), t.size(1)))
+
+
+def _ld_any(t) -> int:
+    """Leading dimension (elements) of a row-major 2-D tensor of any dtype."""
     if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
         raise ValueError("expected a 2-D row-major tensor (unit column stride)")
     return int(t.stride(0)) if t.size(0) > 1 else int(max(t.stride(0), t.size(1)))
@@ -316,3 +333,56 @@ def aq_last_error() -> str:
 
 def aq_status_string(st: int) -> str:
     return load().aq_status_string(int(st)).decode()
+
+
+# ----------------------------------------------------------------------------------
+# the decomposition (load time): band mean, least-squares scale and residual, randomized SVD
+# ----------------------------------------------------------------------------------
+def aq_band_mean(weights, W0=None, stream=None):
+    """W0 = RN_bf16(mean of the band's bf16 [out, in] weights), on the GPU."""
+    import torch
+    weights = list(weights)
+    out, inp = int(weights[0].size(0)), int(weights[0].size(1))
+    ld = _ld(weights[0])
+    for w in weights:
+        assert w.shape == weights[0].shape and _ld(w) == ld, "band weights must share shape and row stride"
+    if W0 is None:
+        W0 = _padded_empty(out, inp, weights[0].device)
+    ptrs = (ctypes.c_void_p * len(weights))(*[_ptr(w) for w in weights])
+    _check(load().aq_band_mean(ptrs, len(weights), out, inp, ld, _ptr(W0), _ld(W0), _stream(stream)))
+    return W0
+
+
+def aq_ls_residual(weight, W0, s=None, resid=None, stream=None):
+    """s = RN_bf16(per-row least-squares scale of W0 toward weight) and resid = weight − s·W0
+    (float64), on the GPU. Returns (s, resid)."""
+    import torch
+    out, inp = int(weight.size(0)), int(weight.size(1))
+    if s is None:
+        s = torch.empty(out, dtype=torch.bfloat16, device=weight.device)
+    if resid is None:
+        resid = torch.empty(out, inp, dtype=torch.float64, device=weight.device)
+    _check(load().aq_ls_residual(_ptr(weight), _ld(weight), _ptr(W0), _ld(W0), out, inp, _ptr(s), _ptr(resid),
+                                 _ld_any(resid), _stream(stream)))
+    return s, resid
+
+
+def aq_randomized_svd(A, r, omega, power_iters=0, U=None, V=None, stream=None):
+    """Rank-r factors (U [m, r], V [n, r], bf16) of the float64 matrix A by the randomized SVD
+    with the caller's test matrix omega [n, k] (float64), on the GPU."""
+    import torch
+    m, n = int(A.size(0)), int(A.size(1))
+    k = int(omega.size(1))
+    if U is None:
+        U = _padded_empty(m, r, A.device) if r > 0 else torch.empty(m, 0, dtype=torch.bfloat16, device=A.device)
+    if V is None:
+        V = _padded_empty(n, r, A.device) if r > 0 else torch.empty(n, 0, dtype=torch.bfloat16, device=A.device)
+    need = load().aq_randomized_svd_workspace_bytes(m, n, k, r)
+    if need == ctypes.c_size_t(-1).value:
+        raise AqError(AQ_ERR_SHAPE, f"aq_randomized_svd: bad sizes m={m} n={n} k={k} r={r}")
+    ws = torch.empty(max(int(need), 16), dtype=torch.uint8, device=A.device)
+    _check(load().aq_randomized_svd(_ptr(A), _ld_any(A), m, n, r, _ptr(omega), _ld_any(omega), k, power_iters,
+                                    _ptr(U) if r > 0 else None, _ld(U) if r > 0 else max(r, 1),
+                                    _ptr(V) if r > 0 else None, _ld(V) if r > 0 else max(r, 1),
+                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return U, V

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libaq_gb300.so")
-SOURCES = ["aq_kernels.cu", "aq_decode.cu", "aq_decode2.cu", "aq_host.cu", "aq_noalloc.cu"]
+SOURCES = ["aq_kernels.cu", "aq_decode.cu", "aq_decode2.cu", "aq_decompose.cu", "aq_host.cu", "aq_noalloc.cu"]
 HEADERS = ["aq_ptx.cuh", "aq_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -23,7 +23,16 @@ thread_local int32_t t_launches = 0;
 std::atomic<int> g_path{AQ_PATH_AUTO};
 
 constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
-constexpr int kMidMaxM = 512;                         // swapped-operand GEMM up to this M
+// The swapped-operand GEMM (output rows as accumulator lanes) is taken automatically where it was
+// measured faster than the token-lane GEMM (bench.py --sweep, gate-like 6912 x 1152 and down-like
+// 1152 x 6912, r = 0..256): calls of at least this many tokens whose families have few 128-row
+// tiles over a deep K (down-like at 4096 tokens: 54-99 us against 74-116 us). At 64-512 tokens
+// the token-lane GEMM was as fast or faster on both shapes, and at 8192 tokens too (the
+// Gemma-3-1B down projection at r = 64: 122 us against 149 us).
+constexpr int64_t kSwapMinM = 1024;
+constexpr int64_t kSwapMaxM = 4096;
+constexpr int64_t kSwapMaxRowTiles = 16;
+constexpr int kSwapMinK = 4096;
 constexpr int kGemmMinMBigW0 = 16;                    // ... but from this M the GEMM takes calls
 constexpr int64_t kGemmBigW0Bytes = 128ll << 20;      // whose W0 has at least this many bytes
 constexpr uint64_t kTimeoutNs = 1000ull * 1000 * 1000;  // limit of one in-kernel wait: 1 s
@@ -568,8 +577,11 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   for (int j = 0; j < n; ++j) w0_bytes += static_cast<int64_t>(th[j]->out) * K * 2;
   const bool gemm_pays = M >= kGemmMinMBigW0 && w0_bytes >= kGemmBigW0Bytes;
   const bool decode = path_cfg == AQ_PATH_DECODE || (path_cfg == AQ_PATH_AUTO && M <= kDecodeMaxM && !gemm_pays);
-  // Mid-M: the tcgen05 GEMM with output rows as accumulator lanes and the tokens as N
-  const bool midm = !decode && (path_cfg == AQ_PATH_MIDM || (path_cfg == AQ_PATH_AUTO && M <= kMidMaxM));
+  // the tcgen05 GEMM with output rows as accumulator lanes and the tokens as N
+  int64_t row_tiles128 = 0;
+  for (int j = 0; j < n; ++j) row_tiles128 += ceil_div(th[j]->out, kMmaM);
+  const bool swap_pays = M >= kSwapMinM && M <= kSwapMaxM && row_tiles128 <= kSwapMaxRowTiles && K >= kSwapMinK;
+  const bool midm = !decode && (path_cfg == AQ_PATH_MIDM || (path_cfg == AQ_PATH_AUTO && swap_pays));
   if (decode && M > kDecodeMaxM)
     return fail(AQ_ERR_UNSUPPORTED, "%s: the decode kernel handles at most %d tokens (M=%lld)", who, kDecodeMaxM,
                 (long long)M);
@@ -1195,6 +1207,7 @@ const char* aq_status_string(aq_status s) {
     case AQ_ERR_OVERLAP: return "AQ_ERR_OVERLAP";
     case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
     case AQ_ERR_TIMEOUT: return "AQ_ERR_TIMEOUT";
+    case AQ_ERR_NUMERIC: return "AQ_ERR_NUMERIC";
   }
   return "AQ_ERR_UNKNOWN";
 }

@@ -302,3 +302,20 @@ def test_pins_catch_decompose_mutants(mutant):
 @pytest.mark.parametrize("mutant", [stack_first_layer_as_w0, stack_interleaved_bands], ids=lambda m: m.__name__)
 def test_pins_catch_stack_mutants(mutant):
     assert not all(pin(mutant) for pin in STACK_PINS)
+
+
+def test_stored_scale_residual_pins():
+    """The residual of the stored (bf16) scale differs from the exact least-squares residual by
+    exactly (s − RN_bf16(s))·W0 row by row, and the stored scale is the bf16 rounding of the
+    exact one (closed forms); with a W0 row of zeros the scale is 1 and the residual the weight."""
+    rng = np.random.default_rng(11)
+    W0 = oracle.round_to_bf16(rng.normal(0, 0.02, (24, 40)))
+    W0[5] = 0.0
+    w = oracle.round_to_bf16(W0 * rng.uniform(0.9, 1.1, (24, 1)) + rng.normal(0, 0.005, (24, 40)))
+    s_b, resid = oracle.ls_residual_stored(w, W0)
+    s = oracle.ls_scale(w, W0)
+    np.testing.assert_array_equal(s_b, oracle.round_to_bf16(s))
+    np.testing.assert_allclose(resid - oracle.ls_residual(w, W0), (s - s_b)[:, None] * W0, rtol=0, atol=1e-15)
+    assert s_b[5] == 1.0 and np.array_equal(resid[5], w[5])
+    # a planted mistake: the residual of the unrounded scale is not the stored one's
+    assert np.max(np.abs(oracle.ls_residual(w, W0) - resid)) > 0

@@ -348,9 +348,8 @@ def test_31b_projection(M):
     th = synth.make_theta(("31b", "wide", 0), out, inp, 128)
     xb = synth.make_x(("31b-x", M), M, inp)
     y = host_f64(run_linear(th, xb))
-    # a W0 of 231 MB takes the mid-M tcgen05 GEMM from 16 tokens on, the prefill GEMM above 512
-    assert aq.aq_last_path() == (aq.AQ_PATH_DECODE if M < 16 else aq.AQ_PATH_MIDM if M <= 512
-                                 else aq.AQ_PATH_PREFILL)
+    # a W0 of 231 MB takes the tcgen05 GEMM from 16 tokens on
+    assert aq.aq_last_path() == (aq.AQ_PATH_DECODE if M < 16 else aq.AQ_PATH_PREFILL)
     # the whole output, every token tile of the persistent multi-wave schedule included
     st, ok = close_over_rows(y, *th.f64(), x_f64(xb, inp), chunk=512)
     assert ok, st
@@ -369,17 +368,27 @@ def test_31b_projection_decode_forced(M):
 
 def test_path_choice_by_size():
     """Up to 32 tokens the decode kernel, except from 16 tokens on for a W0 of 128 MB or more;
-    the mid-M GEMM up to 512 tokens; the prefill GEMM above."""
+    the prefill GEMM above; the swapped-operand GEMM for 1024 to 4096 tokens on a deep K with
+    at most 16 tiles of 128 rows."""
     sq = synth.CLASS31B_SHAPES["square"]
     th = synth.make_theta(("31b", "square", 0), sq[0], sq[1], 128)
     for M, path in ((1, aq.AQ_PATH_DECODE), (16, aq.AQ_PATH_DECODE), (32, aq.AQ_PATH_DECODE),
-                    (33, aq.AQ_PATH_MIDM), (512, aq.AQ_PATH_MIDM), (513, aq.AQ_PATH_PREFILL)):
+                    (33, aq.AQ_PATH_PREFILL), (1024, aq.AQ_PATH_PREFILL)):
         y = host_f64(run_linear(th, synth.make_x(("path", M), M, sq[1])))
         assert aq.aq_last_path() == path, M
-        if M in (33, 513):
+        if M == 33:
             xb = synth.make_x(("path", M), M, sq[1])
             st, ok = close_over_rows(y, *th.f64(), x_f64(xb, sq[1]))
             assert ok, (M, st)
+    # down-like: 9 tiles of 128 rows over K = 6912
+    dn = synth.make_theta(("path", "down"), 1152, 6912, 16)
+    for M, path in ((512, aq.AQ_PATH_PREFILL), (1024, aq.AQ_PATH_MIDM), (4096, aq.AQ_PATH_MIDM),
+                    (4097, aq.AQ_PATH_PREFILL)):
+        xb = synth.make_x(("path", "down", M), M, 6912)
+        y = host_f64(run_linear(dn, xb))
+        assert aq.aq_last_path() == path, M
+        st, ok = close_over_rows(y, *dn.f64(), x_f64(xb, 6912))
+        assert ok, (M, st)
 
 
 # ----------------------------------------------------------------------------------
