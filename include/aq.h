@@ -189,6 +189,25 @@ aq_status aq_linear_noalloc(const aq_theta* th, const void* x, int64_t M, int64_
  * array returns AQ_ERR_INVALID_ARG. Allocates nothing. */
 aq_status aq_noalloc_scratch_read(void* dst, size_t offset, size_t bytes, void* stream);
 
+/* The fused MLP of one layer ("Execution paths", "The custom op": gate, up, activation and down
+ * of a layer in one dispatch), every projection a reconstruction linear:
+ *   y = down( RN_bf16( act(g) * u ) ),  g = RN_bf16(gate(x)), u = RN_bf16(up(x))
+ * The pages do not name the activation. AQ_ACT_GELU_TANH is the tanh approximation of GELU,
+ * v/2 (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))), the MLP activation of Gemma 3 (whose shapes the
+ * benchmark uses); AQ_ACT_SILU is v / (1 + e^-v). gate and up share [inter, in]; down is
+ * [out, inter]. x [M, in], y [M, out] as for aq_linear. gate and up run as one batched launch.
+ * When the cluster decode kernel takes the down projection with both of its input slices (g and
+ * u) staged (up to 16 tokens, and the slices within its shared memory: up to 4 tokens at
+ * inter = 6912), the activation is formed inside that kernel as it loads its input: two
+ * launches in all. Otherwise one activation pass runs between them.
+ * workspace: aq_mlp_workspace_bytes(gate, up, down, M) bytes, 256-byte aligned, its first
+ * AQ_WORKSPACE_SYNC_BYTES zero before first use (as for aq_linear); it also holds g and u. */
+typedef enum aq_act { AQ_ACT_GELU_TANH = 0, AQ_ACT_SILU = 1 } aq_act;
+size_t aq_mlp_workspace_bytes(const aq_theta* gate, const aq_theta* up, const aq_theta* down, int64_t M);
+aq_status aq_mlp(const aq_theta* gate, const aq_theta* up, const aq_theta* down, aq_act act, const void* x,
+                 int64_t M, int64_t ldx, void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
 /* W_eff[o, i] = RN_bf16( s[o] * W0[o,i] + sum_k U[o,k] * V[i,k] )
  * ("Execution paths", "Precompute-outside: the production path": built once per
  * layer at load). W_eff is [out, in] device, row stride ld_weff >= in, and must not

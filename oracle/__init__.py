@@ -28,3 +28,4 @@ from .decomposition import (  # noqa: F401
     randomized_svd,
     truncated_svd,
 )
+from .mlp import GELU_TANH, SILU, activation, gelu_tanh, mlp, silu  # noqa: F401

@@ -5,6 +5,8 @@ behind a C ABI (include/aq.h); this package holds the in-tree build, the ctypes
 binding, the banded-stack bookkeeping and the seeded input generator.
 """
 from .binding import (  # noqa: F401
+    AQ_ACT_GELU_TANH,
+    AQ_ACT_SILU,
     AQ_ERR_TIMEOUT,
     AQ_MAX_FAMILIES,
     AQ_MAX_RANK,
@@ -24,6 +26,8 @@ from .binding import (  # noqa: F401
     aq_linear_multi,
     aq_linear_qkv,
     aq_linear_workspace_bytes,
+    aq_mlp,
+    aq_mlp_workspace_bytes,
     aq_ls_residual,
     aq_precompute,
     aq_randomized_svd,

@@ -29,6 +29,8 @@ AQ_PATH_AUTO = 0
 AQ_PATH_DECODE = 1
 AQ_PATH_PREFILL = 2
 AQ_PATH_MIDM = 3
+AQ_ACT_GELU_TANH = 0
+AQ_ACT_SILU = 1
 
 EXPORTED_SYMBOLS = [
     "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
@@ -36,6 +38,7 @@ EXPORTED_SYMBOLS = [
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
     "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
     "aq_band_mean", "aq_ls_residual", "aq_randomized_svd_workspace_bytes", "aq_randomized_svd",
+    "aq_mlp_workspace_bytes", "aq_mlp",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -90,6 +93,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_linear_noalloc.restype = ctypes.c_int
     lib.aq_noalloc_scratch_read.argtypes = [vp, sz, sz, vp]
     lib.aq_noalloc_scratch_read.restype = ctypes.c_int
+    lib.aq_mlp_workspace_bytes.argtypes = [th_p, th_p, th_p, i64]
+    lib.aq_mlp_workspace_bytes.restype = sz
+    lib.aq_mlp.argtypes = [th_p, th_p, th_p, ctypes.c_int, vp, i64, i64, vp, i64, vp, sz, vp]
+    lib.aq_mlp.restype = ctypes.c_int
     lib.aq_band_mean.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i64, vp, i64, vp]
     lib.aq_band_mean.restype = ctypes.c_int
     lib.aq_ls_residual.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp, i64, vp]
@@ -386,3 +393,21 @@ def aq_randomized_svd(A, r, omega, power_iters=0, U=None, V=None, stream=None):
                                     _ptr(V) if r > 0 else None, _ld(V) if r > 0 else max(r, 1),
                                     _ptr(ws), ws.numel(), _stream(stream)))
     return U, V
+
+
+def aq_mlp_workspace_bytes(gate: Theta, up: Theta, down: Theta, M: int) -> int:
+    g, u, d = gate.c(), up.c(), down.c()
+    return int(load().aq_mlp_workspace_bytes(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), M))
+
+
+def aq_mlp(gate: Theta, up: Theta, down: Theta, x, act=AQ_ACT_GELU_TANH, y=None, workspace=None, stream=None):
+    """y = down(act(gate(x)) * up(x)) with every projection a reconstruction linear."""
+    M = int(x.size(0))
+    if y is None:
+        y = _padded_empty(M, down.out, x.device)
+    if workspace is None:
+        workspace = new_workspace(max(aq_mlp_workspace_bytes(gate, up, down, M), 256), x.device)
+    g, u, d = gate.c(), up.c(), down.c()
+    _check(load().aq_mlp(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), int(act), _ptr(x), M, _ld(x), _ptr(y),
+                         _ld(y), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return y

@@ -82,6 +82,13 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, float a, floa
                : "memory");
 }
 
+// The activations of the fused MLP, in fp32 with CUDA's tanhf / expf: the tanh approximation of
+// GELU, v/2 (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))), and SiLU, v / (1 + e^-v).
+__device__ __forceinline__ float gated_act(float v, int act) {
+  if (act == kActSilu) return v / (1.0f + expf(-v));
+  return 0.5f * v * (1.0f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));
+}
+
 // Barrier of the 256 mma warps (named barrier 1). Every consumer thread reaches each call site
 // on every path, a failed wait included, so it always completes.
 __device__ __forceinline__ void cons_bar() { named_bar_sync(1, kDecConsumers); }
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   uint64_t* vbar = xbar + 1;
   int* abort_flag = reinterpret_cast<int*>(vbar + 1);
   uint8_t* xs = smem + kHeaderBytes;                 // x slice: 3-D box {64, xkb, M}, swizzled
-  uint8_t* vs = xs + p.x_bytes;                      // V slice: [kslice][vrow] bf16
+  uint8_t* xs2 = xs + p.x_bytes;                     // gated input: the second slice, same layout
+  uint8_t* vs = xs2 + p.x2_bytes;                    // V slice: [kslice][vrow] bf16
   uint8_t* us = vs + p.v_bytes;                      // U rows this CTA finishes: [rf][r16] bf16
   uint8_t* ss = us + p.u_bytes;                      // s of those rows, bf16
   float* tf = reinterpret_cast<float*>(ss + p.s_bytes);  // t over the whole K: [r16][M] fp32
@@ -152,6 +160,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&sg.tm_w);
     tma_prefetch_desc(&p.tm_x);
+    if (p.act >= 0) tma_prefetch_desc(&p.tm_x2);
     if (sg.r > 0) tma_prefetch_desc(&sg.tm_v);
   }
   // The next call may start now: its CTAs fit beside this one and stream their weights.
@@ -191,10 +200,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
         const int kk = kb_lo * 64;
         const int len = min(kb_n * 64, p.K - kk);
         if (len > 0) prefetch_l2_bulk(p.x + static_cast<int64_t>(m) * p.ldx + kk, static_cast<uint32_t>(len) * 2u);
+        if (len > 0 && p.act >= 0)
+          prefetch_l2_bulk(p.x2 + static_cast<int64_t>(m) * p.ldx + kk, static_cast<uint32_t>(len) * 2u);
       }
       pdl_wait_prior_grid();
-      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(p.xkb) * static_cast<uint32_t>(M) * 128u);
+      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(p.xkb) * static_cast<uint32_t>(M) * 128u * (p.act >= 0 ? 2u : 1u));
       tma_load_3d(xs, &p.tm_x, 0, kb_lo, 0, xbar);
+      if (p.act >= 0) tma_load_3d(xs2, &p.tm_x2, 0, kb_lo, 0, xbar);
       int slot = pre == p.stages ? 0 : pre;
       uint32_t phase = pre == p.stages ? 1u : 0u;
       for (int q = pre; q < nstage; ++q) {
@@ -273,6 +285,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
     if (rows_here > 0 && kb_n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(xbar, 0u, ctl)) != 0;
       if (ok && sg.r > 0) ok = __all_sync(0xffffffffu, mbar_wait(vbar, 0u, ctl)) != 0;
+    }
+    if (p.act >= 0) {
+      // gated input: x = act(gate output) * up output, formed once in place over the whole
+      // slice (both boxes share one layout; the zeros past K give act(0) * 0 = 0)
+      if (ok && rows_here > 0 && kb_n > 0) {
+        const int n8 = static_cast<int>(static_cast<uint32_t>(p.xkb) * static_cast<uint32_t>(M) * 128u / 16u);
+        for (int e = ct; e < n8; e += kDecConsumers) {
+          uint4* gp = reinterpret_cast<uint4*>(xs) + e;
+          const uint4 gv = *gp, uv = reinterpret_cast<const uint4*>(xs2)[e];
+          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+          uint32_t hw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float g0 = __uint_as_float(gw[q] << 16), g1 = __uint_as_float(gw[q] & 0xFFFF0000u);
+            const float u0 = __uint_as_float(uw[q] << 16), u1 = __uint_as_float(uw[q] & 0xFFFF0000u);
+            hw[q] = pack_bf16x2(gated_act(g0, p.act) * u0, gated_act(g1, p.act) * u1);
+          }
+          *gp = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+      }
+      cons_bar();
     }
     const uint32_t xbase = smem_u32(xs);
     const uint32_t vbase = smem_u32(vs);
@@ -455,6 +488,36 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       }
     }
   }
+}
+
+// h = RN_bf16(act(g) * u), in place of g: one thread per 8 elements (16-byte rows pieces).
+__global__ void __launch_bounds__(256) aq_gated_act_kernel(uint16_t* g, const uint16_t* u, int64_t ld, int64_t M, int n,
+                                                           int act) {
+  const int per = (n + 7) / 8;
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  pdl_wait_prior_grid();   // g and u are the previous grid's outputs
+  if (e >= M * per) return;
+  const int64_t m = e / per;
+  const int c = static_cast<int>(e - m * per) * 8;
+  uint16_t* gr = g + m * ld + c;
+  const uint16_t* ur = u + m * ld + c;
+  for (int j = 0; j < 8 && c + j < n; ++j)
+    gr[j] = f32_to_bf16_rn(gated_act(bf16_to_f32(gr[j]), act) * bf16_to_f32(ur[j]));
+}
+
+cudaError_t launch_gated_act(uint16_t* g, const uint16_t* u, int64_t ld, int64_t M, int32_t n, int32_t act,
+                             cudaStream_t st, bool pdl) {
+  const int64_t threads = M * ((n + 7) / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, aq_gated_act_kernel, g, u, ld, M, static_cast<int>(n), static_cast<int>(act));
 }
 
 cudaError_t launch_decode2(const Dec2Params& p, int grid, size_t smem, cudaStream_t st, bool pdl) {

@@ -386,7 +386,7 @@ aq_status launch_or_fail(cudaError_t e, const char* what) {
 //     rc <= 256 rows per cluster;
 //   * every region in half of an SM's shared memory, so that consecutive calls' CTAs co-reside.
 bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, int64_t ldx, void* const* ys,
-                  const int64_t* ldys, const DevInfo* dev, cudaStream_t cs, aq_status* st) {
+                  const int64_t* ldys, const DevInfo* dev, cudaStream_t cs, aq_status* st, const void* x2, int act) {
   const int K = th[0]->in;
   if (M < 1 || M > 16 || K % kBK != 0) return false;
   int max_r16 = 0;
@@ -459,6 +459,7 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
     // in distinct banks)
     dp.xkb = (dp.kb_per | 1) <= nkb ? (dp.kb_per | 1) : dp.kb_per;
     dp.x_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.xkb) * M * 128, 1024));
+    dp.x2_bytes = act >= 0 ? dp.x_bytes : 0u;   // a gated input stages both slices
     dp.vrow = max_r16;
     const int64_t kslice = static_cast<int64_t>(dp.kb_per) * kBK;
     const int64_t nvb = ceil_div(kslice, 256);
@@ -469,8 +470,8 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
     dp.s_bytes = static_cast<uint32_t>(round_up((rf_max + 15) / 8 * 16, 1024));
     dp.tf_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(static_cast<int64_t>(max_r16) * M * 4, 1024)) : 0u;
     dp.rx_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(C) * (round_up(rf_max, 4) + max_r16) * M * 4, 1024));
-    const size_t fixed =
-        kHeaderBytes + kSmemSlack + dp.x_bytes + dp.v_bytes + dp.u_bytes + dp.s_bytes + dp.tf_bytes + dp.rx_bytes;
+    const size_t fixed = kHeaderBytes + kSmemSlack + dp.x_bytes + dp.x2_bytes + dp.v_bytes + dp.u_bytes + dp.s_bytes +
+                         dp.tf_bytes + dp.rx_bytes;
     if (fixed >= half) continue;
     const size_t ring = half - fixed;
     dp.kbox = 0;
@@ -497,6 +498,11 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
   const int C = dp.C;
   // tensor maps
   if ((*st = tmap_3d(&dp.tm_x, x, K, M, ldx, dp.xkb, static_cast<int>(M), "x")) != AQ_OK) return true;
+  dp.act = act;
+  if (act >= 0) {
+    if ((*st = tmap_3d(&dp.tm_x2, x2, K, M, ldx, dp.xkb, static_cast<int>(M), "x (gated)")) != AQ_OK) return true;
+    dp.x2 = static_cast<const uint16_t*>(x2);
+  }
   for (int j = 0; j < n; ++j) {
     Dec2Seg& sg = dp.seg[j];
     if ((*st = tmap_3d(&sg.tm_w, th[j]->W0, K, th[j]->out, th[j]->ld_w0, dp.kbox, sg.rc, "W0")) != AQ_OK) return true;
@@ -513,8 +519,11 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
   return true;
 }
 
+// x2 / act: a gated input, act(x) * x2 elementwise (the down projection of the fused MLP), which
+// only the cluster decode kernel takes (the caller falls back to a separate activation pass).
 aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M, int64_t ldx,
-                      void* const* ys, const int64_t* ldys, void* ws, size_t ws_bytes, void* stream) {
+                      void* const* ys, const int64_t* ldys, void* ws, size_t ws_bytes, void* stream,
+                      const void* x2 = nullptr, int act = -1) {
   const char* who = n == 1 ? "aq_linear" : "aq_linear_qkv";
   t_launches = 0;
   for (int j = 0; j < n; ++j) {
@@ -566,6 +575,13 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     }
     for (int i = 0; i < ni; ++i)
       if (overlaps(wsp, ins[i])) return fail(AQ_ERR_OVERLAP, "%s: the workspace overlaps input %s", who, ins[i].name);
+    if (act >= 0) {
+      if (!x2 || !aligned16(x2)) return fail(AQ_ERR_ALIGNMENT, "%s: the gated input must be 16-byte aligned", who);
+      const Span x2s = span(x2, M, K, ldx, "x2");
+      for (int j = 0; j < n; ++j)
+        if (overlaps(span(ys[j], M, th[j]->out, ldys[j], "y"), x2s))
+          return fail(AQ_ERR_OVERLAP, "%s: output %d overlaps the gated input", who, j);
+    }
   }
 
   const int path_cfg = g_path.load();
@@ -595,7 +611,8 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
   if (decode) {
-    if (plan_decode2(th, n, x, M, ldx, ys, ldys, dev, cs, &st)) return st;
+    if (plan_decode2(th, n, x, M, ldx, ys, ldys, dev, cs, &st, x2, act)) return st;
+    if (act >= 0) return fail(AQ_ERR_UNSUPPORTED, "%s: a gated input needs the cluster decode kernel", who);
     // ---- one launch: W0 streamed by row-owning CTAs, t = V^T x by a few extra CTAs ----
     DecodeParams dp = {};
     dp.x = static_cast<const uint16_t*>(x);
@@ -817,6 +834,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     return AQ_OK;
   }
 
+  if (act >= 0) return fail(AQ_ERR_UNSUPPORTED, "%s: a gated input needs the cluster decode kernel", who);
   uint16_t* tbuf = reinterpret_cast<uint16_t*>(wsb + kSyncBytes);
   // ---- plan of the prefill GEMM with the fused reconstruction epilogue ----
   GemmParams gp = {};
@@ -1104,6 +1122,85 @@ aq_status aq_linear_multi(const aq_theta* th, int32_t n, const void* x, int64_t 
   const aq_theta* ptrs[AQ_MAX_FAMILIES] = {};
   for (int j = 0; j < n; ++j) ptrs[j] = &th[j];
   return linear_impl(ptrs, n, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
+}
+
+// ---- fused MLP: y = down( act(gate(x)) * up(x) ) ----
+namespace {
+struct MlpLayout {
+  size_t lin = 0;      // workspace of the linear calls (shared: they run one after another)
+  size_t g_off = 0, u_off = 0;
+  int64_t ldg = 0;
+  size_t total = 0;
+};
+
+size_t mlp_layout(const aq_theta* gate, const aq_theta* up, const aq_theta* down, int64_t M, MlpLayout* out) {
+  const aq_theta pair[2] = {*gate, *up};
+  const size_t a = aq_linear_workspace_bytes(pair, 2, M);
+  const size_t b = aq_linear_workspace_bytes(down, 1, M);
+  if (a == static_cast<size_t>(-1) || b == static_cast<size_t>(-1)) return static_cast<size_t>(-1);
+  MlpLayout l;
+  l.lin = static_cast<size_t>(round_up(static_cast<int64_t>(std::max(a, b)), 256));
+  l.ldg = round_up(gate->out, 8);
+  const size_t gbytes = static_cast<size_t>(round_up(M * l.ldg * 2, 256));
+  l.g_off = l.lin;
+  l.u_off = l.g_off + gbytes;
+  l.total = l.u_off + gbytes;
+  if (out) *out = l;
+  return l.total;
+}
+}  // namespace
+
+size_t aq_mlp_workspace_bytes(const aq_theta* gate, const aq_theta* up, const aq_theta* down, int64_t M) {
+  if (!gate || !up || !down || M < 0) return static_cast<size_t>(-1);
+  return mlp_layout(gate, up, down, M, nullptr);
+}
+
+aq_status aq_mlp(const aq_theta* gate, const aq_theta* up, const aq_theta* down, aq_act act, const void* x,
+                 int64_t M, int64_t ldx, void* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  t_launches = 0;
+  if (!gate || !up || !down) return fail(AQ_ERR_INVALID_ARG, "aq_mlp: NULL bundle");
+  if (act != AQ_ACT_GELU_TANH && act != AQ_ACT_SILU) return fail(AQ_ERR_INVALID_ARG, "aq_mlp: unknown activation %d", (int)act);
+  if (gate->out != up->out || gate->in != up->in || down->in != gate->out)
+    return fail(AQ_ERR_SHAPE, "aq_mlp: gate and up must share [out, in] and down.in must equal their out "
+                "(gate %d x %d, up %d x %d, down %d x %d)", gate->out, gate->in, up->out, up->in, down->out, down->in);
+  if (M < 0) return fail(AQ_ERR_SHAPE, "aq_mlp: M=%lld is negative", (long long)M);
+  if (M == 0) return AQ_OK;
+  MlpLayout l;
+  if (mlp_layout(gate, up, down, M, &l) == static_cast<size_t>(-1)) return fail(AQ_ERR_INVALID_ARG, "aq_mlp: bad bundle");
+  if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(AQ_ERR_WORKSPACE, "aq_mlp: workspace of %zu bytes (256-byte aligned) required, got %zu", l.total,
+                workspace_bytes);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  uint16_t* g = reinterpret_cast<uint16_t*>(wsb + l.g_off);
+  uint16_t* u = reinterpret_cast<uint16_t*>(wsb + l.u_off);
+  // gate and up over one x in one launch
+  const aq_theta* gu[2] = {gate, up};
+  void* gys[2] = {g, u};
+  const int64_t glds[2] = {l.ldg, l.ldg};
+  aq_status st = linear_impl(gu, 2, x, M, ldx, gys, glds, workspace, l.lin, stream);
+  if (st != AQ_OK) return st;
+  int launches = t_launches;
+  // down over act(g) * u: fused into the cluster decode kernel's input when it takes the call,
+  // else one activation pass in place of g first
+  const aq_theta* dn[1] = {down};
+  void* dys[1] = {y};
+  const int64_t dlds[1] = {ldy};
+  const int32_t saved_path = g_path.load();
+  if (M <= 16 && saved_path != AQ_PATH_PREFILL && saved_path != AQ_PATH_MIDM) {
+    st = linear_impl(dn, 1, g, M, l.ldg, dys, dlds, workspace, l.lin, stream, u, static_cast<int>(act));
+    if (st == AQ_OK) {
+      t_launches += launches;
+      return AQ_OK;
+    }
+    if (st != AQ_ERR_UNSUPPORTED) return st;
+  }
+  cudaError_t e = launch_gated_act(g, u, l.ldg, M, gate->out, static_cast<int32_t>(act), static_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "aq_mlp: launch activation");
+  ++launches;
+  st = linear_impl(dn, 1, g, M, l.ldg, dys, dlds, workspace, l.lin, stream);
+  if (st == AQ_OK) t_launches += launches;
+  return st;
 }
 
 aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream) {

@@ -220,6 +220,7 @@ struct Dec2Seg {
 
 struct Dec2Params {
   CUtensorMap tm_x;    // x as {64, K/64, M}, box {64, xkb, M}, 128-byte swizzle
+  CUtensorMap tm_x2;   // gated input (act >= 0): the up projection's output, same view as tm_x
   Dec2Seg seg[kMaxSeg];
   const uint16_t* x;   // for L2 prefetch hints
   int64_t ldx;
@@ -237,10 +238,17 @@ struct Dec2Params {
   uint32_t stage_bytes;  // kbox * max rc * 128, 1 KB aligned
   uint32_t x_bytes, v_bytes, u_bytes, s_bytes, tf_bytes;  // shared-memory regions, 1 KB aligned
   uint32_t rx_bytes;     // receive area of the cluster exchange: [C][M][round_up(rf, 4)] + [C][r16][M] fp32
+  uint32_t x2_bytes;     // the second x slice of a gated input (0 without one)
+  int32_t act;           // gated input: -1 none; else the input is act(x) * x2 (kAct* below)
+  const uint16_t* x2;    // for L2 prefetch hints
   int32_t* status;
   uint64_t timeout_ns;
 };
 static_assert(sizeof(Dec2Params) <= 4096, "kernel parameters are limited to 4 KB");
+
+// Activations of the fused MLP (aq_act in aq.h).
+constexpr int kActGeluTanh = 0;
+constexpr int kActSilu = 1;
 
 // V [in, r] -> Vt [r, in] (bf16) for the prefill t GEMM.
 struct TransposeSeg {
@@ -298,6 +306,9 @@ cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);
 cudaError_t launch_decode2(const Dec2Params& p, int grid, size_t smem, cudaStream_t st, bool pdl);
+// h[m, i] = RN_bf16(act(g[m, i]) * u[m, i]) in place of g (rows of `n` elements, stride ld).
+cudaError_t launch_gated_act(uint16_t* g, const uint16_t* u, int64_t ld, int64_t M, int32_t n, int32_t act,
+                             cudaStream_t st, bool pdl);
 cudaError_t configure_decode2(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
