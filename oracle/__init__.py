@@ -29,3 +29,4 @@ from .decomposition import (  # noqa: F401
     truncated_svd,
 )
 from .mlp import GELU_TANH, SILU, activation, gelu_tanh, mlp, silu  # noqa: F401
+from . import nvfp4  # noqa: F401
