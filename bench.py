@@ -67,6 +67,11 @@ def precompute_bytes(out, inp, r):
     return 2 * (2 * out * inp + r * (out + inp) + out)
 
 
+def nvfp4_bytes(out, inp, r):
+    """Read W0, U, V, s once; write the E2M1 codes, the E4M3 scales and the global scale."""
+    return 2 * out * inp + 2 * r * (out + inp) + 2 * out + out * inp // 2 + out * inp // 16 + 4
+
+
 def gate_up_bytes(r, M):
     """gate and up over one x in one batched call: x counted once, like Q/K/V."""
     (og, ig), (ou, iu) = FAMS["gate_proj"], FAMS["up_proj"]
@@ -698,7 +703,47 @@ def extras(result, args, dist, stack, device, pk):
     gbq = precompute_bytes(*shapes["wide"], r) / (tq * 1e-3) / 1e9
     result["precompute"]["wide_single"] = {"GB_s": round(gbq, 1), "us": round(tq * 1e3, 1),
                                            "frac_hbm": round(gbq / pk["hbm_gbs"], 4)}
-    del gpc, gq, thetas, outs, w0d
+    del gpc, gq, outs
+    torch.cuda.empty_cache()
+
+    # ---- the same stack quantized to NVFP4 in the precompute epilogue (128x4 scales) ----
+    qs = {k: [(torch.empty(o, i // 2, dtype=torch.uint8, device=device),
+               torch.empty(aq.binding.nvfp4_scale_bytes(o, i, aq.AQ_SF_128X4), dtype=torch.uint8, device=device))
+              for _ in range(2)] for k, (o, i) in shapes.items()}
+    gsc = torch.ones(len(thetas), dtype=torch.float32, device=device)
+    wsn = torch.empty(aq.binding.load().aq_precompute_nvfp4_workspace_bytes(), dtype=torch.uint8, device=device)
+
+    def nvfp4_call(j, k, T, given):
+        qq, ss = qs[k][(j // 2) % 2]
+        aq.aq_precompute_nvfp4(T, sf_layout=aq.AQ_SF_128X4, global_scale=gsc[j:j + 1], scale_given=given,
+                               q=qq, sf=ss, workspace=wsn)
+
+    Bn = sum(nvfp4_bytes(*shapes[k], r) for k, _ in thetas)
+    nv = {"workload": "NVFP4 W_eff (E2M1 codes, E4M3 scales in the 128x4 layout) for the same 60 layers",
+          "algorithmic_bytes": Bn,
+          "bytes_rule": "W0, U, V, s read once; codes (1/2 B per weight), scales (1/16 B) and g written"}
+    for given in (False, True):
+        for j, (k, T) in enumerate(thetas[:2]):
+            nvfp4_call(j, k, T, given)
+        torch.cuda.synchronize()
+        gn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gn):
+            for j, (k, T) in enumerate(thetas):
+                nvfp4_call(j, k, T, given)
+        tn = time_graph(gn, max(2, args.steps // 2))
+        gbn = Bn / (tn * 1e-3) / 1e9
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1):
+            nvfp4_call(0, thetas[0][0], thetas[0][1], given)
+        t1 = time_graph(g1, 10)
+        gb1 = nvfp4_bytes(*shapes["wide"], r) / (t1 * 1e-3) / 1e9
+        nv["given_scale" if given else "scale_from_amax"] = {
+            "GB_s": round(gbn, 1), "frac_hbm": round(gbn / pk["hbm_gbs"], 4), "ms": round(tn, 3),
+            "launches_per_layer_matrix": 1 if given else 2,
+            "wide_single": {"GB_s": round(gb1, 1), "us": round(t1 * 1e3, 1), "frac_hbm": round(gb1 / pk["hbm_gbs"], 4)}}
+        del gn, g1
+    result["precompute_nvfp4"] = nv
+    del thetas, w0d, qs
     torch.cuda.empty_cache()
 
 
@@ -802,9 +847,20 @@ def run_case(args, dist: Dist):
         W = torch.empty(out, (inp + 7) // 8 * 8, dtype=torch.bfloat16, device=device)[:, :inp]
         run = lambda: aq.aq_precompute(theta, W_eff=W)
         work = {"bytes": precompute_bytes(out, inp, r)}
+    elif kind == "nvfp4":
+        # nvfp4:out,in,r[,given]: NVFP4 precompute, 128x4 scales; given=1 takes g as input
+        given = len(vals) > 3 and vals[3] != 0
+        qq = torch.empty(out, inp // 2, dtype=torch.uint8, device=device)
+        ss = torch.empty(aq.binding.nvfp4_scale_bytes(out, inp, aq.AQ_SF_128X4), dtype=torch.uint8, device=device)
+        gg = torch.full((1,), 1e-4, dtype=torch.float32, device=device)
+        wsn = torch.empty(aq.binding.load().aq_precompute_nvfp4_workspace_bytes(), dtype=torch.uint8, device=device)
+        run = lambda: aq.aq_precompute_nvfp4(theta, sf_layout=aq.AQ_SF_128X4, global_scale=gg, scale_given=given,
+                                             q=qq, sf=ss, workspace=wsn)
+        work = {"bytes": nvfp4_bytes(out, inp, r)}
+        kind = "precompute"
     else:
         raise SystemExit(f"unknown --case kind {kind!r} (linear:out,in,r,M, gateup:out,in,r,M, "
-                         "qkv:out_q,out_kv,in,r,M or precompute:out,in,r)")
+                         "qkv:out_q,out_kv,in,r,M, precompute:out,in,r or nvfp4:out,in,r[,given])")
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()

@@ -215,6 +215,42 @@ aq_status aq_mlp(const aq_theta* gate, const aq_theta* up, const aq_theta* down,
  * the tensor cores; s * W0 is exact in fp32; one final rounding. */
 aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream);
 
+/* W_eff quantized to NVFP4 as it is formed, never written in bf16 ("Execution paths",
+ * "Precompute-outside: the production path": each W_eff quantized to 4 bits at load;
+ * "Internals and extension", "Nvfp4Spec": two E2M1 values per byte, so the [out, in]
+ * weight is held as [out, in/2] bytes, one FP8-E4M3 scale per 16 values along in, one
+ * fp32 global scale; scales in a linear [out, in/16] layout or a "128x4" layout padded to
+ * [ceil(out,128), ceil(in/16,4)] for Blackwell GEMMs).
+ *
+ * The value quantized is the fp32 W_eff of aq_precompute before its bf16 rounding. The
+ * rule, each step one fp32 operation rounded to nearest even (the pages state none):
+ *   g = global scale (decode multiplier: weight = e2m1 * e4m3 * g)
+ *   per 16 values x along in: a = max|x|; scale = E4M3(a / (6 g)), ties to even,
+ *   clamped to 448; d = scale * g; code = E2M1(x * (1/d)), ties to the even code, clamped
+ *   to +-6, sign of x kept (a d of 0 gives +0 codes).
+ * Codes: byte j of a row holds columns 2j (low nibble) and 2j+1 (high nibble).
+ *
+ * q: [out, in/2] bytes, device, row stride ldq >= in/2 bytes, ldq and q 8-byte aligned.
+ * in must be a multiple of 16 (AQ_ERR_SHAPE otherwise).
+ * sf: device, 16-byte aligned; sf_layout AQ_SF_LINEAR: out * (in/16) bytes, row o at
+ *   o * (in/16); AQ_SF_128X4: ceil(out,128) * ceil(in/16,4) bytes in tiles of 128 rows by 4
+ *   scale columns (512 bytes each, tiles of one row band consecutive along in, bands
+ *   consecutive), the scale of row r, column k of a tile at 16 (r mod 32) + 4 (r div 32) + k;
+ *   padding entries are written as 0. (The pages give the padded shape, not this order.)
+ * global_scale: one fp32 in device memory. scale_mode AQ_NVFP4_SCALE_GIVEN: read as g (one
+ *   launch). AQ_NVFP4_SCALE_FROM_AMAX: written with g = RN(max|W_eff| / 2688) (2688 = 6 * 448:
+ *   the largest block lands on the largest E4M3 scale); a first launch finds max|W_eff|
+ *   (each CTA's maximum into `workspace`, aq_precompute_nvfp4_workspace_bytes() bytes,
+ *   4-byte aligned, no initial contents needed), a second quantizes, walking the tiles in
+ *   reverse so that the W0 tail still in L2 is read first. workspace may be NULL when given.
+ * None of q, sf, global_scale, workspace may overlap each other or W0, s, U, V. */
+typedef enum aq_sf_layout { AQ_SF_LINEAR = 0, AQ_SF_128X4 = 1 } aq_sf_layout;
+typedef enum aq_nvfp4_scale { AQ_NVFP4_SCALE_FROM_AMAX = 0, AQ_NVFP4_SCALE_GIVEN = 1 } aq_nvfp4_scale;
+size_t aq_precompute_nvfp4_workspace_bytes(void);
+aq_status aq_precompute_nvfp4(const aq_theta* th, void* q, int64_t ldq, void* sf, int sf_layout,
+                              float* global_scale, int scale_mode, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Synchronises `stream`, then returns the device status word of the current device
  * (AQ_OK, or AQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last clear)
  * and clears it. A kernel whose wait expires stops its work (its outputs are then

@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     AQ_PATH_DECODE,
     AQ_PATH_MIDM,
     AQ_PATH_PREFILL,
+    AQ_SF_128X4,
+    AQ_SF_LINEAR,
     AqError,
     Theta,
     aq_band_mean,
@@ -30,10 +32,12 @@ from .binding import (  # noqa: F401
     aq_mlp_workspace_bytes,
     aq_ls_residual,
     aq_precompute,
+    aq_precompute_nvfp4,
     aq_randomized_svd,
     aq_selftest_bounded_wait,
     aq_set_path,
     load,
     new_workspace,
+    nvfp4_scale_bytes,
 )
 from .stack import StackMismatchError, ThetaStack, band_of  # noqa: F401

@@ -31,6 +31,10 @@ AQ_PATH_PREFILL = 2
 AQ_PATH_MIDM = 3
 AQ_ACT_GELU_TANH = 0
 AQ_ACT_SILU = 1
+AQ_SF_LINEAR = 0
+AQ_SF_128X4 = 1
+AQ_NVFP4_SCALE_FROM_AMAX = 0
+AQ_NVFP4_SCALE_GIVEN = 1
 
 EXPORTED_SYMBOLS = [
     "aq_linear_workspace_bytes", "aq_linear", "aq_linear_qkv", "aq_precompute",
@@ -38,7 +42,7 @@ EXPORTED_SYMBOLS = [
     "aq_last_path", "aq_last_launch_count", "aq_status_string", "aq_last_error",
     "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
     "aq_band_mean", "aq_ls_residual", "aq_randomized_svd_workspace_bytes", "aq_randomized_svd",
-    "aq_mlp_workspace_bytes", "aq_mlp",
+    "aq_mlp_workspace_bytes", "aq_mlp", "aq_precompute_nvfp4_workspace_bytes", "aq_precompute_nvfp4",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -107,6 +111,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_randomized_svd.restype = ctypes.c_int
     lib.aq_precompute.argtypes = [th_p, vp, i64, vp]
     lib.aq_precompute.restype = ctypes.c_int
+    lib.aq_precompute_nvfp4_workspace_bytes.argtypes = []
+    lib.aq_precompute_nvfp4_workspace_bytes.restype = sz
+    lib.aq_precompute_nvfp4.argtypes = [th_p, vp, i64, vp, ctypes.c_int, vp, ctypes.c_int, vp, sz, vp]
+    lib.aq_precompute_nvfp4.restype = ctypes.c_int
     lib.aq_device_status.argtypes = [vp]
     lib.aq_device_status.restype = ctypes.c_int
     lib.aq_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
@@ -303,6 +311,45 @@ def aq_precompute(theta: Theta, W_eff=None, stream=None):
     th = theta.c()
     _check(load().aq_precompute(ctypes.byref(th), _ptr(W_eff), _ld(W_eff), _stream(stream)))
     return W_eff
+
+
+def nvfp4_scale_bytes(out: int, inp: int, layout: int) -> int:
+    """Bytes of the block-scale array of an [out, inp] weight in the given layout."""
+    if layout == AQ_SF_LINEAR:
+        return out * (inp // 16)
+    return -(-out // 128) * 128 * (-(-(inp // 16) // 4) * 4)
+
+
+def aq_precompute_nvfp4(theta: Theta, sf_layout: int = AQ_SF_LINEAR, global_scale=None, scale_given=None,
+                        q=None, sf=None, workspace=None, stream=None):
+    """W_eff quantized to NVFP4 without forming it in bf16: returns (q, sf, global_scale) with
+    q a uint8 [out, in/2] tensor of E2M1 code pairs, sf the uint8 E4M3 block scales (a 2-D
+    [out, in/16] tensor for AQ_SF_LINEAR, a flat tensor for AQ_SF_128X4) and global_scale a
+    one-element float32 device tensor. With ``scale_given`` (default: whether
+    ``global_scale`` is passed) the scale in ``global_scale`` is used; otherwise it is
+    computed from max|W_eff| and written to ``global_scale`` (allocated if None)."""
+    import torch
+    dev = theta.W0.device
+    if q is None:
+        q = torch.empty(theta.out, theta.inp // 2, dtype=torch.uint8, device=dev)
+    if sf is None:
+        n = nvfp4_scale_bytes(theta.out, theta.inp, sf_layout)
+        sf = torch.empty(n, dtype=torch.uint8, device=dev)
+        if sf_layout == AQ_SF_LINEAR:
+            sf = sf.view(theta.out, theta.inp // 16)
+    given = (global_scale is not None) if scale_given is None else bool(scale_given)
+    if global_scale is None:
+        if given:
+            raise ValueError("scale_given needs a global_scale tensor")
+        global_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None and not given:
+        workspace = torch.empty(int(load().aq_precompute_nvfp4_workspace_bytes()), dtype=torch.uint8, device=dev)
+    th = theta.c()
+    _check(load().aq_precompute_nvfp4(
+        ctypes.byref(th), _ptr(q), _ld_any(q), _ptr(sf), int(sf_layout), _ptr(global_scale),
+        AQ_NVFP4_SCALE_GIVEN if given else AQ_NVFP4_SCALE_FROM_AMAX, _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream)))
+    return q, sf, global_scale
 
 
 def aq_device_status(stream=None) -> int:

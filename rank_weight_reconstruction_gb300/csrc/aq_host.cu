@@ -1203,6 +1203,55 @@ aq_status aq_mlp(const aq_theta* gate, const aq_theta* up, const aq_theta* down,
   return st;
 }
 
+constexpr int kPrePfAhead = 4;   // precompute: W0 tiles of a CTA prefetched into L2 ahead
+
+// Tiles, tensor maps and shared-memory budget of the precompute kernel (any output kind).
+static aq_status plan_precompute(const aq_theta* th, DevInfo* dev, PrecomputeParams* pp, size_t* smem,
+                                 int* grid, int out_kind, const char* who) {
+  pp->out = th->out;
+  pp->in = th->in;
+  pp->r = th->r;
+  pp->bn = 128;
+  pp->s = static_cast<const uint16_t*>(th->s);
+  pp->n_row_tiles = static_cast<int32_t>(ceil_div(th->out, kMmaM));
+  pp->n_col_tiles = static_cast<int32_t>(ceil_div(th->in, pp->bn));
+  pp->total_tiles = pp->n_row_tiles * pp->n_col_tiles;
+  aq_status st;
+  if ((st = tmap_2d(&pp->tm_w0, th->W0, th->in, th->out, th->ld_w0, kMmaM, "W0")) != AQ_OK) return st;
+  if (th->r > 0) {
+    if ((st = tmap_2d(&pp->tm_u, th->U, th->r, th->out, th->ld_u, kMmaM, "U")) != AQ_OK) return st;
+    if ((st = tmap_2d(&pp->tm_v, th->V, th->r, th->in, th->ld_v, pp->bn, "V")) != AQ_OK) return st;
+  }
+  pp->stage_bytes = static_cast<uint32_t>(round_up(kStageA + pp->bn * 128, 1024));
+  // Shared memory: W0 / W_eff tile buffers (four kept before the ring grows: measured best
+  // for r = 128, where four buffers and a three-stage ring beat three and four), the U / V
+  // ring (two tiles' chunks where they fit, so that the next tile's chunks arrive from L2
+  // while this tile's MMAs run) and the NVFP4 table of 1/d.
+  const size_t cbuf_bytes = static_cast<size_t>(pp->bn) * 256u;
+  const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
+  const size_t staging = out_kind == kPreNvfp4 ? kNvfp4TableBytes : 0u;
+  const size_t base = kSmemSlack + kHeaderBytes + staging;
+  const int nkb = static_cast<int>(ceil_div(th->r, kBK));
+  if (th->r > 0) {
+    const size_t room = cap > base + 4 * cbuf_bytes ? cap - base - 4 * cbuf_bytes : 0;
+    pp->stages = static_cast<int32_t>(std::max<size_t>(2, std::min<size_t>(2 * nkb, room / pp->stage_bytes)));
+  } else {
+    pp->stages = 0;
+  }
+  const size_t fixed = base + static_cast<size_t>(pp->stages) * pp->stage_bytes;
+  pp->cbufs = static_cast<int32_t>(std::min<size_t>(8, (cap - fixed) / cbuf_bytes));
+  // W0 tiles prefetched into L2 ahead of the tile buffers (beyond what shared memory holds)
+  pp->pf_ahead = out_kind == kPreBf16 ? kPrePfAhead : 0;   // measured: helps bf16 only
+  pp->tmem_cols = th->r > 0 ? tmem_cols_for(2 * pp->bn) : 32;
+  pp->status = dev->status;
+  pp->timeout_ns = kTimeoutNs;
+  *smem = fixed + static_cast<size_t>(pp->cbufs) * cbuf_bytes;
+  if (pp->cbufs < 2) return fail(AQ_ERR_UNSUPPORTED, "%s: shared memory holds %d tile buffers", who, pp->cbufs);
+  if (*smem > dev->smem_optin) return fail(AQ_ERR_UNSUPPORTED, "%s: needs %zu bytes of shared memory", who, *smem);
+  *grid = std::min(pp->total_tiles, dev->sms);
+  return AQ_OK;
+}
+
 aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* stream) {
   t_launches = 0;
   aq_status st = check_theta(th, "aq_precompute");
@@ -1221,36 +1270,86 @@ aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* 
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != AQ_OK) return st;
   PrecomputeParams pp = {};
-  pp.out = th->out;
-  pp.in = th->in;
-  pp.r = th->r;
-  pp.bn = 128;
-  pp.s = static_cast<const uint16_t*>(th->s);
-  pp.n_row_tiles = static_cast<int32_t>(ceil_div(th->out, kMmaM));
-  pp.n_col_tiles = static_cast<int32_t>(ceil_div(th->in, pp.bn));
-  pp.total_tiles = pp.n_row_tiles * pp.n_col_tiles;
-  if ((st = tmap_2d(&pp.tm_w0, th->W0, th->in, th->out, th->ld_w0, kMmaM, "W0")) != AQ_OK) return st;
+  size_t smem = 0;
+  int grid = 0;
+  if ((st = plan_precompute(th, dev, &pp, &smem, &grid, kPreBf16, "aq_precompute")) != AQ_OK) return st;
   if ((st = tmap_2d(&pp.tm_we, W_eff, th->in, th->out, ld_weff, kMmaM, "W_eff")) != AQ_OK) return st;
-  if (th->r > 0) {
-    if ((st = tmap_2d(&pp.tm_u, th->U, th->r, th->out, th->ld_u, kMmaM, "U")) != AQ_OK) return st;
-    if ((st = tmap_2d(&pp.tm_v, th->V, th->r, th->in, th->ld_v, pp.bn, "V")) != AQ_OK) return st;
-  }
-  pp.stage_bytes = static_cast<uint32_t>(round_up(kStageA + pp.bn * 128, 1024));
-  pp.stages = th->r > 0 ? 2 : 0;   // U / V chunks come from L2; a short ring suffices
-  // the rest of shared memory holds W0 / W_eff tiles: the W0 reads in flight are what keep
-  // this stream near the HBM rate
-  const size_t cbuf_bytes = static_cast<size_t>(pp.bn) * 256u;
-  const size_t cap = std::min<size_t>(dev->smem_optin, 227 * 1024);
-  const size_t fixed = kSmemSlack + kHeaderBytes + static_cast<size_t>(pp.stages) * pp.stage_bytes;
-  pp.cbufs = static_cast<int32_t>(std::min<size_t>(8, (cap - fixed) / cbuf_bytes));
-  pp.tmem_cols = th->r > 0 ? tmem_cols_for(2 * pp.bn) : 32;
-  pp.status = dev->status;
-  pp.timeout_ns = kTimeoutNs;
-  const size_t smem = fixed + static_cast<size_t>(pp.cbufs) * cbuf_bytes;
-  if (smem > dev->smem_optin) return fail(AQ_ERR_UNSUPPORTED, "aq_precompute: needs %zu bytes of shared memory", smem);
-  const int grid = std::min(pp.total_tiles, dev->sms);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return launch_or_fail(launch_precompute(pp, grid, smem, cs, true), "launch precompute");
+}
+
+size_t aq_precompute_nvfp4_workspace_bytes(void) { return kNvfp4Partials * sizeof(float); }
+
+aq_status aq_precompute_nvfp4(const aq_theta* th, void* q, int64_t ldq, void* sf, int sf_layout,
+                              float* global_scale, int scale_mode, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  t_launches = 0;
+  const char* who = "aq_precompute_nvfp4";
+  aq_status st = check_theta(th, who);
+  if (st != AQ_OK) return st;
+  if (!q || !sf || !global_scale) return fail(AQ_ERR_INVALID_ARG, "%s: q, sf and global_scale must be non-NULL", who);
+  if (sf_layout != AQ_SF_LINEAR && sf_layout != AQ_SF_128X4)
+    return fail(AQ_ERR_INVALID_ARG, "%s: sf_layout=%d is not AQ_SF_LINEAR or AQ_SF_128X4", who, sf_layout);
+  if (scale_mode != AQ_NVFP4_SCALE_FROM_AMAX && scale_mode != AQ_NVFP4_SCALE_GIVEN)
+    return fail(AQ_ERR_INVALID_ARG, "%s: scale_mode=%d is not a aq_nvfp4_scale value", who, scale_mode);
+  if (th->in % 16 != 0) return fail(AQ_ERR_SHAPE, "%s: in=%d is not a multiple of 16", who, th->in);
+  if (ldq < th->in / 2) return fail(AQ_ERR_SHAPE, "%s: ldq=%lld < in/2=%d", who, (long long)ldq, th->in / 2);
+  if (ldq % 8 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u) != 0 || !aligned16(sf) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u) != 0)
+    return fail(AQ_ERR_ALIGNMENT, "%s: q and ldq must be 8-byte aligned, sf 16-byte, global_scale 4-byte", who);
+  const bool from_amax = scale_mode == AQ_NVFP4_SCALE_FROM_AMAX;
+  if (from_amax) {
+    if (!workspace) return fail(AQ_ERR_INVALID_ARG, "%s: workspace is NULL", who);
+    if (workspace_bytes < aq_precompute_nvfp4_workspace_bytes())
+      return fail(AQ_ERR_WORKSPACE, "%s: workspace of %zu bytes < %zu", who, workspace_bytes,
+                  aq_precompute_nvfp4_workspace_bytes());
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+      return fail(AQ_ERR_ALIGNMENT, "%s: workspace must be 4-byte aligned", who);
+  }
+  const int64_t sf_bytes = sf_layout == AQ_SF_LINEAR
+                               ? static_cast<int64_t>(th->out) * (th->in / 16)
+                               : ceil_div(th->out, 128) * 128 * (ceil_div(th->in / 16, 4) * 4);
+  {
+    // byte ranges as spans of 2-byte elements (ldq is even)
+    Span outs[4] = {span(q, th->out, (th->in / 2 + 1) / 2, ldq / 2, "q"),
+                    span(sf, 1, (sf_bytes + 1) / 2, (sf_bytes + 1) / 2, "sf"),
+                    span(global_scale, 1, 2, 2, "global_scale"),
+                    span(from_amax ? workspace : nullptr, 1, kNvfp4Partials * 2, kNvfp4Partials * 2,
+                         "workspace")};
+    Span ins[4];
+    theta_spans(th, ins);
+    for (int a = 0; a < 4; ++a) {
+      for (int i = 0; i < 4; ++i)
+        if (overlaps(outs[a], ins[i])) return fail(AQ_ERR_OVERLAP, "%s: %s overlaps %s", who, outs[a].name, ins[i].name);
+      for (int b = a + 1; b < 4; ++b)
+        if (overlaps(outs[a], outs[b])) return fail(AQ_ERR_OVERLAP, "%s: %s overlaps %s", who, outs[a].name, outs[b].name);
+    }
+  }
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != AQ_OK) return st;
+  PrecomputeParams pp = {};
+  size_t smem = 0;
+  int grid = 0;
+  if ((st = plan_precompute(th, dev, &pp, &smem, &grid, kPreNvfp4, who)) != AQ_OK) return st;
+  if (grid > kNvfp4Partials) return fail(AQ_ERR_UNSUPPORTED, "%s: %d CTAs exceed the partial maxima", who, grid);
+  pp.q = static_cast<uint8_t*>(q);
+  pp.ldq = ldq;
+  pp.sf = static_cast<uint8_t*>(sf);
+  pp.sf_layout = sf_layout;
+  pp.sf_cols = th->in / 16;
+  pp.sf_ktiles = static_cast<int32_t>(ceil_div(th->in / 16, 4));
+  pp.gscale = global_scale;
+  pp.partials = static_cast<float*>(workspace);
+  pp.n_partials = grid;
+  pp.scale_given = from_amax ? 0 : 1;
+  pp.reverse = from_amax ? 1 : 0;
+  pp.q16 = (ldq % 16 == 0 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) ? 1 : 0;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (from_amax) {
+    if ((st = launch_or_fail(launch_precompute(pp, grid, smem, cs, true, kPreAmax), "launch W_eff amax")) != AQ_OK)
+      return st;
+  }
+  return launch_or_fail(launch_precompute(pp, grid, smem, cs, true, kPreNvfp4), "launch NVFP4 precompute");
 }
 
 aq_status aq_device_status(void* stream) {

@@ -286,7 +286,29 @@ struct PrecomputeParams {
   uint32_t tmem_cols;
   int32_t* status;
   uint64_t timeout_ns;
+  // NVFP4 output (kPreNvfp4) and the W_eff amax pass before it (kPreAmax)
+  uint8_t* q;          // codes [out, in/2] bytes, row stride ldq
+  int64_t ldq;
+  uint8_t* sf;         // E4M3 block scales, layout sf_layout
+  int32_t sf_layout;   // AQ_SF_LINEAR or AQ_SF_128X4
+  int32_t sf_cols;     // in / 16
+  int32_t sf_ktiles;   // ceil(in / 64): 4-scale column tiles of the 128x4 layout
+  int32_t scale_given; // 1: g read from *gscale; 0: g from the amax pass's partial maxima
+  int32_t n_partials;  // partial maxima written by the amax pass (its grid)
+  int32_t reverse;     // walk the tiles last to first (re-reads the amax pass's L2 tail first)
+  float* gscale;       // the fp32 global decode scale g
+  float* partials;     // one max|W_eff| per CTA of the amax pass
+  int32_t q16;         // q and ldq 16-byte aligned: codes leave in 16-byte stores
+  int32_t pf_ahead;    // W0 tiles of this CTA prefetched into L2 ahead of the TMA loads (0: off)
 };
+
+// Output of aq_precompute_kernel: bf16 W_eff, max|W_eff| partials, or NVFP4 codes + scales.
+constexpr int kPreBf16 = 0;
+constexpr int kPreAmax = 1;
+constexpr int kPreNvfp4 = 2;
+constexpr int kNvfp4Partials = 1024;   // partial maxima a workspace holds (>= any grid)
+// NVFP4: 128 floats of 1/d, one per scale byte, after the operand ring
+constexpr int kNvfp4TableBytes = 128 * 4;
 
 // Launch helpers implemented in aq_kernels.cu; each returns the CUDA error of the launch.
 cudaError_t launch_gemm(const GemmParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
@@ -312,7 +334,7 @@ cudaError_t launch_gated_act(uint16_t* g, const uint16_t* u, int64_t ld, int64_t
 cudaError_t configure_decode2(size_t max_smem);
 cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t st, bool pdl);
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
-                              bool pdl);
+                              bool pdl, int out_kind = kPreBf16);
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t configure_kernels(int device, size_t max_smem);
 // Records the message aq_last_error() returns on this thread and passes the status through.

@@ -14,7 +14,11 @@
 //                        plain TMA loads (no multicast) and the even CTA's MMA reads both.
 // aq_transpose_kernel    V [in, r] -> V^T [r, in] so the prefill t GEMM is K-major.
 // aq_precompute_kernel   U V^T on tcgen05 (K = r), W0 tiles TMA-loaded and fused in the
-//                        epilogue, W_eff written back with TMA stores.
+//                        epilogue, W_eff written back with TMA stores; or, never forming
+//                        the bf16 weight, the per-CTA max|W_eff| (amax pass) or W_eff
+//                        quantized to NVFP4 in the epilogue ("Internals and extension",
+//                        "Nvfp4Spec": E2M1 pairs per byte, an E4M3 scale per 16 values
+//                        along K, one fp32 global scale).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -763,7 +767,117 @@ __global__ void __launch_bounds__(256) aq_transpose_kernel(const __grid_constant
 // ------------------------------------------------------------------------------------
 constexpr int kPreMaxCBufs = 8;   // W0 / W_eff tile buffers per CTA (p.cbufs of them used)
 constexpr int kPreAcc = 2;     // TMEM accumulators
+constexpr int kPreRedOffset = 768;   // header bytes holding the epilogue warps' maxima
 
+// FP8 E4M3 byte of a non-negative fp32: nearest, ties to even, clamped to 448.
+__device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float a) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(a));
+  return r & 0xFFu;
+}
+
+// Value of a finite non-negative E4M3 byte: exponent bias 7, 3 mantissa bits, subnormal
+// step 2^-9 (exact in fp32).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u;
+  const uint32_t m = b & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0x1p-9f;
+}
+
+// Eight fp32 values to E2M1 codes (nearest, ties to even, clamped to +-6, sign kept), the
+// first value in the lowest nibble.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1(const float* q) {
+  uint32_t r;
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n"
+      "}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
+// One block of 16 values: returns its E4M3 scale byte, codes in two words. a = max|v|,
+// scale = E4M3(a / (6 g)), d = scale * g, code = E2M1(v * (1 / d)); each step one fp32
+// operation rounded to nearest even (1 / d per scale byte precomputed in inv_tbl, 0 where d
+// is 0); d = 0 stores +0 codes.
+__device__ __forceinline__ uint32_t nvfp4_block(const float* v, float six_g, const float* inv_tbl, uint2* codes) {
+  // max|v| as a tree (max is exact in any order)
+  float m8[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m8[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 8]));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m8[j] = fmaxf(m8[j], m8[j + 4]);
+  const float a = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
+  const float t = six_g > 0.0f ? __fdiv_rn(a, six_g) : 0.0f;
+  const uint32_t sf = f32_to_e4m3_satfinite(t);
+  const float inv = inv_tbl[sf];
+  if (!(inv > 0.0f)) {
+    *codes = make_uint2(0u, 0u);
+    return sf;
+  }
+  float q[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], inv);
+  *codes = make_uint2(f32x8_to_e2m1(q), f32x8_to_e2m1(q + 8));
+  return sf;
+}
+
+// Max over the 512 epilogue threads of the precompute kernel (named barrier 1); every
+// epilogue thread gets the result.
+__device__ __forceinline__ float epilogue_max(float m, float* red, int warp, int lane) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[warp - 2] = m;
+  named_bar_sync(1, kPreThreads - 64);
+  float r = 0.0f;
+#pragma unroll
+  for (int w = 0; w < (kPreThreads - 64) / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// This CTA's tiles: blockIdx.x, then every gridDim.x-th (so that the CTAs together sweep
+// the weight front to back), walked last to first when reversed; (row band, column tile)
+// stepped without divisions.
+struct TileWalk {
+  int count;     // tiles of this CTA
+  int row, col;  // the current tile
+  int n_col, drow, dcol;
+  bool rev;
+  __device__ __forceinline__ TileWalk(int total, int n_col_, bool rev_) : n_col(n_col_), rev(rev_) {
+    const int g = static_cast<int>(gridDim.x);
+    const int b = static_cast<int>(blockIdx.x);
+    count = b < total ? (total - 1 - b) / g + 1 : 0;
+    const int t = rev ? total - 1 - b : b;
+    row = t / n_col;
+    col = t - row * n_col;
+    drow = g / n_col;
+    dcol = g - drow * n_col;
+  }
+  __device__ __forceinline__ void next() {
+    if (rev) {
+      col -= dcol;
+      row -= drow;
+      if (col < 0) {
+        col += n_col;
+        --row;
+      }
+    } else {
+      col += dcol;
+      row += drow;
+      if (col >= n_col) {
+        col -= n_col;
+        ++row;
+      }
+    }
+  }
+};
+
+template <int kOut>
 __global__ void __launch_bounds__(kPreThreads, 1)
     aq_precompute_kernel(const __grid_constant__ PrecomputeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -779,14 +893,19 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t cbuf_bytes = static_cast<uint32_t>(p.bn) * 256u;  // bn/64 boxes of 128 x 128 B
+  const int nkb = p.r > 0 ? ceil_div_i(p.r, kBK) : 0;
   uint8_t* cbuf = smem + kHeaderBytes;
-  uint8_t* ring = cbuf + p.cbufs * cbuf_bytes;
+  uint8_t* ring = cbuf + p.cbufs * cbuf_bytes;                              // U / V chunks
+  // kPreNvfp4: 1/d for each of the 128 scale bytes
+  float* inv_tbl = reinterpret_cast<float*>(ring + static_cast<size_t>(p.stages) * p.stage_bytes);
+  float* red = reinterpret_cast<float*>(smem + kPreRedOffset);
+  // tile order: last to first when the amax pass just walked them first to last
+  const bool rev = kOut == kPreNvfp4 && p.reverse != 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const AbortCtl ctl{abort_flag, p.status, p.timeout_ns};
   const bool has_mma = p.r > 0;
-  const int nkb = has_mma ? ceil_div_i(p.r, kBK) : 0;
   const int nbox = p.bn / 64;
 
   if (threadIdx.x == 0) {
@@ -796,7 +915,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
     for (int b = 0; b < p.cbufs; ++b) {
       mbar_init(&c_full[b], 1);
-      mbar_init(&c_empty[b], 1);
+      // bf16: the leader frees a buffer after its store; otherwise every epilogue thread
+      // frees it once it has read its row segment
+      mbar_init(&c_empty[b], kOut == kPreBf16 ? 1 : kPreThreads - 64);
       mbar_init(&epi_done[b], kPreThreads - 64);
     }
     for (int b = 0; b < kPreAcc; ++b) {
@@ -809,7 +930,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_w0);
-    tma_prefetch_desc(&p.tm_we);
+    if (kOut == kPreBf16) tma_prefetch_desc(&p.tm_we);
     if (has_mma) {
       tma_prefetch_desc(&p.tm_u);
       tma_prefetch_desc(&p.tm_v);
@@ -832,14 +953,17 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     // allow, lane 1 feeds the U / V chunks of the MMA. One thread doing both would tie the
     // W0 prefetch depth to the MMA's progress through the short U / V ring.
     if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();
+      // the amax pass leaves W0 in L2 for the quantizing pass that follows it
+      const uint64_t pol_stream = kOut == kPreAmax ? policy_evict_normal() : policy_evict_first();
       uint32_t cfilled = 0, cfill_par = 0;
       bool ok = true;
       pdl_wait_prior_grid();
-      int it = 0;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-        const int o0 = (tile / p.n_col_tiles) * kMmaM;
-        const int i0 = (tile % p.n_col_tiles) * p.bn;
+      TileWalk tr(p.total_tiles, p.n_col_tiles, rev);
+      TileWalk pf = tr;   // pf_ahead tiles ahead: prefetched into L2 beyond the tile buffers
+      for (int a = 0; a < p.pf_ahead; ++a) pf.next();
+      for (int it = 0; ok && it < tr.count; ++it, tr.next()) {
+        const int o0 = tr.row * kMmaM;
+        const int i0 = tr.col * p.bn;
         const int cb = it % p.cbufs;
         const uint32_t cph = static_cast<uint32_t>(it / p.cbufs) & 1u;
         if (!mbar_wait(&c_empty[cb], cph ^ 1u, ctl)) {
@@ -850,6 +974,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         for (int j = 0; j < nbox; ++j)
           tma_load_2d(cbuf + cb * cbuf_bytes + j * kStageA, &p.tm_w0, i0 + 64 * j, o0, &c_full[cb],
                       pol_stream);
+        if (p.pf_ahead > 0 && it + p.pf_ahead < tr.count) {
+          for (int j = 0; j < nbox; ++j) tma_prefetch_l2_2d(&p.tm_w0, pf.col * p.bn + 64 * j, pf.row * kMmaM);
+          pf.next();
+        }
         cfilled |= 1u << cb;
         cfill_par = (cfill_par & ~(1u << cb)) | (cph << cb);
       }
@@ -863,9 +991,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       uint32_t phase = 0;
       uint32_t filled = 0, fill_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        const int o0 = (tile / p.n_col_tiles) * kMmaM;
-        const int i0 = (tile % p.n_col_tiles) * p.bn;
+      TileWalk tr(p.total_tiles, p.n_col_tiles, rev);
+      for (int it = 0; ok && it < tr.count; ++it, tr.next()) {
+        const int o0 = tr.row * kMmaM;
+        const int i0 = tr.col * p.bn;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, ctl)) {
             ok = false;
@@ -884,8 +1013,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         }
       }
       if (!ok) {
-        for (int s = 0; s < p.stages; ++s)
-          if (filled & (1u << s)) mbar_wait_drain(&full[s], (fill_par >> s) & 1u, kDrainNs);
+        for (int s2 = 0; s2 < p.stages; ++s2)
+          if (filled & (1u << s2)) mbar_wait_drain(&full[s2], (fill_par >> s2) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -894,8 +1023,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int it = 0;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const int count = TileWalk(p.total_tiles, p.n_col_tiles, rev).count;
+      for (int it = 0; ok && it < count; ++it) {
         const int ab = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
         if (!warp_wait(&acc_empty[ab], aph ^ 1u, ctl)) break;
@@ -937,79 +1066,159 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const int lrow = q * 32 + lane;  // row of the tile (TMEM lane) this thread owns
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const bool leader = (warp == 2 && lane == 0);
-    const int chalf = (warp - 2) >> 2;  // which part of the tile's columns this warp does
-    constexpr int kParts = (kPreThreads - 64) / 128;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const int o0 = (tile / p.n_col_tiles) * kMmaM;
-      const int i0 = (tile % p.n_col_tiles) * p.bn;
-      const int cb = it % p.cbufs;
-      const uint32_t cph = static_cast<uint32_t>(it / p.cbufs) & 1u;
-      const int ab = it & 1;
-      const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+    const int et = threadIdx.x - 64;   // epilogue thread index, 0..511
+    // four warps per TMEM lane quadrant, each 32 of the tile's 128 columns (bn = 128)
+    const int c = ((warp - 2) >> 2) * 32;
+    float amax = 0.0f;   // kPreAmax: this thread's max|W_eff|
+    float six_g = 0.0f;
+    if (kOut == kPreNvfp4) {
+      // the global scale: given, or amax / (6 * 448) from the amax pass's partial maxima
+      pdl_wait_prior_grid();
+      float g;
+      if (p.scale_given) {
+        g = *p.gscale;
+      } else {
+        float m = 0.0f;
+        for (int i = et; i < p.n_partials; i += kPreThreads - 64) m = fmaxf(m, p.partials[i]);
+        g = __fdiv_rn(epilogue_max(m, red, warp, lane), 2688.0f);
+        if (blockIdx.x == 0 && et == 0) *p.gscale = g;
+      }
+      six_g = __fmul_rn(6.0f, g);
+      // 1/d for each scale byte a block can take: d = value(scale) * g, each one rounding
+      if (et < 128) {
+        const float dd = __fmul_rn(e4m3_value(static_cast<uint32_t>(et)), g);
+        inv_tbl[et] = dd > 0.0f ? __frcp_rn(dd) : 0.0f;
+      }
+      named_bar_sync(1, kPreThreads - 64);
+    }
+    TileWalk tr(p.total_tiles, p.n_col_tiles, rev);
+    int cb = 0, ab = 0;
+    uint32_t cph = 0, aph = 0;
+    // s of the row this thread owns, loaded one tile ahead (the load's latency is hidden
+    // behind a tile)
+    uint16_t s_next = (tr.row * kMmaM + lrow < p.out) ? p.s[tr.row * kMmaM + lrow] : uint16_t(0);
+    for (int it = 0; it < tr.count; ++it) {
+      const int o0 = tr.row * kMmaM;
+      const int i0 = tr.col * p.bn;
+      const float sc = bf16_to_f32(s_next);
       if (!warp_wait(&c_full[cb], cph, ctl)) break;
+      const int o = o0 + lrow;
+      uint8_t* ctile = cbuf + cb * cbuf_bytes;
+      // W0 row segment: box (c / 64), four 16-byte chunks at swizzled positions.
+      uint8_t* rowp = ctile + (c / 64) * kStageA + lrow * 128;
+      const int ch0 = (c % 64) / 8;
+      uint4 w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) w[h] = *reinterpret_cast<const uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4));
+      // amax / NVFP4 only read the tile: its buffer is free again once every thread has it
+      if (kOut != kPreBf16) mbar_arrive(&c_empty[cb]);
+      float d[32];
       if (has_mma) {
         if (!warp_wait(&acc_full[ab], aph, ctl)) break;
         tc_fence_after();
+        float d0[16], d1[16];
+        tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c), d0);
+        tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c + 16), d1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          d[j] = d0[j];
+          d[16 + j] = d1[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) d[j] = 0.0f;
       }
-      const int o = o0 + lrow;
-      const float sc = (o < p.out) ? bf16_to_f32(p.s[o]) : 0.0f;
-      uint8_t* ctile = cbuf + cb * cbuf_bytes;
-      const int cw = p.bn / kParts;   // columns per warp, a multiple of 32
-      for (int c = chalf * cw; c < (chalf + 1) * cw; c += 32) {
-        float d[32];
-        if (has_mma) {
-          float d0[16], d1[16];
-          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c), d0);
-          tmem_ld_16(t_lane + static_cast<uint32_t>(ab * p.bn + c + 16), d1);
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            d[j] = d0[j];
-            d[16 + j] = d1[j];
-          }
-        } else {
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t ww[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
+        uint32_t res[4];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = 0.0f;
-        }
-        // W0 row segment: box (c / 64), four 16-byte chunks at swizzled positions.
-        uint8_t* rowp = ctile + (c / 64) * kStageA + lrow * 128;
-        const int ch0 = (c % 64) / 8;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint4* cp = reinterpret_cast<uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4));
-          const uint4 w = *cp;
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          uint32_t res[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = fmaf(sc, __uint_as_float(ww[e] << 16), d[h * 8 + 2 * e]);
-            const float hi = fmaf(sc, __uint_as_float(ww[e] & 0xFFFF0000u), d[h * 8 + 2 * e + 1]);
+        for (int e = 0; e < 4; ++e) {
+          const float lo = fmaf(sc, __uint_as_float(ww[e] << 16), d[h * 8 + 2 * e]);
+          const float hi = fmaf(sc, __uint_as_float(ww[e] & 0xFFFF0000u), d[h * 8 + 2 * e + 1]);
+          if (kOut == kPreBf16) {
             res[e] = pack_bf16x2(lo, hi);
+          } else {
+            d[h * 8 + 2 * e] = lo;
+            d[h * 8 + 2 * e + 1] = hi;
           }
-          *cp = make_uint4(res[0], res[1], res[2], res[3]);
         }
+        if (kOut == kPreBf16)
+          *reinterpret_cast<uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4)) = make_uint4(res[0], res[1], res[2], res[3]);
       }
       if (has_mma) {
         tc_fence_before();
         mbar_arrive(&acc_empty[ab]);
       }
-      // All 128 epilogue threads publish their rows; the leader waits (bounded) for
-      // all of them, then one TMA store per 64-column box writes the tile out.
-      fence_proxy_async_smem();
-      mbar_arrive(&epi_done[cb]);
-      if (leader) {
-        if (!mbar_wait(&epi_done[cb], cph, ctl)) break;
-        for (int j = 0; j < nbox; ++j) tma_store_2d(&p.tm_we, ctile + j * kStageA, i0 + 64 * j, o0);
-        tma_store_commit();
-        // one store group may still be reading its buffer: release the previous tile's
-        if (it > 0) {
-          tma_store_wait_read_but_one();
-          mbar_arrive(&c_empty[(it - 1) % p.cbufs]);
+      if (kOut == kPreAmax) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(d[j]));
+      } else if (kOut == kPreNvfp4) {
+        uint2 codes[2];
+        const uint32_t sf0 = nvfp4_block(d, six_g, inv_tbl, &codes[0]);
+        const uint32_t sf1 = nvfp4_block(d + 16, six_g, inv_tbl, &codes[1]);
+        const int col = i0 + c;   // first W_eff column of the two blocks (a multiple of 32)
+        // codes straight from registers: a warp writes 16 bytes of each of 32 rows, the other
+        // warps of the quadrant the rest of those rows' 64 bytes (measured faster than staging
+        // the tile for full-row stores behind a per-tile barrier)
+        if (o < p.out && col < p.in) {
+          uint8_t* dst = p.q + static_cast<int64_t>(o) * p.ldq + col / 2;
+          if (col + 16 < p.in && p.q16) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y);
+          } else {
+            *reinterpret_cast<uint2*>(dst) = codes[0];
+            if (col + 16 < p.in) *reinterpret_cast<uint2*>(dst + 8) = codes[1];
+          }
+        }
+        if (p.sf_layout == 0) {
+          if (o < p.out) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+              if (col + 16 * b < p.in)
+                p.sf[static_cast<int64_t>(o) * p.sf_cols + col / 16 + b] = static_cast<uint8_t>(b ? sf1 : sf0);
+          }
+        } else {
+          // 128x4 tiles of 512 bytes, K tiles fastest; row r, column k of a tile at
+          // 16 (r mod 32) + 4 (r div 32) + k. Rows past out and columns past in/16 up to the
+          // padded shape hold the zero scales of their zero weights.
+          const int kb0 = col / 16;
+          if ((kb0 >> 2) < p.sf_ktiles)
+            *reinterpret_cast<uint16_t*>(p.sf + (static_cast<int64_t>(tr.row) * p.sf_ktiles + (kb0 >> 2)) * 512 +
+                                         (lrow & 31) * 16 + (lrow >> 5) * 4 + (kb0 & 3)) =
+                static_cast<uint16_t>(sf0 | (sf1 << 8));
+        }
+      } else {
+        // All epilogue threads publish their rows; the leader waits (bounded) for all of
+        // them, then one TMA store per 64-column box writes the tile out.
+        fence_proxy_async_smem();
+        mbar_arrive(&epi_done[cb]);
+        if (leader) {
+          if (!mbar_wait(&epi_done[cb], cph, ctl)) break;
+          for (int j = 0; j < nbox; ++j) tma_store_2d(&p.tm_we, ctile + j * kStageA, i0 + 64 * j, o0);
+          tma_store_commit();
+          // one store group may still be reading its buffer: release the previous tile's
+          if (it > 0) {
+            tma_store_wait_read_but_one();
+            mbar_arrive(&c_empty[cb == 0 ? p.cbufs - 1 : cb - 1]);
+          }
         }
       }
+      // next tile of this CTA and its buffers
+      tr.next();
+      if (it + 1 < tr.count) s_next = (tr.row * kMmaM + lrow < p.out) ? p.s[tr.row * kMmaM + lrow] : uint16_t(0);
+      if (++cb == p.cbufs) {
+        cb = 0;
+        cph ^= 1u;
+      }
+      ab ^= 1;
+      if (ab == 0) aph ^= 1u;
     }
-    if (leader) tma_store_wait_all();
+    if (kOut == kPreBf16 && leader) tma_store_wait_all();
+    if (kOut == kPreAmax) {
+      const float m = epilogue_max(amax, red, warp, lane);
+      if (warp == 2 && lane == 0) p.partials[blockIdx.x] = m;
+    }
   }
 
   tc_fence_before();
@@ -1105,10 +1314,12 @@ cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t s
 }
 
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
-                              bool pdl) {
+                              bool pdl, int out_kind) {
   void* args[] = {const_cast<PrecomputeParams*>(&p)};
-  return launch_ex(reinterpret_cast<const void*>(&aq_precompute_kernel), dim3(grid), dim3(kPreThreads),
-                   smem, st, pdl, args);
+  const void* fn = out_kind == kPreAmax    ? reinterpret_cast<const void*>(&aq_precompute_kernel<kPreAmax>)
+                   : out_kind == kPreNvfp4 ? reinterpret_cast<const void*>(&aq_precompute_kernel<kPreNvfp4>)
+                                           : reinterpret_cast<const void*>(&aq_precompute_kernel<kPreBf16>);
+  return launch_ex(fn, dim3(grid), dim3(kPreThreads), smem, st, pdl, args);
 }
 
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st) {
@@ -1126,7 +1337,11 @@ cudaError_t configure_kernels(int device, size_t max_smem) {
   if ((e = cudaFuncSetAttribute(aq_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
   if ((e = configure_decode(max_smem))) return e;
   if ((e = configure_decode2(max_smem))) return e;
-  if ((e = cudaFuncSetAttribute(aq_precompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+  if ((e = cudaFuncSetAttribute(aq_precompute_kernel<kPreBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+    return e;
+  if ((e = cudaFuncSetAttribute(aq_precompute_kernel<kPreAmax>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
+    return e;
+  if ((e = cudaFuncSetAttribute(aq_precompute_kernel<kPreNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, s)))
     return e;
   return cudaSuccess;
 }
