@@ -1111,7 +1111,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 #pragma unroll
       for (int h = 0; h < 4; ++h) w[h] = *reinterpret_cast<const uint4*>(rowp + (((ch0 + h) ^ (lrow & 7)) << 4));
       // amax / NVFP4 only read the tile: its buffer is free again once every thread has it
-      if (kOut != kPreBf16) mbar_arrive(&c_empty[cb]);
+      // (the proxy fence orders these reads before the next TMA write into the buffer)
+      if (kOut != kPreBf16) {
+        fence_proxy_async_smem();
+        mbar_arrive(&c_empty[cb]);
+      }
       float d[32];
       if (has_mma) {
         if (!warp_wait(&acc_full[ab], aph, ctl)) break;

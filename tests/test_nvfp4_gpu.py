@@ -71,6 +71,25 @@ def test_exact_inputs_bit_exact(shape, given, layout):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("given", [False, True], ids=["from_amax", "given"])
+def test_exact_inputs_full_size_repeated(given):
+    """The 31B-class square projection (5376 x 5376, r = 128) on exact integer inputs, every
+    code and scale compared bit for bit, three launches in a row (the tile buffers are
+    recycled hundreds of times per CTA: a buffer freed too early would show here)."""
+    out, inp, r = 5376, 5376, 128
+    th = synth.small_int_theta(("nvfp4-full", out, inp, r), out, inp, r)
+    x = nvfp4.weff_f32(*th.f64())
+    g = nvfp4.global_scale(np.max(np.abs(x))) if not given else np.float32(0.0117)
+    codes_ref, sf_ref = nvfp4.quantize(x, g)
+    del x
+    for _ in range(3):
+        codes, sf, g_gpu = _run(th, aq.AQ_SF_128X4, float(g) if given else None)
+        assert g_gpu == g
+        np.testing.assert_array_equal(sf, sf_ref)
+        np.testing.assert_array_equal(codes, codes_ref)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["linear", "128x4"])
 def test_hand_worked_row_on_the_gpu(layout):
     """The golden row (ties, a subnormal scale, saturation, negative zero) as row 1 of a
