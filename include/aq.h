@@ -225,9 +225,9 @@ aq_status aq_precompute(const aq_theta* th, void* W_eff, int64_t ld_weff, void* 
  * The value quantized is the fp32 W_eff of aq_precompute before its bf16 rounding. The
  * rule, each step one fp32 operation rounded to nearest even (the pages state none):
  *   g = global scale (decode multiplier: weight = e2m1 * e4m3 * g)
- *   per 16 values x along in: a = max|x|; scale = E4M3(a / (6 g)), ties to even,
- *   clamped to 448; d = scale * g; code = E2M1(x * (1/d)), ties to the even code, clamped
- *   to +-6, sign of x kept (a d of 0 gives +0 codes).
+ *   per 16 values x along in: a = max|x|; scale = E4M3(a * (1/(6 g))), ties to even,
+ *   clamped to 448 (1/(6 g) formed once); d = scale * g; code = E2M1(x * (1/d)), ties to the
+ *   even code, clamped to +-6, sign of x kept (a d of 0 gives +0 codes).
  * Codes: byte j of a row holds columns 2j (low nibble) and 2j+1 (high nibble).
  *
  * q: [out, in/2] bytes, device, row stride ldq >= in/2 bytes, ldq and q 8-byte aligned.

@@ -23,12 +23,13 @@ Readings where the pages are silent (each also listed in the design notes):
 * The stored global scale g is the decode multiplier: a weight decodes as
   e2m1 · e4m3 · g. Unless the caller gives g, it is amax / 2688 in fp32, amax = max|W_eff|
   and 2688 = 6 · 448, so that the largest block scale lands on the largest E4M3 value.
-* One block: a = max|x|; t = a / (6·g); the stored scale is E4M3(t), rounded to nearest
-  even and clamped to 448 ("satfinite"); d = E4M3(t) · g; each x becomes
-  E2M1(x · (1/d)), rounded to nearest even (ties to the even code), clamped to ±6, keeping
-  the sign of x (a small negative x gives −0). A block whose d is 0 stores +0 codes.
-  Every one of these operations is a single fp32 operation rounded to nearest even; they
-  are the decision steps both sides take in the same precision.
+* One block: a = max|x|; t = a · (1/(6·g)), the factor 1/(6·g) formed once per tensor; the
+  stored scale is E4M3(t), rounded to nearest even and clamped to 448 ("satfinite");
+  d = E4M3(t) · g; each x becomes E2M1(x · (1/d)), rounded to nearest even (ties to the even
+  code), clamped to ±6, keeping the sign of x (a small negative x gives −0). A block whose d
+  is 0 stores +0 codes. Every one of these operations is a single fp32 operation rounded to
+  nearest even (6·g, 1/(6·g), a·that, value·g, 1/d, x·that); they are the decision steps both
+  sides take in the same precision.
 * Two codes per byte, the even column in the low nibble.
 * The "128x4" layout's order inside a tile is not on the pages. Taken here: 128-row by
   4-column tiles of 512 bytes, tiles ordered with the K direction fastest, and inside a
@@ -132,9 +133,9 @@ def quantize(x32, g):
     g = np.float32(g)
     blocks = x.reshape(N, K // BLOCK, BLOCK)
     a = np.max(np.abs(blocks), axis=2)                        # exact in fp32
-    denom = np.float32(np.float32(6.0) * g)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        t = np.where(denom > 0, a / denom, np.float32(0)).astype(np.float32)
+    six_g = np.float32(np.float32(6.0) * g)
+    inv6 = np.float32(np.float32(1.0) / six_g) if six_g > 0 else np.float32(0.0)
+    t = (a * inv6).astype(np.float32)
     sf = e4m3_round(t)
     d = (e4m3_value(sf).astype(np.float32) * g).astype(np.float32)
     with np.errstate(divide="ignore"):
