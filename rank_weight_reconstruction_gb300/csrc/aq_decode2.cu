@@ -14,11 +14,12 @@
 //     fragments of V^T through ldmatrix.trans, and the x fragments the W0 product loads anyway
 //     are the B operand. The t product is a second, independent mma chain of the same loop.
 //   * After the loop every CTA holds partial sums over its K slice of W0 x (its rows) and of
-//     t. They are added across the cluster through distributed shared memory: each CTA sums
-//     its own t partials, the cluster barrier publishes them, every CTA reads the C partial
-//     t and, for the rows it finishes (1/C of the cluster's rows), the C partial sums of W0 x.
-//     y = RN_bf16(s * z + U t) is formed in fp32 (U t on the FP32 pipes: r products per
-//     output) and rounded once.
+//     t. They are added across the cluster through distributed shared memory, by stores only:
+//     each CTA sums its own partials (k-block groups, warps) and pushes, with 16-byte stores
+//     into the peers' shared memory, the W0 x sums of the rows peer q finishes (1/C of the
+//     cluster's rows) to q and its t to every peer. One cluster barrier publishes the pushes;
+//     every CTA then adds the C partials it received, in rank order. y = RN_bf16(s * z + U t)
+//     is formed in fp32 (U t on the FP32 pipes: r products per output) and rounded once.
 // Warp 0 feeds the TMA ring (one lane); warps 1..8 run mma.sync m16n8k16 (bf16 in, fp32
 // accumulate). Every wait on an mbarrier is bounded; a CTA whose wait expires records
 // AQ_ERR_TIMEOUT, skips the remaining work and still takes part in every barrier, so the

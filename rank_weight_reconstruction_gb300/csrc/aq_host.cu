@@ -1204,6 +1204,7 @@ aq_status aq_mlp(const aq_theta* gate, const aq_theta* up, const aq_theta* down,
 }
 
 constexpr int kPrePfAhead = 4;   // precompute: W0 tiles of a CTA prefetched into L2 ahead
+constexpr int kPreNvfp4Keep = 3;  // NVFP4 frees its W0 buffers on read: three suffice (2-4 measured equal)
 
 // Tiles, tensor maps and shared-memory budget of the precompute kernel (any output kind).
 static aq_status plan_precompute(const aq_theta* th, DevInfo* dev, PrecomputeParams* pp, size_t* smem,
@@ -1233,7 +1234,8 @@ static aq_status plan_precompute(const aq_theta* th, DevInfo* dev, PrecomputePar
   const size_t base = kSmemSlack + kHeaderBytes + staging;
   const int nkb = static_cast<int>(ceil_div(th->r, kBK));
   if (th->r > 0) {
-    const size_t room = cap > base + 4 * cbuf_bytes ? cap - base - 4 * cbuf_bytes : 0;
+    const size_t keep = (out_kind == kPreBf16 ? 4 : kPreNvfp4Keep) * cbuf_bytes;
+    const size_t room = cap > base + keep ? cap - base - keep : 0;
     pp->stages = static_cast<int32_t>(std::max<size_t>(2, std::min<size_t>(2 * nkb, room / pp->stage_bytes)));
   } else {
     pp->stages = 0;

@@ -801,20 +801,25 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1(const float* q) {
   return r;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // One block of 16 values: returns its E4M3 scale byte, codes in two words. a = max|v|,
-// scale = E4M3(a / (6 g)), d = scale * g, code = E2M1(v * (1 / d)); each step one fp32
-// operation rounded to nearest even (1 / d per scale byte precomputed in inv_tbl, 0 where d
-// is 0); d = 0 stores +0 codes.
-__device__ __forceinline__ uint32_t nvfp4_block(const float* v, float six_g, const float* inv_tbl, uint2* codes) {
-  // max|v| as a tree (max is exact in any order)
-  float m8[8];
+// scale = E4M3(a * (1 / (6 g))), d = scale * g, code = E2M1(v * (1 / d)); each step one fp32
+// operation rounded to nearest even (1 / (6 g) formed once per CTA; 1 / d per scale byte
+// precomputed in inv_tbl, 0 where d is 0); d = 0 stores +0 codes.
+__device__ __forceinline__ uint32_t nvfp4_block(const float* v, float inv6g, const float* inv_tbl, uint2* codes) {
+  // max|v| as a tree of three-input maxima (max is exact in any order)
+  float m[6];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) m8[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 8]));
-#pragma unroll
-  for (int j = 0; j < 4; ++j) m8[j] = fmaxf(m8[j], m8[j + 4]);
-  const float a = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
-  const float t = six_g > 0.0f ? __fdiv_rn(a, six_g) : 0.0f;
-  const uint32_t sf = f32_to_e4m3_satfinite(t);
+  for (int j = 0; j < 5; ++j) m[j] = fmax3(fabsf(v[3 * j]), fabsf(v[3 * j + 1]), fabsf(v[3 * j + 2]));
+  m[5] = fabsf(v[15]);
+  const float a = fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]));
+  const uint32_t sf = f32_to_e4m3_satfinite(__fmul_rn(a, inv6g));
   const float inv = inv_tbl[sf];
   if (!(inv > 0.0f)) {
     *codes = make_uint2(0u, 0u);
@@ -1070,7 +1075,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     // four warps per TMEM lane quadrant, each 32 of the tile's 128 columns (bn = 128)
     const int c = ((warp - 2) >> 2) * 32;
     float amax = 0.0f;   // kPreAmax: this thread's max|W_eff|
-    float six_g = 0.0f;
+    float inv6g = 0.0f;
     if (kOut == kPreNvfp4) {
       // the global scale: given, or amax / (6 * 448) from the amax pass's partial maxima
       pdl_wait_prior_grid();
@@ -1083,7 +1088,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         g = __fdiv_rn(epilogue_max(m, red, warp, lane), 2688.0f);
         if (blockIdx.x == 0 && et == 0) *p.gscale = g;
       }
-      six_g = __fmul_rn(6.0f, g);
+      const float six_g = __fmul_rn(6.0f, g);
+      inv6g = six_g > 0.0f ? __frcp_rn(six_g) : 0.0f;
       // 1/d for each scale byte a block can take: d = value(scale) * g, each one rounding
       if (et < 128) {
         const float dd = __fmul_rn(e4m3_value(static_cast<uint32_t>(et)), g);
@@ -1157,11 +1163,14 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
       if (kOut == kPreAmax) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(d[j]));
+        for (int j = 0; j < 30; j += 6)
+          amax = fmax3(amax, fmax3(fabsf(d[j]), fabsf(d[j + 1]), fabsf(d[j + 2])),
+                       fmax3(fabsf(d[j + 3]), fabsf(d[j + 4]), fabsf(d[j + 5])));
+        amax = fmax3(amax, fabsf(d[30]), fabsf(d[31]));
       } else if (kOut == kPreNvfp4) {
         uint2 codes[2];
-        const uint32_t sf0 = nvfp4_block(d, six_g, inv_tbl, &codes[0]);
-        const uint32_t sf1 = nvfp4_block(d + 16, six_g, inv_tbl, &codes[1]);
+        const uint32_t sf0 = nvfp4_block(d, inv6g, inv_tbl, &codes[0]);
+        const uint32_t sf1 = nvfp4_block(d + 16, inv6g, inv_tbl, &codes[1]);
         const int col = i0 + c;   // first W_eff column of the two blocks (a multiple of 32)
         // codes straight from registers: a warp writes 16 bytes of each of 32 rows, the other
         // warps of the quadrant the rest of those rows' 64 bytes (measured faster than staging
