@@ -897,6 +897,14 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     if (cl == 1 || smem >= kGemmPairMinSmem) break;
   }
   gp.n_tok_units = static_cast<int32_t>(ceil_div(gp.n_tok_tiles, gp.cluster));
+  // Walk order: the larger operand streams once, the smaller is re-read from L2. More tokens
+  // than output rows (the Gemma-sized families at thousands of tokens) walk a token unit's row
+  // tiles first; otherwise (the 31B-class rows) a row tile's token units first.
+  {
+    int64_t rows_total = 0;
+    for (int j = 0; j < n; ++j) rows_total += th[j]->out;
+    gp.tok_major = (!midm && M > rows_total) ? 1 : 0;
+  }
   const int box_rows = gp.row_tile / gp.cluster;
   // t = x V as the first tiles of the same launch, when the sync region holds a flag per
   // token tile; otherwise as a GEMM launch of its own before it

@@ -58,6 +58,8 @@ struct GemmParams {
                         //    CTA loads half of the row operand (its own TMA loads, no
                         //    multicast) and the pair's 2-SM MMAs read both halves
   int32_t n_tok_units;  // ceil(n_tok_tiles / cluster): token tiles per row tile, in pairs
+  int32_t tok_major;    // 1: units walk a token unit's row tiles first (x read once, the row
+                        //    operand kept in L2); 0: a row tile's token units first
   int32_t total_tiles;  // work units: row tiles x n_tok_units, summed over the segments
   int32_t n_mma;        // MMA N: round_up(row_tile, 16)
   int32_t stages;

@@ -64,7 +64,10 @@ struct TileCoord {
 };
 
 // Work unit -> tile of this CTA: a unit is one row tile and `cluster` adjacent token tiles,
-// one per CTA of the cluster (rank crank), token tiles fastest.
+// one per CTA of the cluster (rank crank). Consecutive units (which run at the same time) share
+// the operand that is re-read: token units fastest keep the token tiles in L2 while each row
+// tile streams once; row tiles fastest (tok_major) keep the rows in L2 while each token tile
+// streams once.
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, int crank) {
   int si = 0;
 #pragma unroll
@@ -73,8 +76,11 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int unit, i
   const int local = unit - p.seg[si].tile_begin;
   TileCoord c;
   c.seg = si;
-  c.tok0 = ((local % p.n_tok_units) * p.cluster + crank) * p.tok_tile;
-  c.row0 = (local / p.n_tok_units) * p.row_tile;
+  const int nrt = p.seg[si].n_row_tiles;
+  const int tu = p.tok_major ? local / nrt : local % p.n_tok_units;
+  const int rt = p.tok_major ? local - tu * nrt : local / p.n_tok_units;
+  c.tok0 = (tu * p.cluster + crank) * p.tok_tile;
+  c.row0 = rt * p.row_tile;
   return c;
 }
 
@@ -209,13 +215,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol = policy_evict_normal();
+      // the operand that later waves of tiles read again stays in L2 (evict-last); the other is
+      // shared by the tiles running at the same time, so it keeps the normal policy (an
+      // evict-first stream was measured to re-read it from DRAM)
+      const uint64_t pol_tok = p.tok_major ? policy_evict_normal() : policy_evict_last();
+      const uint64_t pol_row = p.tok_major ? policy_evict_last() : policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t filled = 0, fill_par = 0;
       bool ok = true;
       // one box into this CTA's stage, counted on the even CTA's `full` barrier
-      auto load = [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+      auto load = [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar, uint64_t pol) {
         if constexpr (kPair) {
           tma_load_2d_pair(dst, m, c0, c1, cluster_map(bar, 0), pol);
         } else {
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       };
       // B: the whole N rows, or this CTA's half of them (rows n_mma / 2 apart)
       auto load_rows = [&](uint8_t* st, const CUtensorMap* m, int kb, int row0, int n_mma, uint64_t* bar) {
-        load(st + kStageA, m, kb * kBK, row0 + crank * (n_mma / cl), bar);
+        load(st + kStageA, m, kb * kBK, row0 + crank * (n_mma / cl), bar, pol_row);
       };
       // one k block of work item (tile, low) into the next stage
       auto push = [&](const TileCoord& tc, const GemmSeg& sg, bool low, int kb) -> bool {
@@ -233,11 +243,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         if (leader) mbar_arrive_expect_tx(&full[stage], tx_bytes);
         if constexpr (kSwap) {
           // A = 128 rows (W0, or U), B = the tokens (x, or t for the rank-r blocks)
-          load(st, low ? &sg.tm_u : &sg.tm_w, kb * kBK, tc.row0, &full[stage]);
-          load(st + kStageA, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
+          load(st, low ? &sg.tm_u : &sg.tm_w, kb * kBK, tc.row0, &full[stage], pol_row);
+          load(st + kStageA, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage], pol_tok);
         } else {
           // A = tokens (x, or t for the rank-r blocks), B = rows (W0, or U)
-          load(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage]);
+          load(st, low ? &sg.tm_t : &p.tm_x, kb * kBK, tc.tok0, &full[stage], pol_tok);
           load_rows(st, low ? &sg.tm_u : &sg.tm_w, kb, tc.row0, sg.n_mma, &full[stage]);
         }
         filled |= 1u << stage;
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
               uint8_t* st = ring + static_cast<size_t>(kb) * p.stage_bytes;
               if (leader) mbar_arrive_expect_tx(&full[kb], tx_bytes);
               if constexpr (kSwap) {
-                load(st, &sg.tm_w, (cur.kb_lo + kb) * kBK, tc.row0, &full[kb]);
+                load(st, &sg.tm_w, (cur.kb_lo + kb) * kBK, tc.row0, &full[kb], pol_row);
               } else {
                 load_rows(st, &sg.tm_w, cur.kb_lo + kb, tc.row0, sg.n_mma, &full[kb]);
               }
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
             pdl_wait_prior_grid();
             for (int j = 0; j < pre; ++j) {
               uint8_t* st = ring + static_cast<size_t>(j) * p.stage_bytes;
-              load(kSwap ? st + kStageA : st, &p.tm_x, (cur.kb_lo + j) * kBK, tc.tok0, &full[j]);
+              load(kSwap ? st + kStageA : st, &p.tm_x, (cur.kb_lo + j) * kBK, tc.tok0, &full[j], pol_tok);
             }
             stage = pre;
             if (stage == p.stages) {
