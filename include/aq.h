@@ -274,6 +274,17 @@ aq_status aq_device_status(void* stream);
  * exits; aq_device_status() then reports it. No fault, trap or hang is involved. */
 aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
 
+/* Test hook for the bounded waits of a real kernel: runs aq_linear on the prefill GEMM with
+ * its wait for the t tiles of the same launch set to a count no tile reaches and a limit of
+ * timeout_us microseconds (1..1000000). Needs r > 0, a call that takes the t tiles inside the
+ * GEMM launch and unpaired CTAs (one token tile, no split of K), else AQ_ERR_UNSUPPORTED. The
+ * waits expire; each CTA records AQ_ERR_TIMEOUT, lets its issued copies land and its issued
+ * MMAs finish (bounded), frees its tensor memory, counts itself out (the last CTA returns the
+ * workspace's sync region to zero) and exits. y is undefined afterwards; aq_device_status()
+ * reports the timeout and the context stays usable. No fault, trap or hang is involved. */
+aq_status aq_selftest_prefill_timeout(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y, int64_t ldy,
+                                      void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream);
+
 /* Path selection for aq_linear / aq_linear_qkv / aq_linear_multi. Three kernels serve the
  * three token buckets of one call:
  *   AQ_PATH_DECODE   the mma.sync streaming kernel, M <= aq_decode_max_m() = 32: W0 split by

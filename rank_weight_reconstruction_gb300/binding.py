@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = [
     "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
     "aq_band_mean", "aq_ls_residual", "aq_randomized_svd_workspace_bytes", "aq_randomized_svd",
     "aq_mlp_workspace_bytes", "aq_mlp", "aq_precompute_nvfp4_workspace_bytes", "aq_precompute_nvfp4",
+    "aq_selftest_prefill_timeout",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -119,6 +120,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_device_status.restype = ctypes.c_int
     lib.aq_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
     lib.aq_selftest_bounded_wait.restype = ctypes.c_int
+    lib.aq_selftest_prefill_timeout.argtypes = [th_p, vp, i64, i64, vp, i64, vp, sz, ctypes.c_uint32, vp]
+    lib.aq_selftest_prefill_timeout.restype = ctypes.c_int
     lib.aq_set_path.argtypes = [ctypes.c_int]
     lib.aq_set_path.restype = ctypes.c_int
     for name in ("aq_decode_max_m", "aq_last_path", "aq_last_launch_count", "aq_abi_version"):
@@ -359,6 +362,20 @@ def aq_device_status(stream=None) -> int:
 
 def aq_selftest_bounded_wait(timeout_us: int, stream=None) -> None:
     _check(load().aq_selftest_bounded_wait(int(timeout_us), _stream(stream)))
+
+
+def aq_selftest_prefill_timeout(theta: Theta, x, timeout_us: int, y=None, workspace=None, stream=None):
+    """aq_linear on the prefill GEMM with its t-flag wait made unreachable (test hook)."""
+    M = int(x.shape[0])
+    if y is None:
+        y = _padded_empty(M, theta.out, x.device)
+    if workspace is None:
+        workspace = new_workspace(aq_linear_workspace_bytes(theta, M), x.device)
+    th = theta.c()
+    _check(load().aq_selftest_prefill_timeout(ctypes.byref(th), _ptr(x), M, _ld(x), _ptr(y), _ld(y), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), int(timeout_us),
+                                              _stream(stream)))
+    return y
 
 
 def aq_set_path(path: int) -> None:

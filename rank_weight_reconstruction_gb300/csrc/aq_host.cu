@@ -21,6 +21,9 @@ thread_local std::string t_err;
 thread_local int32_t t_last_path = 0;
 thread_local int32_t t_launches = 0;
 std::atomic<int> g_path{AQ_PATH_AUTO};
+// aq_selftest_prefill_timeout: on this thread, the next prefill GEMM waits for a t-flag count
+// no tile reaches, with this limit (0: the normal plan)
+thread_local uint64_t t_test_unreachable_t_ns = 0;
 
 constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
 // The swapped-operand GEMM (output rows as accumulator lanes) is taken automatically where it was
@@ -584,7 +587,7 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
     }
   }
 
-  const int path_cfg = g_path.load();
+  const int path_cfg = t_test_unreachable_t_ns ? static_cast<int>(AQ_PATH_PREFILL) : g_path.load();
   // From 16 tokens on, a call with a large W0 runs faster on the tcgen05 GEMM than on the
   // mma.sync decode kernel, whose issue rate then bounds it (measured on the 31B-class
   // 21504 x 5376 projection: 50.9 vs 62.3 us at M = 16, 50.7 vs 84.8 us at M = 32); at
@@ -1038,6 +1041,12 @@ aq_status linear_impl(const aq_theta* const* th, int n, const void* x, int64_t M
   gp.tmem_cols = tmem_cols_for(2 * gp.n_mma);   // two accumulator buffers
   gp.status = dev->status;
   gp.timeout_ns = kTimeoutNs;
+  if (t_test_unreachable_t_ns) {
+    if (!gp.t_flags || gp.cluster != 1)
+      return fail(AQ_ERR_UNSUPPORTED, "aq_selftest_prefill_timeout: the call must wait on t flags in unpaired CTAs");
+    gp.t_need = 1 << 30;
+    gp.timeout_ns = t_test_unreachable_t_ns;
+  }
   const int grid = gp.cluster > 1 ? 2 * std::min(tiles, dev->gemm_pairs) : std::min(gp.total_tiles, dev->sms);
   if ((st = launch_or_fail(launch_gemm(gp, grid, smem, cs, true), "launch reconstruction GEMM")) != AQ_OK) return st;
   if (split > 1) {
@@ -1388,6 +1397,17 @@ aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
   return launch_or_fail(launch_bounded_wait_selftest(dev->status, uint64_t(timeout_us) * 1000u,
                                                      static_cast<cudaStream_t>(stream)),
                         "launch bounded-wait self test");
+}
+
+aq_status aq_selftest_prefill_timeout(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y, int64_t ldy,
+                                      void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000)
+    return fail(AQ_ERR_INVALID_ARG, "aq_selftest_prefill_timeout: timeout_us=%u outside [1, 1000000]", timeout_us);
+  if (!th || th->r <= 0) return fail(AQ_ERR_INVALID_ARG, "aq_selftest_prefill_timeout: needs a bundle with r > 0");
+  t_test_unreachable_t_ns = static_cast<uint64_t>(timeout_us) * 1000u;
+  const aq_status st = aq_linear(th, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
+  t_test_unreachable_t_ns = 0;
+  return st;
 }
 
 aq_status aq_set_path(aq_path path) {

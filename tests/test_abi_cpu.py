@@ -194,3 +194,10 @@ def test_path_setting(lib):
 def test_selftest_argument_check(lib):
     assert lib.aq_selftest_bounded_wait(0, None) == binding.AQ_ERR_INVALID_ARG
     assert lib.aq_selftest_bounded_wait(2_000_000, None) == binding.AQ_ERR_INVALID_ARG
+    th = binding.c_theta(W0=0x1000, s=0x2000, U=None, V=None, ld_w0=64, ld_u=0, ld_v=0, out=64, in_=64, r=0)
+    for us in (0, 2_000_000):
+        assert lib.aq_selftest_prefill_timeout(ctypes.byref(th), 0x3000, 4, 64, 0x4000, 64, 0x5000, 1 << 20, us,
+                                               None) == binding.AQ_ERR_INVALID_ARG
+    # r = 0: no t tiles to wait for
+    assert lib.aq_selftest_prefill_timeout(ctypes.byref(th), 0x3000, 4, 64, 0x4000, 64, 0x5000, 1 << 20, 1000,
+                                           None) == binding.AQ_ERR_INVALID_ARG

@@ -69,6 +69,33 @@ def test_bounded_wait_reports_timeout():
     assert aq.aq_device_status() == aq.AQ_OK
 
 
+def test_prefill_gemm_abort_path():
+    """A real kernel's bounded wait running out: the prefill GEMM (unpaired, one token tile,
+    r = 32 so that K is not split) waits for a t-flag count no tile reaches, with a 1 ms limit.
+    The call reports AQ_ERR_TIMEOUT through aq_device_status, the kernel frees its tensor memory
+    and returns the workspace's sync region to zero, and the same workspace then serves a normal
+    call whose output matches the oracle."""
+    from rank_weight_reconstruction_gb300 import binding
+    assert aq.aq_device_status() == aq.AQ_OK
+    th = synth.make_theta(("abort",), 6912, 1152, 32)
+    xb = synth.make_x(("abort",), 64, 1152)
+    T = dev_theta(th)
+    x = dev(xb)[:, :1152]
+    ws = aq.new_workspace(aq.aq_linear_workspace_bytes(T, 64), x.device)
+    binding.aq_selftest_prefill_timeout(T, x, 1000, workspace=ws)
+    assert aq.aq_device_status() == aq.AQ_ERR_TIMEOUT
+    sync = ws[: aq.binding.AQ_WORKSPACE_SYNC_BYTES].cpu()
+    assert not sync.any(), "the aborted launch left the sync region dirty"
+    aq.aq_set_path(aq.AQ_PATH_PREFILL)
+    try:
+        y = aq.aq_linear(T, x, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        aq.aq_set_path(aq.AQ_PATH_AUTO)
+    assert aq.aq_device_status() == aq.AQ_OK
+    assert_close(host_f64(y), oracle.linear(*th.f64(), x_f64(xb, 1152)))
+
+
 # ----------------------------------------------------------------------------------
 # integer-valued cases: bit-exact on every path
 # ----------------------------------------------------------------------------------
