@@ -103,7 +103,9 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int kbox, int row, in
 
 }  // namespace
 
-template <int NT>
+// kStaged: x and V ride in every stage behind its W0 box (Dec2Params::staged), a separate
+// instantiation so that the resident layout keeps its own code
+template <int NT, bool kStaged>
 __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid_constant__ Dec2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1k2(smem_raw);
@@ -173,19 +175,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
     // ---------------- TMA producer ----------------
     if (lane == 0 && rows_here > 0 && kb_n > 0) {
       const uint32_t wbytes = static_cast<uint32_t>(p.kbox) * static_cast<uint32_t>(Rc) * 128u;
-      auto issue = [&](int q, int slot) {
-        mbar_arrive_expect_tx(&full[slot], wbytes);
-        tma_load_3d(ring + static_cast<size_t>(slot) * p.stage_bytes, &sg.tm_w, 0, kb_lo + q * p.kbox, row0,
-                    &full[slot]);
+      // staged: the stage's x box and V rows count on the same barrier (x after the wait)
+      const uint32_t xsb = kStaged ? static_cast<uint32_t>(p.kbox) * static_cast<uint32_t>(M) * 128u : 0u;
+      const uint32_t vkb = static_cast<uint32_t>(64 * p.vrow * 2);   // V bytes of one k block
+      const uint32_t vsb = (kStaged && sg.r > 0) ? static_cast<uint32_t>(p.kbox) * vkb : 0u;
+      auto issue = [&](int q, int slot, bool with_x) {
+        uint8_t* st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], wbytes + xsb + vsb);
+        tma_load_3d(st, &sg.tm_w, 0, kb_lo + q * p.kbox, row0, &full[slot]);
+        if (vsb)
+          for (int b = 0; b < p.kbox; ++b)
+            tma_load_2d_plain(st + p.sv_off + b * vkb, &sg.tm_v, 0, (kb_lo + q * p.kbox + b) * 64, &full[slot]);
+        if (xsb && with_x) tma_load_3d(st + p.sx_off, &p.tm_x, 0, kb_lo + q * p.kbox, 0, &full[slot]);
       };
       const int pre = nstage < p.stages ? nstage : p.stages;
       uint32_t filled = 0, fill_par = 0;
       // weights first: W0 stages and this CTA's V slice, before the dependency wait
       for (int q = 0; q < pre; ++q) {
-        issue(q, q);
+        issue(q, q, false);
         filled |= 1u << q;
       }
-      if (sg.r > 0) {
+      if (sg.r > 0 && !kStaged) {
         const uint32_t vb = static_cast<uint32_t>(p.vbox) * static_cast<uint32_t>(p.vrow) * 2u;
         const int nvb = (kb_n * 64 + p.vbox - 1) / p.vbox;
         mbar_arrive_expect_tx(vbar, static_cast<uint32_t>(nvb) * vb);
@@ -205,9 +215,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
           prefetch_l2_bulk(p.x2 + static_cast<int64_t>(m) * p.ldx + kk, static_cast<uint32_t>(len) * 2u);
       }
       pdl_wait_prior_grid();
-      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(p.xkb) * static_cast<uint32_t>(M) * 128u * (p.act >= 0 ? 2u : 1u));
-      tma_load_3d(xs, &p.tm_x, 0, kb_lo, 0, xbar);
-      if (p.act >= 0) tma_load_3d(xs2, &p.tm_x2, 0, kb_lo, 0, xbar);
+      if (kStaged) {
+        // x of the stages already issued, onto their barriers
+        for (int q = 0; q < pre; ++q)
+          tma_load_3d(ring + static_cast<size_t>(q) * p.stage_bytes + p.sx_off, &p.tm_x, 0, kb_lo + q * p.kbox, 0,
+                      &full[q]);
+      } else {
+        mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(p.xkb) * static_cast<uint32_t>(M) * 128u * (p.act >= 0 ? 2u : 1u));
+        tma_load_3d(xs, &p.tm_x, 0, kb_lo, 0, xbar);
+        if (p.act >= 0) tma_load_3d(xs2, &p.tm_x2, 0, kb_lo, 0, xbar);
+      }
       int slot = pre == p.stages ? 0 : pre;
       uint32_t phase = pre == p.stages ? 1u : 0u;
       for (int q = pre; q < nstage; ++q) {
@@ -215,7 +232,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
           ok = false;
           break;
         }
-        issue(q, slot);
+        issue(q, slot, true);
         filled |= 1u << slot;
         fill_par = (fill_par & ~(1u << slot)) | (phase << slot);
         if (++slot == p.stages) {
@@ -232,8 +249,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
               if (global_timer_ns() - t0 > 20000000ull) break;
           }
       }
-      // the x and V copies land before the CTA can exit, whatever happened
-      {
+      // the resident x and V copies land before the CTA can exit, whatever happened
+      if (!kStaged) {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(xbar, 0u))
           if (global_timer_ns() - t0 > 20000000ull) break;
@@ -283,7 +300,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[a][nt][e] = tacc[a][nt][e] = 0.0f;
 
-    if (rows_here > 0 && kb_n > 0) {
+    if (rows_here > 0 && kb_n > 0 && !kStaged) {
       ok = __all_sync(0xffffffffu, mbar_wait(xbar, 0u, ctl)) != 0;
       if (ok && sg.r > 0) ok = __all_sync(0xffffffffu, mbar_wait(vbar, 0u, ctl)) != 0;
     }
@@ -323,6 +340,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       const int kb0 = sq * p.kbox;                     // first k block of the stage, within the slice
       const int nb = min(p.kbox, kb_n - kb0);
       const uint32_t wbase = smem_u32(ring + static_cast<size_t>(slot) * p.stage_bytes);
+      // x and V of this stage: in the stage (staged) or in the resident slices
+      const uint32_t sxbase = kStaged ? wbase + p.sx_off : xbase;
+      const int sxkb = kStaged ? p.kbox : p.xkb;
+      const uint32_t svbase = kStaged ? wbase + p.sv_off : vbase;
+      const int sk0 = kStaged ? kb0 : 0;              // first k block held at svbase / sxbase
       if (active) {
         for (int b = (nslab >= 8) ? 0 : (kgi - kb0 % kg + kg) % kg; b < nb; b += (nslab >= 8 ? 1 : kg)) {
           const int bx = kb0 + b;                      // k block within the slice
@@ -334,10 +356,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
             // B: x^T fragments of this 16-wide step (token rows past M repeat the last token)
             uint32_t bfr[NT][2];
             if constexpr (NT == 1) {
-              ldsm2(sw_addr(xbase, p.xkb, min(lane & 7, M - 1), bx, 2 * j + ((lane >> 3) & 1)), bfr[0][0], bfr[0][1]);
+              ldsm2(sw_addr(sxbase, sxkb, min(lane & 7, M - 1), bx - sk0, 2 * j + ((lane >> 3) & 1)), bfr[0][0],
+                    bfr[0][1]);
             } else {
               uint32_t b0, b1, b2, b3;
-              ldsm4(sw_addr(xbase, p.xkb, min((lane & 7) + (lane >> 4) * 8, M - 1), bx, 2 * j + ((lane >> 3) & 1)),
+              ldsm4(sw_addr(sxbase, sxkb, min((lane & 7) + (lane >> 4) * 8, M - 1), bx - sk0, 2 * j + ((lane >> 3) & 1)),
                     b0, b1, b2, b3);
               bfr[0][0] = b0;
               bfr[0][1] = b1;
@@ -355,12 +378,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
             }
             if (t_own) {
               // A: V^T [16 ranks x 16 k] from the V slice [k][vrow] (ldmatrix.trans)
-              const int kl = bx * 64 + 16 * j + (lane & 7) + ((lane >> 4) & 1) * 8;
+              const int kl = (bx - sk0) * 64 + 16 * j + (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt) {
                 if (mt < mtn) {
                   uint32_t a0, a1, a2, a3;
-                  ldsm4_trans(vbase + (kl * p.vrow + 16 * mt + ((lane >> 3) & 1) * 8) * 2, a0, a1, a2, a3);
+                  ldsm4_trans(svbase + (kl * p.vrow + 16 * mt + ((lane >> 3) & 1) * 8) * 2, a0, a1, a2, a3);
 #pragma unroll
                   for (int nt = 0; nt < NT; ++nt) mma16816(tacc[mt][nt], a0, a1, a2, a3, bfr[nt][0], bfr[nt][1]);
                 }
@@ -523,8 +546,10 @@ cudaError_t launch_gated_act(uint16_t* g, const uint16_t* u, int64_t ld, int64_t
 
 cudaError_t launch_decode2(const Dec2Params& p, int grid, size_t smem, cudaStream_t st, bool pdl) {
   void* args[] = {const_cast<Dec2Params*>(&p)};
-  const void* fn = p.M > 8 ? reinterpret_cast<const void*>(&aq_decode2_kernel<2>)
-                           : reinterpret_cast<const void*>(&aq_decode2_kernel<1>);
+  const void* fn = p.staged ? (p.M > 8 ? reinterpret_cast<const void*>(&aq_decode2_kernel<2, true>)
+                                       : reinterpret_cast<const void*>(&aq_decode2_kernel<1, true>))
+                            : (p.M > 8 ? reinterpret_cast<const void*>(&aq_decode2_kernel<2, false>)
+                                       : reinterpret_cast<const void*>(&aq_decode2_kernel<1, false>));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);
@@ -550,8 +575,10 @@ cudaError_t launch_decode2(const Dec2Params& p, int grid, size_t smem, cudaStrea
 cudaError_t configure_decode2(size_t max_smem) {
   cudaError_t e;
   const int s = static_cast<int>(max_smem);
-  if ((e = cudaFuncSetAttribute(aq_decode2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
-  return cudaFuncSetAttribute(aq_decode2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s);
+  if ((e = cudaFuncSetAttribute(aq_decode2_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_decode2_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  if ((e = cudaFuncSetAttribute(aq_decode2_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s))) return e;
+  return cudaFuncSetAttribute(aq_decode2_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s);
 }
 
 }  // namespace aq

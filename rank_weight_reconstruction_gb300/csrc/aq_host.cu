@@ -26,6 +26,7 @@ std::atomic<int> g_path{AQ_PATH_AUTO};
 thread_local uint64_t t_test_unreachable_t_ns = 0;
 
 constexpr int kDecodeMaxM = kDecMaxTok;               // mma.sync decode kernel up to this M
+constexpr int kDec2Staged = 1;   // cluster decode: x and V in the W0 stages (no gated input)
 // The swapped-operand GEMM (output rows as accumulator lanes) is taken automatically where it was
 // measured faster than the token-lane GEMM (bench.py --sweep, gate-like 6912 x 1152 and down-like
 // 1152 x 6912, r = 0..256): calls of at least this many tokens whose families have few 128-row
@@ -461,34 +462,74 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
     // (x box odd where the tensor has the block: its eight token rows of an ldmatrix then land
     // in distinct banks)
     dp.xkb = (dp.kb_per | 1) <= nkb ? (dp.kb_per | 1) : dp.kb_per;
-    dp.x_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.xkb) * M * 128, 1024));
-    dp.x2_bytes = act >= 0 ? dp.x_bytes : 0u;   // a gated input stages both slices
     dp.vrow = max_r16;
     const int64_t kslice = static_cast<int64_t>(dp.kb_per) * kBK;
     const int64_t nvb = ceil_div(kslice, 256);
-    dp.vbox = static_cast<int32_t>(round_up(ceil_div(kslice, nvb), 16));
-    dp.v_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(nvb * dp.vbox * dp.vrow * 2, 1024)) : 0u;
     const int64_t rf_max = ceil_div(rc_max, C);
     dp.u_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(rf_max * max_r16 * 2, 1024)) : 0u;
     dp.s_bytes = static_cast<uint32_t>(round_up((rf_max + 15) / 8 * 16, 1024));
     dp.tf_bytes = max_r16 > 0 ? static_cast<uint32_t>(round_up(static_cast<int64_t>(max_r16) * M * 4, 1024)) : 0u;
     dp.rx_bytes = static_cast<uint32_t>(round_up(static_cast<int64_t>(C) * (round_up(rf_max, 4) + max_r16) * M * 4, 1024));
-    const size_t fixed = kHeaderBytes + kSmemSlack + dp.x_bytes + dp.x2_bytes + dp.v_bytes + dp.u_bytes + dp.s_bytes +
-                         dp.tf_bytes + dp.rx_bytes;
-    if (fixed >= half) continue;
-    const size_t ring = half - fixed;
-    dp.kbox = 0;
-    int kb_start = std::min(9, static_cast<int>(dp.kb_per));
-    if (kb_start % 2 == 0) --kb_start;   // odd, and never past the slice
-    for (int kb = kb_start; kb >= 1; kb -= 2) {
-      const size_t sb = static_cast<size_t>(round_up(static_cast<int64_t>(kb) * rc_max * 128, 1024));
-      if (ring / sb >= 2 || kb == 1) {
-        dp.kbox = kb;
-        dp.stage_bytes = static_cast<uint32_t>(sb);
-        dp.stages = static_cast<int32_t>(std::min<size_t>(kMaxStages, ring / sb));
-        break;
+    // The W0 ring of one layout: x and V resident (staged = 0), or riding in every stage behind
+    // its W0 box (staged = 1: x after the dependency wait, no resident slices). k blocks per
+    // stage: the largest odd count (conflict-free ldmatrix rows, at most nine) that leaves two
+    // stages (measured: many one-block stages are slower than fewer larger ones, even with
+    // more of W0 in flight).
+    struct Ring {
+      bool ok = false;
+      int kbox = 0, stages = 0;
+      size_t sb = 0, wb = 0, xb = 0, fixed = 0;
+    };
+    auto ring_for = [&](bool staged) {
+      Ring g;
+      const size_t xres = staged ? 0 : static_cast<size_t>(round_up(static_cast<int64_t>(dp.xkb) * M * 128, 1024));
+      const size_t x2res = act >= 0 ? xres : 0;
+      const size_t vres = (max_r16 > 0 && !staged)
+                              ? static_cast<size_t>(round_up(nvb * round_up(ceil_div(kslice, nvb), 16) * dp.vrow * 2, 1024))
+                              : 0;
+      g.fixed = kHeaderBytes + kSmemSlack + xres + x2res + vres + dp.u_bytes + dp.s_bytes + dp.tf_bytes + dp.rx_bytes;
+      if (g.fixed >= half) return g;
+      const size_t ring = half - g.fixed;
+      int kb_start = std::min(9, static_cast<int>(dp.kb_per));
+      if (kb_start % 2 == 0) --kb_start;   // odd, and never past the slice
+      for (int kb = kb_start; kb >= 1; kb -= 2) {
+        const size_t wb = static_cast<size_t>(round_up(static_cast<int64_t>(kb) * rc_max * 128, 1024));
+        const size_t xb = staged ? static_cast<size_t>(round_up(static_cast<int64_t>(kb) * M * 128, 1024)) : 0;
+        const size_t vb = (staged && max_r16 > 0) ? static_cast<size_t>(round_up(static_cast<int64_t>(kb) * kBK * dp.vrow * 2, 1024)) : 0;
+        const size_t sb = wb + xb + vb;
+        if (ring / sb >= 2 || kb == 1) {
+          g.kbox = kb;
+          g.stages = static_cast<int>(std::min<size_t>(kMaxStages, ring / sb));
+          g.sb = sb;
+          g.wb = wb;
+          g.xb = xb;
+          g.ok = g.stages >= 2;
+          break;
+        }
       }
-    }
+      return g;
+    };
+    // Resident x and V unless the ring then holds less of the slice than riding them in the
+    // stages would (a gated input keeps both x slices resident: the activation is formed over
+    // them once, before the loop). Measured: riding costs the small calls whose slice fits the
+    // ring either way (q/k/v, o) about 0.4 us, and gains where the slice does not fit.
+    const Ring rr = ring_for(false);
+    const Ring rs = (act < 0 && kDec2Staged) ? ring_for(true) : Ring{};
+    const auto held = [&](const Ring& g) { return g.ok ? std::min(g.kbox * g.stages, static_cast<int>(dp.kb_per)) : 0; };
+    const bool use_staged = rs.ok && (!rr.ok || (held(rr) < dp.kb_per && held(rs) > held(rr)));
+    const Ring& g = use_staged ? rs : rr;
+    if (!g.ok) continue;
+    dp.staged = use_staged ? 1 : 0;
+    dp.x_bytes = dp.staged ? 0u : static_cast<uint32_t>(round_up(static_cast<int64_t>(dp.xkb) * M * 128, 1024));
+    dp.x2_bytes = act >= 0 ? dp.x_bytes : 0u;   // a gated input stages both slices
+    dp.vbox = dp.staged ? kBK : static_cast<int32_t>(round_up(ceil_div(kslice, nvb), 16));
+    dp.v_bytes = (max_r16 > 0 && !dp.staged) ? static_cast<uint32_t>(round_up(nvb * dp.vbox * dp.vrow * 2, 1024)) : 0u;
+    const size_t fixed = g.fixed;
+    dp.kbox = g.kbox;
+    dp.stages = g.stages;
+    dp.stage_bytes = static_cast<uint32_t>(g.sb);
+    dp.sx_off = static_cast<uint32_t>(g.wb);
+    dp.sv_off = static_cast<uint32_t>(g.wb + g.xb);
     if (dp.kbox < 1 || dp.kbox > dp.kb_per || dp.stages < 2) continue;
     // the partial sums of W0 x and t reuse the ring once the loop is done
     const size_t exch = (static_cast<size_t>(kg_max) * rc_max * M + static_cast<size_t>(8) * max_r16 * M) * 4;
@@ -500,7 +541,8 @@ bool plan_decode2(const aq_theta* const* th, int n, const void* x, int64_t M, in
   if (!fits) return false;
   const int C = dp.C;
   // tensor maps
-  if ((*st = tmap_3d(&dp.tm_x, x, K, M, ldx, dp.xkb, static_cast<int>(M), "x")) != AQ_OK) return true;
+  if ((*st = tmap_3d(&dp.tm_x, x, K, M, ldx, dp.staged ? dp.kbox : dp.xkb, static_cast<int>(M), "x")) != AQ_OK)
+    return true;
   dp.act = act;
   if (act >= 0) {
     if ((*st = tmap_3d(&dp.tm_x2, x2, K, M, ldx, dp.xkb, static_cast<int>(M), "x (gated)")) != AQ_OK) return true;

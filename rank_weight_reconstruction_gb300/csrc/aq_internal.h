@@ -243,6 +243,10 @@ struct Dec2Params {
   uint32_t x2_bytes;     // the second x slice of a gated input (0 without one)
   int32_t act;           // gated input: -1 none; else the input is act(x) * x2 (kAct* below)
   const uint16_t* x2;    // for L2 prefetch hints
+  int32_t staged;        // 1: x and V ride in every stage behind its W0 box (x box {64, kbox, M},
+                         //    V rows {vrow, 64} per k block); no resident x or V slice
+  uint32_t sx_off;       // staged: byte offset of a stage's x box
+  uint32_t sv_off;       // staged: byte offset of a stage's V rows
   int32_t* status;
   uint64_t timeout_ns;
 };
