@@ -66,7 +66,8 @@ typedef enum aq_status {
   AQ_ERR_OVERLAP = 6,      /* an output buffer overlaps an input buffer */
   AQ_ERR_CUDA = 7,         /* a CUDA runtime or driver call failed (message in aq_last_error) */
   AQ_ERR_TIMEOUT = 8,      /* device side: a bounded wait inside a kernel expired */
-  AQ_ERR_NUMERIC = 9       /* aq_randomized_svd: a factorisation met a non-positive pivot */
+  AQ_ERR_NUMERIC = 9,      /* aq_randomized_svd: a factorisation met a non-positive pivot */
+  AQ_ERR_BOUNDS = 10       /* checked build only: a kernel skipped a store outside its output */
 } aq_status;
 
 /* One projection's theta bundle. All pointers are device pointers to bf16 data.
@@ -252,7 +253,8 @@ aq_status aq_precompute_nvfp4(const aq_theta* th, void* q, int64_t ldq, void* sf
                               void* stream);
 
 /* Synchronises `stream`, then returns the device status word of the current device
- * (AQ_OK, or AQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last clear)
+ * (AQ_OK, AQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last clear, or in the
+ * checked build AQ_ERR_BOUNDS if a kernel skipped an out-of-range store)
  * and clears it. A kernel whose wait expires stops its work (its outputs are then
  * undefined), releases its tensor memory and exits; the CUDA context stays usable.
  *
@@ -273,6 +275,17 @@ aq_status aq_device_status(void* stream);
  * wait expires, the block records AQ_ERR_TIMEOUT in the device status word and
  * exits; aq_device_status() then reports it. No fault, trap or hang is involved. */
 aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream);
+
+/* Checked build (compiled with AQ_DEBUG_CHECKS; libaq_gb300_debug.so): every plain output store
+ * of the hot-path kernels (decode y, the GEMM's column and partial-sum stores, NVFP4 codes and
+ * scales) checks its index against the extent of the output it addresses; a violation skips
+ * the store and sets the device status word to AQ_ERR_BOUNDS. TMA stores are bounded by their
+ * tensor maps in every build. aq_checked_build() is 1 in that build, 0 otherwise.
+ * aq_selftest_bounds_check launches one thread that checks two indices outside their extents
+ * (nothing is accessed): afterwards aq_device_status() reports AQ_ERR_BOUNDS in the checked
+ * build and AQ_OK in the normal one. */
+int32_t aq_checked_build(void);
+aq_status aq_selftest_bounds_check(void* stream);
 
 /* Test hook for the bounded waits of a real kernel: runs aq_linear on the prefill GEMM with
  * its wait for the t tiles of the same launch set to a count no tile reaches and a limit of

@@ -23,6 +23,7 @@ AQ_ERR_OVERLAP = 6
 AQ_ERR_CUDA = 7
 AQ_ERR_TIMEOUT = 8
 AQ_ERR_NUMERIC = 9
+AQ_ERR_BOUNDS = 10
 AQ_MAX_RANK = 256
 
 AQ_PATH_AUTO = 0
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = [
     "aq_abi_version", "aq_linear_noalloc", "aq_linear_multi", "aq_noalloc_scratch_read",
     "aq_band_mean", "aq_ls_residual", "aq_randomized_svd_workspace_bytes", "aq_randomized_svd",
     "aq_mlp_workspace_bytes", "aq_mlp", "aq_precompute_nvfp4_workspace_bytes", "aq_precompute_nvfp4",
-    "aq_selftest_prefill_timeout",
+    "aq_selftest_prefill_timeout", "aq_checked_build", "aq_selftest_bounds_check",
 ]
 AQ_MAX_FAMILIES = 3
 AQ_NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024
@@ -122,6 +123,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.aq_selftest_bounded_wait.restype = ctypes.c_int
     lib.aq_selftest_prefill_timeout.argtypes = [th_p, vp, i64, i64, vp, i64, vp, sz, ctypes.c_uint32, vp]
     lib.aq_selftest_prefill_timeout.restype = ctypes.c_int
+    lib.aq_checked_build.argtypes = []
+    lib.aq_checked_build.restype = ctypes.c_int32
+    lib.aq_selftest_bounds_check.argtypes = [vp]
+    lib.aq_selftest_bounds_check.restype = ctypes.c_int
     lib.aq_set_path.argtypes = [ctypes.c_int]
     lib.aq_set_path.restype = ctypes.c_int
     for name in ("aq_decode_max_m", "aq_last_path", "aq_last_launch_count", "aq_abi_version"):

@@ -16,6 +16,10 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libaq_gb300.so")
+# Checked build (tests only): every plain output store checks its index against the output's
+# extent and records a violation as AQ_ERR_BOUNDS in the device status word.
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libaq_gb300_debug.so")
 SOURCES = ["aq_kernels.cu", "aq_decode.cu", "aq_decode2.cu", "aq_decompose.cu", "aq_host.cu", "aq_noalloc.cu"]
 HEADERS = ["aq_ptx.cuh", "aq_internal.h"]
 
@@ -38,23 +42,27 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of the shared library."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile (if needed) and return the path of the shared library (the checked build with
+    ``debug=True``)."""
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    bdir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(lib):
+        return lib
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *(["-DAQ_DEBUG_CHECKS=1"] if debug else []), "-c",
+               os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -66,14 +74,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose and out:
             print(out.decode(errors="replace"), file=sys.stderr)
         objs.append(obj)
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout.decode(errors='replace')}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

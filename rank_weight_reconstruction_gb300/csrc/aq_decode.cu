@@ -840,8 +840,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const int m = 8 * nt + 2 * qq + e;
-                  if (m < p.M)
-                    sg.y[static_cast<int64_t>(m) * sg.ldy + o] = f32_to_bf16_rn(fmaf(sc, acc[nt][2 * h + e], lw[nt][2 * h + e]));
+                  const int64_t yi = static_cast<int64_t>(m) * sg.ldy + o;
+                  if (m < p.M && dbg_in_bounds(yi, dbg_extent(p.M, sg.ldy, sg.rows), p.status))
+                    sg.y[yi] = f32_to_bf16_rn(fmaf(sc, acc[nt][2 * h + e], lw[nt][2 * h + e]));
                 }
             }
           }

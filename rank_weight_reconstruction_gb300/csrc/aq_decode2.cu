@@ -508,7 +508,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
           }
         }
         const float sc = bf16_to_f32(sv[soff + rr]);
-        sg.y[static_cast<int64_t>(tok) * sg.ldy + row0 + f0 + rr] = f32_to_bf16_rn(fmaf(sc, z, lr));
+        const int64_t yi = static_cast<int64_t>(tok) * sg.ldy + row0 + f0 + rr;
+        if (dbg_in_bounds(yi, dbg_extent(M, sg.ldy, sg.rows), p.status) && dbg_in_bounds(row0 + f0 + rr, sg.rows, p.status))
+          sg.y[yi] = f32_to_bf16_rn(fmaf(sc, z, lr));
       }
     }
   }

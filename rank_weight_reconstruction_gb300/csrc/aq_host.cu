@@ -1426,6 +1426,7 @@ aq_status aq_device_status(void* stream) {
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   if (v == AQ_OK) return AQ_OK;
   if (v == AQ_ERR_TIMEOUT) return fail(AQ_ERR_TIMEOUT, "a bounded wait inside a kernel expired");
+  if (v == AQ_ERR_BOUNDS) return fail(AQ_ERR_BOUNDS, "checked build: a kernel skipped a store outside its output");
   return fail(AQ_ERR_CUDA, "unexpected device status %d", v);
 }
 
@@ -1439,6 +1440,23 @@ aq_status aq_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
   return launch_or_fail(launch_bounded_wait_selftest(dev->status, uint64_t(timeout_us) * 1000u,
                                                      static_cast<cudaStream_t>(stream)),
                         "launch bounded-wait self test");
+}
+
+aq_status aq_selftest_bounds_check(void* stream) {
+  DevInfo* dev = nullptr;
+  aq_status st = device_info(&dev);
+  if (st != AQ_OK) return st;
+  t_launches = 0;
+  return launch_or_fail(launch_bounds_selftest(dev->status, static_cast<cudaStream_t>(stream)),
+                        "launch bounds-check self test");
+}
+
+int32_t aq_checked_build(void) {
+#ifdef AQ_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 aq_status aq_selftest_prefill_timeout(const aq_theta* th, const void* x, int64_t M, int64_t ldx, void* y, int64_t ldy,
@@ -1476,6 +1494,7 @@ const char* aq_status_string(aq_status s) {
     case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
     case AQ_ERR_TIMEOUT: return "AQ_ERR_TIMEOUT";
     case AQ_ERR_NUMERIC: return "AQ_ERR_NUMERIC";
+    case AQ_ERR_BOUNDS: return "AQ_ERR_BOUNDS";
   }
   return "AQ_ERR_UNKNOWN";
 }

@@ -342,6 +342,7 @@ cudaError_t launch_transpose(const TransposeParams& p, int max_r, cudaStream_t s
 cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, cudaStream_t st,
                               bool pdl, int out_kind = kPreBf16);
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_bounds_selftest(int32_t* status, cudaStream_t st);
 cudaError_t configure_kernels(int device, size_t max_smem);
 // Records the message aq_last_error() returns on this thread and passes the status through.
 int set_last_error(int status, const char* message);

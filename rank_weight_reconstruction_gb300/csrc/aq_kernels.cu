@@ -483,7 +483,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int tok = tc.tok0 + c + j;
-              if (tok < p.M) pcol[static_cast<int64_t>(tok) * sg.ld_part] = v[j];
+              if (tok < p.M &&
+                  dbg_in_bounds(static_cast<int64_t>(itm.ks) * p.M * sg.ld_part + static_cast<int64_t>(tok) * sg.ld_part + row,
+                                static_cast<int64_t>(p.ksplit) * p.M * sg.ld_part, p.status))
+                pcol[static_cast<int64_t>(tok) * sg.ld_part] = v[j];
             }
           }
         } else {
@@ -496,7 +499,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int tok = tc.tok0 + c + j;
-              if (tok < p.M) ycol[static_cast<int64_t>(tok) * sg.ldy] = f32_to_bf16_rn(has_lr ? v[j] : v[j] * sc);
+              if (tok < p.M && dbg_in_bounds(static_cast<int64_t>(tok) * sg.ldy + row, dbg_extent(p.M, sg.ldy, sg.rows), p.status))
+                ycol[static_cast<int64_t>(tok) * sg.ldy] = f32_to_bf16_rn(has_lr ? v[j] : v[j] * sc);
             }
           }
         }
@@ -599,6 +603,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           tmem_ld_wait();
           const int o0 = tc.row0 + c;
           if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
+          if (!dbg_in_bounds((static_cast<int64_t>(itm.ks) * p.M + tok) * sg.ld_part + min(o0 + 15, sg.rows - 1),
+                             static_cast<int64_t>(p.ksplit) * p.M * sg.ld_part, p.status))
+            continue;
           if ((c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows)) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
@@ -622,6 +629,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         tmem_ld_wait();
         const int o0 = tc.row0 + c;
         if (!tok_ok || c >= p.row_tile || o0 >= sg.rows) continue;
+        if (!dbg_in_bounds(static_cast<int64_t>(tok) * sg.ldy + min(o0 + 15, sg.rows - 1), dbg_extent(p.M, sg.ldy, sg.rows),
+                           p.status))
+          continue;
         if (!has_lr) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
@@ -1185,7 +1195,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         // codes straight from registers: a warp writes 16 bytes of each of 32 rows, the other
         // warps of the quadrant the rest of those rows' 64 bytes (measured faster than staging
         // the tile for full-row stores behind a per-tile barrier)
-        if (o < p.out && col < p.in) {
+        if (o < p.out && col < p.in &&
+            dbg_in_bounds(static_cast<int64_t>(o) * p.ldq + min(col + 31, p.in - 1) / 2, dbg_extent(p.out, p.ldq, p.in / 2),
+                          p.status)) {
           uint8_t* dst = p.q + static_cast<int64_t>(o) * p.ldq + col / 2;
           if (col + 16 < p.in && p.q16) {
             *reinterpret_cast<uint4*>(dst) = make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y);
@@ -1198,7 +1210,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           if (o < p.out) {
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-              if (col + 16 * b < p.in)
+              if (col + 16 * b < p.in &&
+                  dbg_in_bounds(static_cast<int64_t>(o) * p.sf_cols + col / 16 + b, static_cast<int64_t>(p.out) * p.sf_cols,
+                                p.status))
                 p.sf[static_cast<int64_t>(o) * p.sf_cols + col / 16 + b] = static_cast<uint8_t>(b ? sf1 : sf0);
           }
         } else {
@@ -1206,7 +1220,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           // 16 (r mod 32) + 4 (r div 32) + k. Rows past out and columns past in/16 up to the
           // padded shape hold the zero scales of their zero weights.
           const int kb0 = col / 16;
-          if ((kb0 >> 2) < p.sf_ktiles)
+          const int64_t sf_tiles = static_cast<int64_t>(p.n_row_tiles) * p.sf_ktiles;
+          if ((kb0 >> 2) < p.sf_ktiles &&
+              dbg_in_bounds((static_cast<int64_t>(tr.row) * p.sf_ktiles + (kb0 >> 2)) * 512 + (lrow & 31) * 16 +
+                                (lrow >> 5) * 4 + (kb0 & 3) + 1,
+                            sf_tiles * 512, p.status))
             *reinterpret_cast<uint16_t*>(p.sf + (static_cast<int64_t>(tr.row) * p.sf_ktiles + (kb0 >> 2)) * 512 +
                                          (lrow & 31) * 16 + (lrow >> 5) * 4 + (kb0 & 3)) =
                 static_cast<uint16_t>(sf0 | (sf1 << 8));
@@ -1265,6 +1283,12 @@ __global__ void aq_selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
   const AbortCtl ctl{&abort_flag, status, timeout_ns};
   if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, ctl);
   __syncthreads();
+}
+
+// Checked-build self test: two indices outside their extents, checked but never accessed.
+__global__ void aq_selftest_bounds_kernel(int32_t* status) {
+  (void)dbg_in_bounds(-1, 8, status);
+  (void)dbg_in_bounds(8, 8, status);
 }
 
 // ------------------------------------------------------------------------------------
@@ -1343,6 +1367,11 @@ cudaError_t launch_precompute(const PrecomputeParams& p, int grid, size_t smem, 
                    : out_kind == kPreNvfp4 ? reinterpret_cast<const void*>(&aq_precompute_kernel<kPreNvfp4>)
                                            : reinterpret_cast<const void*>(&aq_precompute_kernel<kPreBf16>);
   return launch_ex(fn, dim3(grid), dim3(kPreThreads), smem, st, pdl, args);
+}
+
+cudaError_t launch_bounds_selftest(int32_t* status, cudaStream_t st) {
+  void* args[] = {&status};
+  return launch_ex(reinterpret_cast<const void*>(&aq_selftest_bounds_kernel), dim3(1), dim3(1), 0, st, false, args);
 }
 
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t st) {

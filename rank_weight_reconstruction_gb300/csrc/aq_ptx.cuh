@@ -12,6 +12,29 @@ namespace aq {
 // Device status codes (mirror aq_status in aq.h).
 constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = 8;
+constexpr int kStatusBounds = 10;
+
+// Checked build (compiled with -DAQ_DEBUG_CHECKS): a store whose element index falls outside
+// [0, n) of the output it addresses is skipped and recorded in the device status word as
+// AQ_ERR_BOUNDS (never a trap or a device assert, which would end the shared context). In the
+// normal build the check compiles away.
+__device__ __forceinline__ bool dbg_in_bounds(int64_t idx, int64_t n, int32_t* status) {
+#ifdef AQ_DEBUG_CHECKS
+  if (idx < 0 || idx >= n) {
+    atomicExch(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)idx;
+  (void)n;
+  (void)status;
+#endif
+  return true;
+}
+// Elements an output [rows_major, ld] spans when its last row holds `cols` elements.
+__device__ __forceinline__ int64_t dbg_extent(int64_t rows_major, int64_t ld, int64_t cols) {
+  return rows_major > 0 ? (rows_major - 1) * ld + cols : 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

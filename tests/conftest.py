@@ -10,6 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103) GPU and the built CUDA library")
+    # A child run of the suites on the checked build (tests/test_checked_build_gpu.py) names
+    # that library here; it is loaded before any test loads the normal one.
+    checked = os.environ.get("AQ_TEST_CHECKED_LIB")
+    if checked:
+        from rank_weight_reconstruction_gb300 import binding
+        binding.load(checked)
 
 
 def pytest_collection_modifyitems(config, items):
