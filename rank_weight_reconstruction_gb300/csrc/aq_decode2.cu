@@ -282,7 +282,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       }
     }
     cp_async_commit();
-    pdl_wait_prior_grid();   // y of this call may be read by the previous kernel until it ends
+    // No dependency wait of their own: everything the mma warps read after this point came
+    // through the producer's copies issued after its wait, and their y stores follow the
+    // cluster barrier, which every CTA with work reaches only after that wait.
 
     const int nslab = (Rc + 15) / 16;
     const int kg = nslab >= 8 ? 1 : 8 / nslab;          // warps sharing one slab (split over k blocks)
@@ -456,15 +458,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
         }
         st_dsmem_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
-      const int tq = tn / 4;
-      for (int idx = ct; idx < C * tq; idx += kDecConsumers) {
-        const int q = idx / tq, e = (idx - q * tq) * 4;
+      // t: this CTA's sum over its eight warps, formed once and pushed to every peer
+      for (int e = 4 * ct; e < tn; e += 4 * kDecConsumers) {
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int w = 0; w < 8; ++w)
 #pragma unroll
           for (int i = 0; i < 4; ++i) v[i] += tex[static_cast<size_t>(w) * tn + e + i];
-        st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
+        for (int q = 0; q < C; ++q)
+          st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
     }
   }

@@ -12,7 +12,8 @@ constexpr int kBK = 64;            // K elements per pipeline stage: one 128-byt
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma kind::f16
 constexpr int kMmaM = 128;         // accumulator lanes (tokens or output rows)
 constexpr int kMaxSeg = 3;         // projection families batched into one launch
-constexpr int kGemmThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kGemmEpiWarps = 8;   // prefill GEMM epilogue: two warps per TMEM lane quadrant
+constexpr int kGemmThreads = 64 + 32 * kGemmEpiWarps;  // warp 0 TMA producer, warp 1 MMA issuer, then the epilogue
 constexpr int kPreThreads = 576;   // precompute: warps 2-17 epilogue, four per TMEM lane quadrant
 constexpr int kStageA = kMmaM * 128;  // bytes of the A tile of one stage (128 rows x 128 B)
 constexpr int kHeaderBytes = 1024;    // barriers + TMEM address at the start of shared memory
@@ -326,10 +327,10 @@ constexpr size_t kGemmPairMinSmem = 120 * 1024;
 // k blocks of the next tile the MMA warp issues while the epilogue scales a tile by s (the
 // scale pass takes about as long as five 64-wide k blocks of a 256-wide tile)
 constexpr int kGemmHeadKb = 6;
-// Output staging of the prefill epilogue: per epilogue warp two buffers of 32 tokens x 64
+// Output staging of the prefill epilogue: per epilogue warp one buffer of 32 tokens x 64
 // columns of bf16 (128-byte swizzled rows), after the ring
 constexpr int kYStageBytes = 32 * 128;
-constexpr int kYStageTotal = 4 * 2 * kYStageBytes;
+constexpr int kYStageTotal = kGemmEpiWarps * kYStageBytes;
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st, bool pdl);
 cudaError_t launch_decode(const DecodeParams& p, int grid, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t configure_decode(size_t max_smem);

@@ -54,6 +54,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
 }
 
+// v[j] *= sc[j] for 16 columns: the scales as four 16-byte shared loads (sc 16-byte
+// aligned), two columns per multiply instruction, each product rounded as a plain multiply
+__device__ __forceinline__ void scale16(float (&v)[16], const float* sc) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 s4 = reinterpret_cast<const float4*>(sc)[q];
+    fmul2_rn(v[4 * q], v[4 * q + 1], v[4 * q], v[4 * q + 1], s4.x, s4.y);
+    fmul2_rn(v[4 * q + 2], v[4 * q + 3], v[4 * q + 2], v[4 * q + 3], s4.z, s4.w);
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // GEMM with fused reconstruction epilogue
 // ------------------------------------------------------------------------------------
@@ -150,11 +161,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_scaled[b], 4 * cl);   // one arrival per epilogue warp of each CTA
+      mbar_init(&acc_scaled[b], kGemmEpiWarps * cl);   // one arrival per epilogue warp of each CTA
       mbar_init(&acc_done[b], 1);
-      mbar_init(&acc_empty[b], 4 * cl);
+      mbar_init(&acc_empty[b], kGemmEpiWarps * cl);
     }
-    mbar_init(epi_bar, 4 * 32);
+    mbar_init(epi_bar, kGemmEpiWarps * 32);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -416,10 +427,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: warps 2..5, one TMEM lane quadrant each ----------------
+    // ------- epilogue: warps 2.., two per TMEM lane quadrant, each one half of the columns -------
     const int q = warp & 3;
     const int et = q * 32 + lane;                 // 0..127: TMEM lane = token of the tile
+    const int ect = threadIdx.x - 64;             // epilogue thread, 0..32 * kGemmEpiWarps - 1
+    const int hw = (warp - 2) >> 2;               // column half of this warp
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // this warp's accumulator columns of an n-column tile (n a multiple of 16): [c_lo, c_hi)
+    auto col_lo = [&](int n) { return hw ? (((n >> 4) + 1) >> 1) << 4 : 0; };
+    auto col_hi = [&](int n) { return hw ? n : (((n >> 4) + 1) >> 1) << 4; };
     // one arrival per warp on the MMA-issuing CTA's barrier
     auto mbar_arrive_lead = [&](uint64_t* bar) {
       if constexpr (kPair) {
@@ -455,7 +471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         tc_fence_after();
         if (has_lr) {
           // scale the W0 x accumulator by s in place; the MMA warp then adds U t
-          for (int c = 0; c < sg.n_mma; c += 16) {
+          for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
             float v[16];
             tmem_ld_16(acc + c, v);
             tmem_ld_wait();
@@ -475,7 +491,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           // split K: this slice's raw fp32 sums [slice][token][row], 32 consecutive rows per
           // warp-wide store
           float* pcol = sg.part + static_cast<int64_t>(itm.ks) * p.M * sg.ld_part + (row_ok ? row : 0);
-          for (int c = 0; c < sg.n_mma; c += 16) {
+          for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
             float v[16];
             tmem_ld_16(acc + c, v);
             tmem_ld_wait();
@@ -491,7 +507,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           }
         } else {
           uint16_t* ycol = sg.y + (row_ok ? row : 0);
-          for (int c = 0; c < sg.n_mma; c += 16) {
+          for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
             float v[16];
             tmem_ld_16(acc + c, v);
             tmem_ld_wait();
@@ -512,14 +528,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
           __threadfence();
           fence_proxy_async_global();
           if (!epi_sync()) break;
-          if (et == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
+          if (ect == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
         }
         continue;
       }
       // s of this tile's rows into shared memory (fp32, zero past the tile) while the
       // tensor core works on it
       if (!epi_sync()) break;   // every epilogue warp is done with the previous tile's s
-      for (int c = et; c < p.n_mma; c += 4 * 32) {
+      for (int c = ect; c < p.n_mma; c += kGemmEpiWarps * 32) {
         const int o = tc.row0 + c;
         sbuf[c] = (c < p.row_tile && o < sg.rows) ? (sg.s ? bf16_to_f32(sg.s[o]) : 1.0f) : 0.0f;
       }
@@ -528,12 +544,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
       tc_fence_after();
       if (has_lr) {
         // scale the W0 x accumulator by s in place; the MMA warp then adds U t
-        for (int c = 0; c < sg.n_mma; c += 16) {
+        for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
           float v[16];
           tmem_ld_16(acc + c, v);
           tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
+          scale16(v, sbuf + c);
           tmem_st_16(acc + c, v);
         }
         tmem_st_wait();
@@ -545,38 +560,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         tc_fence_after();
       }
       if (sg.tma_y) {
-        // 64-column chunks through this warp's two staging buffers (row = token, 128-byte
-        // swizzle), each written out by one bulk tensor store; the tensor map clips rows
-        // past M and columns past the family's rows
-        uint8_t* wst = ystage + static_cast<size_t>(q) * 2 * kYStageBytes;
+        // 64-column chunks (the two warps of a lane quadrant alternate) through this warp's
+        // staging buffer (row = token, 128-byte swizzle), each written out by one bulk tensor
+        // store; the tensor map clips rows past M and columns past the family's rows. A chunk
+        // is converted into registers before the wait for the previous store's read.
+        uint8_t* buf = ystage + static_cast<size_t>(warp - 2) * kYStageBytes;
+        uint8_t* row = buf + lane * 128;
         int nst = 0;
-        for (int c0 = 0; c0 < sg.n_mma; c0 += 64, ++nst) {
-          uint8_t* buf = wst + (nst & 1) * kYStageBytes;
-          if (nst >= 2 && lane == 0) tma_store_wait_read_but_one();   // this buffer's last store read it
-          __syncwarp();
-          uint8_t* row = buf + lane * 128;
+        for (int c0 = 64 * hw; c0 < sg.n_mma; c0 += 128, ++nst) {
+          uint32_t pk[32];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int c = c0 + q4 * 16;
             float v[16];
             tmem_ld_16(acc + c, v);
             tmem_ld_wait();
-            if (!has_lr) {
+            if (!has_lr) scale16(v, sbuf + c);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
-            }
-            uint4 w0, w1;
-            w0.x = pack_bf16x2(v[0], v[1]);
-            w0.y = pack_bf16x2(v[2], v[3]);
-            w0.z = pack_bf16x2(v[4], v[5]);
-            w0.w = pack_bf16x2(v[6], v[7]);
-            w1.x = pack_bf16x2(v[8], v[9]);
-            w1.y = pack_bf16x2(v[10], v[11]);
-            w1.z = pack_bf16x2(v[12], v[13]);
-            w1.w = pack_bf16x2(v[14], v[15]);
-            *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (lane & 7)) << 4)) = w0;
-            *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (lane & 7)) << 4)) = w1;
+            for (int e = 0; e < 8; ++e) pk[8 * q4 + e] = pack_bf16x2_cvt(v[2 * e], v[2 * e + 1]);
           }
+          if (nst > 0 && lane == 0) tma_store_wait_read_all();   // the previous chunk's store read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            *reinterpret_cast<uint4*>(row + ((h ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -597,7 +605,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         // split K: this slice's raw fp32 sums (no scale, no rank-r part), summed in order
         // and finished by the finalize kernel; ld_part and the columns are multiples of 4
         float* prow = sg.part + (static_cast<int64_t>(itm.ks) * p.M + (tok_ok ? tok : 0)) * sg.ld_part;
-        for (int c = 0; c < sg.n_mma; c += 16) {
+        for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
           float v[16];
           tmem_ld_16(acc + c, v);
           tmem_ld_wait();
@@ -623,7 +631,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         continue;
       }
       uint16_t* yrow = sg.y + static_cast<int64_t>(tok) * sg.ldy;
-      for (int c = 0; c < sg.n_mma; c += 16) {
+      for (int c = col_lo(sg.n_mma); c < col_hi(sg.n_mma); c += 16) {
         float v[16];
         tmem_ld_16(acc + c, v);
         tmem_ld_wait();
@@ -632,20 +640,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         if (!dbg_in_bounds(static_cast<int64_t>(tok) * sg.ldy + min(o0 + 15, sg.rows - 1), dbg_extent(p.M, sg.ldy, sg.rows),
                            p.status))
           continue;
-        if (!has_lr) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= sbuf[c + j];
-        }
+        if (!has_lr) scale16(v, sbuf + c);
         if ((c + 16 <= p.row_tile) && (o0 + 16 <= sg.rows)) {
           uint4 w0, w1;
-          w0.x = pack_bf16x2(v[0], v[1]);
-          w0.y = pack_bf16x2(v[2], v[3]);
-          w0.z = pack_bf16x2(v[4], v[5]);
-          w0.w = pack_bf16x2(v[6], v[7]);
-          w1.x = pack_bf16x2(v[8], v[9]);
-          w1.y = pack_bf16x2(v[10], v[11]);
-          w1.z = pack_bf16x2(v[12], v[13]);
-          w1.w = pack_bf16x2(v[14], v[15]);
+          w0.x = pack_bf16x2_cvt(v[0], v[1]);
+          w0.y = pack_bf16x2_cvt(v[2], v[3]);
+          w0.z = pack_bf16x2_cvt(v[4], v[5]);
+          w0.w = pack_bf16x2_cvt(v[6], v[7]);
+          w1.x = pack_bf16x2_cvt(v[8], v[9]);
+          w1.y = pack_bf16x2_cvt(v[10], v[11]);
+          w1.z = pack_bf16x2_cvt(v[12], v[13]);
+          w1.w = pack_bf16x2_cvt(v[14], v[15]);
           *reinterpret_cast<uint4*>(yrow + o0) = w0;
           *reinterpret_cast<uint4*>(yrow + o0 + 8) = w1;
         } else {
@@ -662,7 +667,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
         __threadfence();
         fence_proxy_async_global();
         if (!epi_sync()) break;
-        if (et == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
+        if (ect == 0) red_release_gpu_add(p.t_flags + 1 + tc.tok0 / p.tok_tile, 1);
       }
     }
     if (lane == 0) tma_store_wait_all();   // this warp's bulk stores of y are complete
@@ -847,7 +852,7 @@ __device__ __forceinline__ uint32_t nvfp4_block(const float* v, float inv6g, con
   }
   float q[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], inv);
+  for (int j = 0; j < 16; j += 2) fmul2_rn(q[j], q[j + 1], v[j], v[j + 1], inv, inv);
   *codes = make_uint2(f32x8_to_e2m1(q), f32x8_to_e2m1(q + 8));
   return sf;
 }
@@ -1165,8 +1170,16 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         uint32_t res[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float lo = fmaf(sc, __uint_as_float(ww[e] << 16), d[h * 8 + 2 * e]);
-          const float hi = fmaf(sc, __uint_as_float(ww[e] & 0xFFFF0000u), d[h * 8 + 2 * e + 1]);
+          // s * W0 + (U V^T), one rounding each; the quantising epilogues take two columns per
+          // instruction (measured: the bf16 store path is 1.5 % slower that way)
+          float lo, hi;
+          if (kOut == kPreBf16) {
+            lo = fmaf(sc, __uint_as_float(ww[e] << 16), d[h * 8 + 2 * e]);
+            hi = fmaf(sc, __uint_as_float(ww[e] & 0xFFFF0000u), d[h * 8 + 2 * e + 1]);
+          } else {
+            ffma2_rn(lo, hi, sc, sc, __uint_as_float(ww[e] << 16), __uint_as_float(ww[e] & 0xFFFF0000u),
+                     d[h * 8 + 2 * e], d[h * 8 + 2 * e + 1]);
+          }
           if (kOut == kPreBf16) {
             res[e] = pack_bf16x2(lo, hi);
           } else {

@@ -453,4 +453,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
 }
 
+// The same packing as one conversion instruction (nearest, ties to even; lo in the low half).
+// Measured: faster in the prefill GEMM's output pass, slower in the W_eff precompute epilogue.
+__device__ __forceinline__ uint32_t pack_bf16x2_cvt(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packed fp32 pairs (one instruction for two lanes; each lane rounded exactly as fmaf /
+// __fmul_rn): (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) and (a0 * b0, a1 * b1).
+__device__ __forceinline__ void ffma2_rn(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                         float c1) {
+  asm("{\n"
+      " .reg .b64 ra, rb, rc, rd;\n"
+      " mov.b64 ra, {%2, %3};\n"
+      " mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n"
+      " mov.b64 {%0, %1}, rd;\n"
+      "}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void fmul2_rn(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n"
+      " .reg .b64 ra, rb, rd;\n"
+      " mov.b64 ra, {%2, %3};\n"
+      " mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n"
+      " mov.b64 {%0, %1}, rd;\n"
+      "}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 }  // namespace aq
