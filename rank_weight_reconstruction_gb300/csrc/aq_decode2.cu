@@ -17,7 +17,9 @@
 //     t. They are added across the cluster through distributed shared memory, by stores only:
 //     each CTA sums its own partials (k-block groups, warps) and pushes, with 16-byte stores
 //     into the peers' shared memory, the W0 x sums of the rows peer q finishes (1/C of the
-//     cluster's rows) to q and its t to every peer. One cluster barrier publishes the pushes;
+//     cluster's rows) to q and its t to every peer (its own share by plain shared stores; the
+//     first push waits on a cluster barrier that every thread arrives on when it starts, so
+//     no peer is written before it runs). One cluster barrier publishes the pushes;
 //     every CTA then adds the C partials it received, in rank order. y = RN_bf16(s * z + U t)
 //     is formed in fp32 (U t on the FP32 pipes: r products per output) and rounded once.
 // Warp 0 feeds the TMA ring (one lane); warps 1..8 run mma.sync m16n8k16 (bf16 in, fp32
@@ -101,6 +103,13 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int kbox, int row, in
   return base + line * 128 + ((c ^ (line & 7)) << 4);
 }
 
+// The cluster's start barrier in two halves: every thread arrives (relaxed) when it starts and
+// waits before its first access to a peer's shared memory, by then long complete.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 }  // namespace
 
 // kStaged: x and V ride in every stage behind its W0 box (Dec2Params::staged), a separate
@@ -169,6 +178,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   // The next call may start now: its CTAs fit beside this one and stream their weights.
   pdl_launch_dependents();
   __syncthreads();
+  cluster_arrive_relaxed();
 
   bool ok = true;
   if (warp == 0) {
@@ -260,6 +270,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       }
     }
     __syncwarp();
+    cluster_wait();
   } else {
     // ---------------- mma warps ----------------
     const int cw = warp - 1;                 // 0..7
@@ -402,6 +413,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       }
     }
     cp_async_wait_all();
+    cluster_wait();   // every CTA of the cluster has started: its shared memory may be written
     // ---- partial sums into this CTA's ring (no stage is in use any more) ----
     cons_bar();
     float* zex = reinterpret_cast<float*>(ring);               // [kg][M][Rc]: rows fastest
@@ -456,7 +468,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
           if (rr + i < rf && row < rows_here)
             for (int k = 0; k < kg; ++k) v[i] += zex[k * grp + tok * Rc + row];
         }
-        st_dsmem_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
+        if (q == rank)   // this CTA's own rows: a plain shared store
+          *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(zrx) + static_cast<size_t>(rank * zn + e) * 4u) =
+              make_float4(v[0], v[1], v[2], v[3]);
+        else
+          st_dsmem_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
       // t: this CTA's sum over its eight warps, formed once and pushed to every peer
       for (int e = 4 * ct; e < tn; e += 4 * kDecConsumers) {
@@ -465,8 +481,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
         for (int w = 0; w < 8; ++w)
 #pragma unroll
           for (int i = 0; i < 4; ++i) v[i] += tex[static_cast<size_t>(w) * tn + e + i];
+        *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(zrx) + static_cast<size_t>(C * zn + rank * tn + e) * 4u) =
+            make_float4(v[0], v[1], v[2], v[3]);
         for (int q = 0; q < C; ++q)
-          st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
+          if (q != rank) st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
       }
     }
   }
