@@ -103,6 +103,44 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int kbox, int row, in
   return base + line * 128 + ((c ^ (line & 7)) << 4);
 }
 
+// Asynchronous 16-byte store into a peer's shared memory that completes `16 bytes` of the
+// transaction count of the peer's mbarrier (both shared::cluster addresses of that CTA).
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+               : "memory");
+}
+
+// Bounded wait on a phase that remote CTAs complete (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const AbortCtl& ctl) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 31u) == 31u) {
+      if (*reinterpret_cast<volatile int*>(ctl.abort_flag)) return false;
+      if (global_timer_ns() - t0 > ctl.timeout_ns) {
+        *reinterpret_cast<volatile int*>(ctl.abort_flag) = 1;
+        atomicExch(ctl.status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed_end() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 // The cluster's start barrier in two halves: every thread arrives (relaxed) when it starts and
 // waits before its first access to a peer's shared memory, by then long complete.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -122,7 +160,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
   uint64_t* empty = full + kMaxStages;
   uint64_t* xbar = empty + kMaxStages;
   uint64_t* vbar = xbar + 1;
-  int* abort_flag = reinterpret_cast<int*>(vbar + 1);
+  uint64_t* rbar = vbar + 1;   // the peers' pushes into this CTA (transaction bytes)
+  int* abort_flag = reinterpret_cast<int*>(rbar + 1);
   uint8_t* xs = smem + kHeaderBytes;                 // x slice: 3-D box {64, xkb, M}, swizzled
   uint8_t* xs2 = xs + p.x_bytes;                     // gated input: the second slice, same layout
   uint8_t* vs = xs2 + p.x2_bytes;                    // V slice: [kslice][vrow] bf16
@@ -166,8 +205,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
     }
     mbar_init(xbar, 1);
     mbar_init(vbar, 1);
+    mbar_init(rbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // every peer pushes the W0 x sums of this CTA's rows and its t here: (C - 1) (zn + tn) floats
+    mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(C - 1) * static_cast<uint32_t>((rf4 + r16) * M) * 4u);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&sg.tm_w);
@@ -472,7 +514,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
           *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(zrx) + static_cast<size_t>(rank * zn + e) * 4u) =
               make_float4(v[0], v[1], v[2], v[3]);
         else
-          st_dsmem_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
+          st_async_v4(mapa_u32(zr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3],
+                      mapa_u32(smem_u32(rbar), static_cast<uint32_t>(q)));
       }
       // t: this CTA's sum over its eight warps, formed once and pushed to every peer
       for (int e = 4 * ct; e < tn; e += 4 * kDecConsumers) {
@@ -484,16 +527,23 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
         *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(zrx) + static_cast<size_t>(C * zn + rank * tn + e) * 4u) =
             make_float4(v[0], v[1], v[2], v[3]);
         for (int q = 0; q < C; ++q)
-          if (q != rank) st_dsmem_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3]);
+          if (q != rank)
+            st_async_v4(mapa_u32(tr_me + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)), v[0], v[1], v[2], v[3],
+                        mapa_u32(smem_u32(rbar), static_cast<uint32_t>(q)));
       }
     }
   }
 
-  // ---- every push of the cluster is visible after this barrier; nothing remote follows it ----
-  cluster_sync_all();
-  ok = ok && !*reinterpret_cast<volatile int*>(abort_flag);
+  // The second cluster barrier phase: arrived once this thread's pushes are issued (the
+  // producer warp: once its copies are done), waited on at the very end, so no CTA leaves
+  // while a peer may still push into it.
+  cluster_arrive_relaxed_end();
   if (warp > 0) {
     const int ct = threadIdx.x - 32;
+    // the own pushes (plain stores) of every mma warp, then the peers' (their bytes on rbar)
+    cons_bar();
+    ok = __all_sync(0xffffffffu, mbar_wait_cluster(rbar, 0u, ctl)) != 0 && ok;
+    ok = ok && !*reinterpret_cast<volatile int*>(abort_flag);
     const int zn = rf4 * M, tn = r16 * M;
     const float* zr = zrx;
     const float* tr = zrx + static_cast<size_t>(C) * zn;
@@ -534,6 +584,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
       }
     }
   }
+  cluster_wait();
 }
 
 // h = RN_bf16(act(g) * u), in place of g: one thread per 8 elements (16-byte rows pieces).
