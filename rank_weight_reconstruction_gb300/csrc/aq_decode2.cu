@@ -19,9 +19,12 @@
 //     into the peers' shared memory, the W0 x sums of the rows peer q finishes (1/C of the
 //     cluster's rows) to q and its t to every peer (its own share by plain shared stores; the
 //     first push waits on a cluster barrier that every thread arrives on when it starts, so
-//     no peer is written before it runs). One cluster barrier publishes the pushes;
-//     every CTA then adds the C partials it received, in rank order. y = RN_bf16(s * z + U t)
-//     is formed in fp32 (U t on the FP32 pipes: r products per output) and rounded once.
+//     no peer is written before it runs). The remote pushes are asynchronous stores that count
+//     their bytes on the receiver's barrier, so a CTA starts its final phase as soon as its
+//     own inputs have landed; a second cluster barrier phase, arrived on after the pushes and
+//     waited on at exit, keeps every CTA alive while a peer may still push into it. Every CTA
+//     adds the C partials it received, in rank order. y = RN_bf16(s * z + U t) is formed in
+//     fp32 (U t on the FP32 pipes: r products per output) and rounded once.
 // Warp 0 feeds the TMA ring (one lane); warps 1..8 run mma.sync m16n8k16 (bf16 in, fp32
 // accumulate). Every wait on an mbarrier is bounded; a CTA whose wait expires records
 // AQ_ERR_TIMEOUT, skips the remaining work and still takes part in every barrier, so the
@@ -71,18 +74,6 @@ __device__ __forceinline__ uint32_t mapa_u32(uint32_t smem_addr, uint32_t rank) 
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
   return r;
-}
-
-// Store into a peer's shared memory (a shared::cluster address from mapa). No round trip: the
-// cluster barrier's release / acquire makes the stores visible to the peer.
-__device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
-}
-
-// 16-byte store into a peer's shared memory (16-byte aligned shared::cluster address).
-__device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 // The activations of the fused MLP, in fp32 with CUDA's tanhf / expf: the tanh approximation of
@@ -336,8 +327,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) aq_decode2_kernel(const __grid
     }
     cp_async_commit();
     // No dependency wait of their own: everything the mma warps read after this point came
-    // through the producer's copies issued after its wait, and their y stores follow the
-    // cluster barrier, which every CTA with work reaches only after that wait.
+    // through the producer's copies issued after its wait, and a CTA stores y only after its
+    // W0 loop, which cannot end before x (copied after that wait) has landed.
 
     const int nslab = (Rc + 15) / 16;
     const int kg = nslab >= 8 ? 1 : 8 / nslab;          // warps sharing one slab (split over k blocks)

@@ -324,8 +324,9 @@ cudaError_t gemm_max_clusters(size_t smem, int cluster, int* n);
 // Shared memory from which one aq_gemm_kernel CTA fills an SM (CTA pairs need that: the pair
 // count is taken at this size).
 constexpr size_t kGemmPairMinSmem = 120 * 1024;
-// k blocks of the next tile the MMA warp issues while the epilogue scales a tile by s (the
-// scale pass takes about as long as five 64-wide k blocks of a 256-wide tile)
+// k blocks of the next tile the MMA warp issues while the epilogue scales a tile by s (sized
+// when four epilogue warps took about five 64-wide k blocks of a 256-wide tile for the scale
+// pass; with eight it takes about half that, and the head is kept as measured)
 constexpr int kGemmHeadKb = 6;
 // Output staging of the prefill epilogue: per epilogue warp one buffer of 32 tokens x 64
 // columns of bf16 (128-byte swizzled rows), after the ring

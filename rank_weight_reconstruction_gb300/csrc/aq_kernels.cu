@@ -5,8 +5,9 @@
 // aq_gemm_kernel         prefill (M > 32): tcgen05 GEMM over the K = in loop with a TMA-fed
 //                        shared-memory ring, 128 tokens per tile as accumulator lanes and
 //                        output rows as N, two accumulator buffers so a tile's epilogue
-//                        overlaps the next tile's MMAs; the epilogue scales the W0 x sum by
-//                        s in TMEM, the rank-r up-projection is then added as extra K blocks
+//                        overlaps the next tile's MMAs; the epilogue (eight warps, two per
+//                        TMEM lane quadrant) scales the W0 x sum by s in TMEM, the rank-r
+//                        up-projection is then added as extra K blocks
 //                        into the same accumulator, and y is rounded once. t = x V runs as
 //                        the first tiles of the same launch (or, for very large M, as a
 //                        launch of its own). A CTA pair runs 2-SM MMAs (cta_group::2):
@@ -135,10 +136,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) aq_gemm_kernel(const __grid_c
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;   // [2] W0 loop of a tile done (MMA commit)
-  uint64_t* acc_scaled = acc_full + 2;       // [2] accumulator scaled by s (epilogue, 128)
+  uint64_t* acc_scaled = acc_full + 2;       // [2] accumulator scaled by s (one arrival per epilogue warp)
   uint64_t* acc_done = acc_scaled + 2;       // [2] rank-r blocks added (MMA commit)
-  uint64_t* acc_empty = acc_done + 2;        // [2] accumulator drained (epilogue, 128)
-  uint64_t* epi_bar = acc_empty + 2;         // epilogue warps' own barrier (128)
+  uint64_t* acc_empty = acc_done + 2;        // [2] accumulator drained (one arrival per epilogue warp)
+  uint64_t* epi_bar = acc_empty + 2;         // epilogue warps' own barrier (every epilogue thread)
   uint64_t* mma_done = epi_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
