@@ -267,7 +267,9 @@ aq_status aq_precompute_nvfp4(const aq_theta* th, void* q, int64_t ldq, void* sf
  * green context, some CTAs may not run until the waits of others expire: such a call ends
  * with AQ_ERR_TIMEOUT in the status word and undefined outputs, and reports nothing else.
  * Callers that share the GPU that way should poll aq_device_status() after a batch of
- * calls (it synchronises the stream) and recompute the batch when it reports a timeout. */
+ * calls (it synchronises the stream) and recompute the batch when it reports a timeout.
+ * The cluster decode kernel (M <= 16) is not subject to this: its CTAs wait only on the
+ * other CTAs of their thread-block cluster, which the hardware schedules together. */
 aq_status aq_device_status(void* stream);
 
 /* Test hook for the bounded-wait path: launches one block that waits on a barrier no
