@@ -57,3 +57,21 @@ def test_roofline_time_takes_the_larger_bound():
         t_star = max(B / hbm, F / pk)
         assert t_star == (B / hbm if M == 1 else F / pk)
     assert np.isclose(pk / hbm, 289.7, rtol=1e-3)   # the ridge, in flops per byte
+
+
+def test_committed_traffic_capture_matches_the_sources():
+    """The DRAM traffic the bench reports comes from profiles/dram_traffic.json only while the
+    kernel sources hash to the value recorded with it; the committed capture must describe the
+    committed sources and cover every decode call type of the step, each reading its operands
+    once (traffic within a few percent of the algorithmic bytes)."""
+    import json
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)
+    assert rec["source_hash"] == bench.kernel_source_hash()
+    for M in bench.DECODE_MS:
+        for kind in ("qkv", "o_proj", "gate_up", "down_proj"):
+            ent = rec["launches"][f"decode:{kind}:M{M}"]
+            assert ent["algorithmic_bytes"] == bench.call_bytes(kind, M)
+            assert 0.95 < ent["dram_bytes"] / ent["algorithmic_bytes"] < 1.05, (kind, M)
+            traffic, src = bench.captured_traffic(f"decode:{kind}:M{M}")
+            assert traffic == ent["dram_bytes"] and src.startswith("ncu capture")
