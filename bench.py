@@ -943,6 +943,113 @@ def run_sweep(args, dist: Dist):
             "copies_per_point": SWEEP_COPIES, "status": aq.aq_device_status(), "points": points}
 
 
+FP64_NOMINAL_TFLOPS = 1.25   # GB300 fp64 FMA rate, nominal (no measured figure exists for it)
+
+
+def mlp_bytes(M, r=DECODE_RANK):
+    """Algorithmic bytes of one fused MLP call over the step's gate, up and down families: the
+    three weight bundles (W0, U, V, s), x and y; the gated activation is the call's own."""
+    w = lambda o, i: 2 * (o * i + r * (o + i) + o)
+    g, u, d = FAMS["gate_proj"], FAMS["up_proj"], FAMS["down_proj"]
+    return w(*g) + w(*u) + w(*d) + 2 * M * g[1] + 2 * M * d[0]
+
+
+def rsvd_flops(m, n, k, q):
+    """fp64 flops of the randomized SVD's dense products: A Omega, then q rounds of A^T Q and
+    A Q', then Q^T A (each 2 m n k), the CholeskyQR2 Gram products (2 x 2 m k^2 per
+    orthonormalisation) and U = Q W (2 m k^2); the k x k eigen-solve is not counted."""
+    return 2 * m * n * k * (2 + 2 * q) + 4 * m * k * k * (2 + 2 * q) + 2 * m * k * k
+
+
+def run_extras(args, dist: Dist):
+    """The fused MLP and the decomposition, measured.
+
+    * aq_mlp (gate and up batched, the activation, down) for every layer of the Gemma-3-1B-shaped
+      stack at M = 1, 4, 16: a graph of 26 calls, each layer on its own W0 copies (L2-cold).
+    * The decomposition of one band of four Gemma-3-1B o_proj-shaped layers (1152 x 1024):
+      band mean, then per layer the stored scale with its fp64 residual and the randomized SVD
+      (r = 16, k = 24, q = 0 and 1), eager calls timed with CUDA events (the SVD synchronises
+      its stream)."""
+    import torch
+    import rank_weight_reconstruction_gb300 as aq
+    from rank_weight_reconstruction_gb300 import build_lib
+
+    if dist.rank != 0:
+        return None
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    aq.load()
+    pk = peaks()
+    stack = DecodeStack(device, copies=True, seed_tag="extras")
+    th0 = stack.layers[0]
+    ws_bytes = max(aq.aq_mlp_workspace_bytes(th0["gate_proj"], th0["up_proj"], th0["down_proj"], M) for M in DECODE_MS)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    mlp = {}
+    for M in DECODE_MS:
+        views = [(lay, xv, yv) for (m, lay, xv), yv in zip(stack.x_views, stack.y_views) if m == M]
+        call = lambda lay, xv, yv: aq.aq_mlp(stack.layers[lay]["gate_proj"], stack.layers[lay]["up_proj"],
+                                             stack.layers[lay]["down_proj"], xv["mlp"], y=yv["down_proj"],
+                                             workspace=ws)
+        for v in views:
+            call(*v)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        launches = 0
+        with torch.cuda.graph(g):
+            for v in views:
+                call(*v)
+                launches += aq.aq_last_launch_count()
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        us = time_graph(g, max(5, min(args.steps, 50))) * 1e3 / len(views)
+        del g
+        B = mlp_bytes(M)
+        mlp[f"M{M}"] = {"us_per_call": round(us, 3), "GB_s": round(B / us * 1e-3, 1),
+                        "frac_hbm": round(B / us * 1e-3 / pk["hbm_gbs"], 4), "launches_per_call": launches // len(views),
+                        "algorithmic_bytes": B}
+    status_mlp = aq.aq_device_status()
+    del stack
+    torch.cuda.empty_cache()
+
+    out, inp, L, r, k = 1152, 1024, 4, 16, 24
+    ws_host = [synth.make_w0(("extras", "band", l), out, inp) for l in range(L)]
+    weights = [dev_bits(w, device)[:, :inp] for w in ws_host]
+    omega = torch.from_numpy(synth.normal_f64(synth.stream_seed("extras", "omega"), inp * k).reshape(inp, k)).to(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    W0 = aq.aq_band_mean(weights)
+    t_band = timed(lambda: aq.aq_band_mean(weights, W0=W0))
+    s_, resid = aq.aq_ls_residual(weights[0], W0)
+    t_ls = timed(lambda: aq.aq_ls_residual(weights[0], W0, s=s_, resid=resid))
+    t_svd = {q: timed(lambda q=q: aq.aq_randomized_svd(resid, r, omega, power_iters=q)) for q in (0, 1)}
+    band_b = 2 * L * out * inp + 2 * out * inp
+    ls_b = out * inp * (2 + 2 + 8) + 2 * out
+    dec = {"workload": f"one band of {L} layers of {out}x{inp} (Gemma-3-1B o_proj shape), r={r}, k={k}",
+           "band_mean": {"ms": round(t_band, 4), "GB_s": round(band_b / t_band * 1e-6, 1),
+                         "frac_hbm": round(band_b / t_band * 1e-6 / pk["hbm_gbs"], 4)},
+           "ls_residual_per_layer": {"ms": round(t_ls, 4), "GB_s": round(ls_b / t_ls * 1e-6, 1),
+                                     "frac_hbm": round(ls_b / t_ls * 1e-6 / pk["hbm_gbs"], 4)},
+           "randomized_svd_per_layer": {f"q{q}": {"ms": round(t, 4), "fp64_TFLOP_s": round(rsvd_flops(out, inp, k, q) / t * 1e-9, 3),
+                                                  "frac_fp64_nominal": round(rsvd_flops(out, inp, k, q) / t * 1e-9 / FP64_NOMINAL_TFLOPS, 4)}
+                                        for q, t in t_svd.items()},
+           "band_total_ms_q1": round(t_band + L * (t_ls + t_svd[1]), 3)}
+    return {"extras": "fused MLP over the decode stack and the GPU decomposition of one band", "peaks": pk,
+            "fp64_peak_tflops": {"value": FP64_NOMINAL_TFLOPS, "source": "nominal"},
+            "mlp": mlp, "decomposition": dec, "status": [status_mlp, aq.aq_device_status()]}
+
+
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
@@ -978,6 +1085,8 @@ def main():
                     help="run only the captured decode step (for kernel-profiler launch lists)")
     ap.add_argument("--sweep", action="store_true",
                     help="the rank/shape sweep (gate-like and down-like, r in 0..256, M in 1..4096)")
+    ap.add_argument("--extras", action="store_true",
+                    help="the fused MLP over the decode stack and the GPU decomposition of one band")
     ap.add_argument("--path", choices=["auto", "decode", "midm", "prefill"], default="auto",
                     help="--sweep / --case: force one path (aq_set_path) to map where the paths cross")
     ap.add_argument("--case", default=None,
@@ -993,6 +1102,8 @@ def main():
         res = run_case(args, dist)
     elif args.sweep:
         res = run_sweep(args, dist)
+    elif args.extras:
+        res = run_extras(args, dist)
     else:
         res = run_ours(args, dist)
     if dist.rank == 0 and res is not None:

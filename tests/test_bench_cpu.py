@@ -75,3 +75,16 @@ def test_committed_traffic_capture_matches_the_sources():
             assert 0.95 < ent["dram_bytes"] / ent["algorithmic_bytes"] < 1.05, (kind, M)
             traffic, src = bench.captured_traffic(f"decode:{kind}:M{M}")
             assert traffic == ent["dram_bytes"] and src.startswith("ncu capture")
+
+
+def test_mlp_and_decomposition_accounting_by_hand():
+    r, M = 16, 4
+    (go, gi), (uo, ui), (do, di) = (bench.FAMS[f] for f in ("gate_proj", "up_proj", "down_proj"))
+    weights = sum(2 * (o * i + r * (o + i) + o) for o, i in ((go, gi), (uo, ui), (do, di)))
+    assert bench.mlp_bytes(M) == weights + 2 * M * gi + 2 * M * do
+    # the fused MLP moves what the step's gate/up and down calls move, less the intermediates
+    assert bench.mlp_bytes(M) == (bench.gate_up_bytes(r, M) + bench.linear_bytes(do, di, r, M)
+                                  - 2 * M * (go + uo) - 2 * M * di)
+    m, n, k = 1152, 1024, 24
+    assert bench.rsvd_flops(m, n, k, 0) == 2 * (2 * m * n * k) + 2 * (4 * m * k * k) + 2 * m * k * k
+    assert bench.rsvd_flops(m, n, k, 1) - bench.rsvd_flops(m, n, k, 0) == 2 * (2 * m * n * k + 4 * m * k * k)
