@@ -201,3 +201,34 @@ def test_selftest_argument_check(lib):
     # r = 0: no t tiles to wait for
     assert lib.aq_selftest_prefill_timeout(ctypes.byref(th), 0x3000, 4, 64, 0x4000, 64, 0x5000, 1 << 20, 1000,
                                            None) == binding.AQ_ERR_INVALID_ARG
+
+
+def _mlp_thetas(inter=256, inp=128, out=128, r=4, down_in=None):
+    def th(o, i, W0):
+        return binding.c_theta(W0=W0, s=W0 + 0x100000, U=W0 + 0x200000, V=W0 + 0x300000, ld_w0=i, ld_u=8, ld_v=8,
+                               out=o, in_=i, r=r)
+    return th(inter, inp, 0x1000000), th(inter, inp, 0x2000000), th(out, down_in or inter, 0x3000000)
+
+
+def _mlp(lib, g, u, d, act=binding.AQ_ACT_GELU_TANH, x=0x4000000, M=2, ldx=128, y=0x5000000, ldy=128,
+         ws=0x6000000, ws_bytes=1 << 20):
+    return lib.aq_mlp(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), act, x, M, ldx, y, ldy, ws, ws_bytes, None)
+
+
+def test_mlp_validation(lib):
+    """aq_mlp refuses bad calls before any device work: the families' shapes must chain
+    (gate and up [inter, in], down [out, inter]), the activation must be known, and the
+    workspace must hold g and u besides the projections' own scratch."""
+    g, u, d = _mlp_thetas()
+    assert _mlp(lib, *_mlp_thetas(down_in=200)) == binding.AQ_ERR_SHAPE
+    assert "down.in" in binding.aq_last_error()
+    g2, _, _ = _mlp_thetas(inp=64)
+    assert _mlp(lib, g2, u, d) == binding.AQ_ERR_SHAPE
+    assert _mlp(lib, g, u, d, act=9) == binding.AQ_ERR_INVALID_ARG
+    assert "activation" in binding.aq_last_error()
+    need = lib.aq_mlp_workspace_bytes(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), 2)
+    # g and u in bf16 at least, plus what the projections need
+    assert need >= 2 * 2 * 256 * 2
+    assert need > lib.aq_mlp_workspace_bytes(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), 1)
+    assert _mlp(lib, g, u, d, ws_bytes=need - 256) == binding.AQ_ERR_WORKSPACE
+    assert _mlp(lib, g, u, d, x=0) == binding.AQ_ERR_INVALID_ARG
